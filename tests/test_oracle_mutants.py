@@ -1,0 +1,69 @@
+"""Plant plausible slips in the oracle (on the CPU) and check a pin catches each.
+
+Each mutant is the oracle's C source with one textual change, compiled into a
+temporary library.  The pins of ``test_oracle_pins.py`` are rerun against it;
+at least one must fail.  This shows the pins constrain every part of the
+oracle: the scale, the causal index, the operands, the normalisation, the
+LSE's log base and shift, the rescale direction of the recurrence, its causal
+loop bound, and the bf16/fp16 decoders.  No mutant indexes outside its arrays.
+"""
+from __future__ import annotations
+
+import os
+
+import pytest
+
+import oracle
+from oracle.build import SRC, build
+from test_oracle_pins import PINS
+
+MUTANTS = {
+    "drop_scale": ("        x[j] = s * dot;", "        x[j] = dot;"),
+    "ignore_causal": ("long nvis = causal ? i + 1 : N;     /* |J|", "long nvis = causal ? N : N;     /* |J|"),
+    "causal_off_by_one": ("long nvis = causal ? i + 1 : N;     /* |J|", "long nvis = causal ? i + (i == 0) : N;     /* |J|"),
+    "wrong_key_index": ("dot += q[d] * Kh[j * D + d];", "dot += q[d] * Kh[(N - 1 - j) * D + d];"),
+    "k_instead_of_v": ("o[d] += w * Vh[j * D + d];", "o[d] += w * Kh[j * D + d];"),
+    "no_normalisation": ("        o[d] /= l;", "        o[d] /= 1.0;"),
+    "lse_log2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
+    "lse_no_shift": ("*lse = m + log(l);", "*lse = log(l);"),
+    "exp_sign": ("double w = exp(x[j] - m);", "double w = exp(m - x[j]);"),
+    "probs_unnormalised": ("            P[i * N + j] /= l;", "            P[i * N + j] /= 1.0;"),
+    "tiled_inverse_rescale": ("double alpha = exp(m[r] - shift);", "double alpha = exp(shift - m[r]);"),
+    "tiled_no_acc_rescale": ("acc[r * D + d] = alpha * acc[r * D + d] + pv;", "acc[r * D + d] = acc[r * D + d] + pv;"),
+    "tiled_skips_diagonal": ("hi = (q0 + BM < N) ? q0 + BM : N;", "hi = q0;"),
+    "tiled_no_key_mask": ("if (kj >= N || (causal && kj > qi)) {", "if (kj >= N) {"),
+    "bf16_shift": ("uint32_t u = ((uint32_t)h) << 16;", "uint32_t u = ((uint32_t)h) << 15;"),
+    "fp16_bias": ("v = ldexp((double)(f + 1024), e - 25);", "v = ldexp((double)(f + 1024), e - 24);"),
+}
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, source, tmp_path):
+    old, new = MUTANTS[name]
+    assert source.count(old) >= 1, f"mutation site for {name} not found in the oracle source"
+    src = tmp_path / f"mut_{name}.c"
+    src.write_text(source.replace(old, new, 1))
+    so = build(str(src), str(tmp_path / f"mut_{name}.so"))
+    lib = oracle._load(so)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except Exception as e:  # an assertion, or a NaN that breaks a closed form
+            caught.append(f"{pin.__name__}: {type(e).__name__}")
+    assert caught, f"mutant {name} passed every pin"
+
+
+def test_unmutated_source_passes_all_pins(source, tmp_path):
+    """Control: the same build route with no change passes every pin."""
+    src = tmp_path / "same.c"
+    src.write_text(source)
+    lib = oracle._load(build(str(src), str(tmp_path / "same.so")))
+    for pin in PINS:
+        pin(lib)

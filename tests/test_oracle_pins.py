@@ -1,0 +1,294 @@
+"""Pins for the fp64 oracle (CPU only).
+
+Each test ties the oracle to something other than itself: a closed form, an
+invariant the pages state, an independent library routine (PyTorch's fp64 CPU
+scaled-dot-product attention, scipy's softmax, torch's dtype conversion), a
+brute-force equivalence on tiny inputs, or a figure the pages print.  The
+pins are chosen so that a plausible slip anywhere in the oracle (a dropped
+scale, a wrong causal index, V swapped for K, a missing normalisation, an
+inverted rescale, log2 for ln) fails at least one of them;
+``test_oracle_mutants.py`` plants such slips and checks exactly that.
+
+Every test takes the oracle library handle as a parameter so the mutant test
+can rerun them against a deliberately broken build.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# Every scale used below is exactly representable in float32: the oracle, like
+# the library, takes the softmax scale as a float32 value.
+
+def _rand(shape, seed, scale=1.0):
+    g = np.random.default_rng(seed)
+    return g.standard_normal(shape) * scale
+
+
+# ---------------------------------------------------------------------------
+# Individual pins (each a plain function of the library handle)
+# ---------------------------------------------------------------------------
+
+def pin_decode(lib):
+    """bf16/fp16 decoding equals torch's exact widening, for every bit pattern."""
+    bits = np.arange(65536, dtype=np.uint16)
+    for name, tdt in (("bf16", torch.bfloat16), ("fp16", torch.float16)):
+        ours = oracle.decode(bits, name, lib=lib)
+        ref = torch.from_numpy(bits.view(np.int16).copy()).view(tdt).to(torch.float64).numpy()
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(ours), nan), name
+        assert np.array_equal(ours[~nan], ref[~nan]), name
+
+
+def pin_rows_sum_to_one(lib):
+    """Each row of softmax(S) sums to 1; masked entries (j > i under causal) are 0.
+
+    "Triton: FlashAttention-2 Forward Pass", Verification checklist / Bugs
+    found: check that each softmax row sums to 1."""
+    for causal in (False, True):
+        for N, D in ((1, 1), (5, 3), (17, 8)):
+            q, k = _rand((N, D), 1), _rand((N, D), 2)
+            P = oracle.probs(q, k, causal, 0.6875, lib=lib)
+            assert np.all(P >= 0.0)
+            assert np.allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+            if causal:
+                assert np.all(P[np.triu_indices(N, 1)] == 0.0)
+
+
+def pin_probs_vs_scipy(lib):
+    """softmax(S) equals scipy.special.softmax of the scaled scores with a -inf causal mask."""
+    from scipy.special import softmax
+    for causal in (False, True):
+        q, k = _rand((9, 6), 3), _rand((9, 6), 4)
+        s = 0.375
+        S = s * (q @ k.T)
+        if causal:
+            S = np.where(np.triu(np.ones((9, 9), bool), 1), -np.inf, S)
+        ref = softmax(S, axis=1)
+        P = oracle.probs(q, k, causal, s, lib=lib)
+        assert np.allclose(P, ref, rtol=0, atol=1e-14)
+
+
+def pin_constant_v(lib):
+    """Constant V gives constant O: O is a convex combination of V rows.
+
+    "A09 - Advanced Triton & FlashAttention", 3. Deep Dive: acc / l is
+    softmax(s) @ V, an exact identity."""
+    for causal in (False, True):
+        q, k = _rand((2, 13, 5), 5), _rand((2, 13, 5), 6)
+        v = np.full((2, 13, 5), 0.0)
+        v[..., :] = np.array([1.5, -2.0, 0.25, 3.0, -0.125])
+        O, _ = oracle.forward(q, k, v, causal, 0.875, lib=lib)
+        assert np.allclose(O, v, rtol=0, atol=1e-14)
+
+
+def pin_identical_keys(lib):
+    """All keys equal: uniform weights, O = mean of the visible V rows and
+    LSE = x + log|J| with x the common scaled score (closed form)."""
+    N, D = 11, 4
+    q = _rand((N, D), 7)
+    k = np.tile(_rand((1, D), 8), (N, 1))
+    v = _rand((N, D), 9)
+    s = 0.625
+    for causal in (False, True):
+        O, L = oracle.forward(q, k, v, causal, s, lib=lib)
+        x = s * (q @ k[0])
+        for i in range(N):
+            n = i + 1 if causal else N
+            assert np.allclose(O[i], v[:n].mean(axis=0), rtol=0, atol=1e-14)
+            assert abs(L[i] - (x[i] + math.log(n))) < 1e-13
+
+
+def pin_zero_query(lib):
+    """Q = 0 makes every score 0: O = mean of visible V, LSE = log|J|."""
+    N, D = 9, 3
+    q = np.zeros((N, D))
+    k, v = _rand((N, D), 10), _rand((N, D), 11)
+    for causal in (False, True):
+        O, L = oracle.forward(q, k, v, causal, 1.25, lib=lib)
+        for i in range(N):
+            n = i + 1 if causal else N
+            assert np.allclose(O[i], v[:n].mean(axis=0), rtol=0, atol=1e-14)
+            assert abs(L[i] - math.log(n)) < 1e-14
+
+
+def pin_causal_row0(lib):
+    """Under the causal mask row 0 sees only key 0: O[0] = V[0], LSE[0] = s q0.k0."""
+    q, k, v = _rand((3, 7, 6), 12), _rand((3, 7, 6), 13), _rand((3, 7, 6), 14)
+    s = 0.4375
+    O, L = oracle.forward(q, k, v, True, s, lib=lib)
+    assert np.array_equal(O[:, 0], v[:, 0])
+    assert np.allclose(L[:, 0], s * np.einsum("bd,bd->b", q[:, 0], k[:, 0]), rtol=0, atol=1e-14)
+
+
+def pin_one_hot(lib):
+    """One key whose score leads all others by > 60 takes all the weight: O = that V row."""
+    N, D = 8, 4
+    q = np.zeros((N, D)); q[:, 0] = 10.0
+    k = _rand((N, D), 15) * 0.1
+    k[5, 0] = 10.0            # score of key 5 is ~ 100 * s higher than the others
+    v = _rand((N, D), 16)
+    O, L = oracle.forward(q, k, v, False, 1.0, lib=lib)
+    assert np.allclose(O, np.tile(v[5], (N, 1)), rtol=0, atol=1e-20 + 1e-15)
+    assert np.allclose(L, q @ k[5], rtol=0, atol=1e-12)
+
+
+def pin_vs_torch_sdpa(lib):
+    """Full forward equals PyTorch's fp64 CPU scaled_dot_product_attention (an
+    independent implementation), and LSE equals torch.logsumexp of the masked
+    scaled scores."""
+    for causal in (False, True):
+        for (B, H, N, D, s) in ((2, 3, 37, 16, 0.25), (1, 2, 130, 64, 1.0 / 8)):
+            q = torch.from_numpy(_rand((B, H, N, D), 17))
+            k = torch.from_numpy(_rand((B, H, N, D), 18))
+            v = torch.from_numpy(_rand((B, H, N, D), 19))
+            ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=s)
+            S = s * (q @ k.transpose(-1, -2))
+            if causal:
+                S = S.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+            lse_ref = torch.logsumexp(S, dim=-1)
+            O, L = oracle.forward(q, k, v, causal, s, lib=lib)
+            assert np.allclose(O, ref.numpy(), rtol=0, atol=1e-13)
+            assert np.allclose(L, lse_ref.numpy(), rtol=0, atol=1e-12)
+
+
+def pin_tiled_equals_explicit(lib):
+    """The tiled online-softmax recurrence equals the explicit softmax on
+    brute-force tiny inputs: ragged tails, BM != BN, one key, causal skip.
+
+    "Building a Verifiable FlashAttention Forward from PyTorch to Triton",
+    Part 2 (tiled PyTorch validates the recurrence) and Part 4 (lengths 127,
+    128, 129); "Triton: FlashAttention-2 Forward Pass", Verification checklist."""
+    seed = 20
+    for N in (1, 2, 3, 15, 16, 17, 37, 53):
+        for D in (1, 4, 64):
+            q, k, v = _rand((2, N, D), seed), _rand((2, N, D), seed + 1), _rand((2, N, D), seed + 2)
+            seed += 3
+            for causal in (False, True):
+                O_ref, L_ref = oracle.forward(q, k, v, causal, 0.5, lib=lib)
+                for BM, BN in ((16, 16), (16, 32), (32, 16), (7, 5), (64, 64), (1, 3)):
+                    O, L = oracle.tiled(q, k, v, causal, 0.5, BM, BN, lib=lib)
+                    assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+                    assert np.max(np.abs(O - O_ref)) <= 1e-12, (N, D, causal, BM, BN)
+                    assert np.max(np.abs(L - L_ref)) <= 1e-12, (N, D, causal, BM, BN)
+
+
+def pin_unbalanced_magnitudes(lib):
+    """Keys scaled up tile by tile so every new tile raises the running max: a
+    missing or inverted rescale shows up.  ("A09 - Advanced Triton &
+    FlashAttention", pitfalls: unbalanced magnitudes expose a missing rescale.)"""
+    N, D, BN = 64, 8, 8
+    q = _rand((N, D), 40)
+    k = _rand((N, D), 41)
+    for t in range(N // BN):
+        k[t * BN:(t + 1) * BN] *= 1.0 + 2.0 * t
+    v = _rand((N, D), 42)
+    for causal in (False, True):
+        O_ref, L_ref = oracle.forward(q, k, v, causal, 0.5, lib=lib)
+        O, L = oracle.tiled(q, k, v, causal, 0.5, 16, BN, lib=lib)
+        assert np.max(np.abs(O - O_ref)) <= 1e-12
+        assert np.max(np.abs(L - L_ref)) <= 1e-11
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), is_causal=causal, scale=0.5)
+        assert np.allclose(O_ref, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def pin_first_step_rescale(lib):
+    """m_old = -inf on the first tile gives alpha = exp(-inf) = 0, not NaN
+    ("FlashAttention 2 from PyTorch to Triton", Step 1 notes; "Triton:
+    FlashAttention-2 Forward Pass", rescale direction): a single key tile of a
+    single key reproduces the key's V row exactly."""
+    q, k, v = _rand((1, 1, 5), 43), _rand((1, 1, 5), 44), _rand((1, 1, 5), 45)
+    for causal in (False, True):
+        O, L = oracle.tiled(q, k, v, causal, 0.3125, 1, 1, lib=lib)
+        assert np.array_equal(O, v)
+        assert abs(L[0, 0] - 0.3125 * float(q[0, 0] @ k[0, 0])) < 1e-15
+
+
+PINS = [pin_decode, pin_rows_sum_to_one, pin_probs_vs_scipy, pin_constant_v, pin_identical_keys,
+        pin_zero_query, pin_causal_row0, pin_one_hot, pin_vs_torch_sdpa, pin_tiled_equals_explicit,
+        pin_unbalanced_magnitudes, pin_first_step_rescale]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin, oracle_lib):
+    pin(oracle_lib)
+
+
+# ---------------------------------------------------------------------------
+# Consistency of the entry points with each other on low-precision inputs
+# ---------------------------------------------------------------------------
+
+def test_bf16_inputs_are_decoded_exactly(oracle_lib):
+    """Forward on bf16 tensors equals forward on the same values widened to fp64 (bit for bit)."""
+    from exact_attention_10_gb300.inputs import make_custom
+    q, k, v = make_custom(1, 2, 40, 16, "bf16", seed=3)
+    O1, L1 = oracle.forward(q, k, v, True, 0.25, lib=oracle_lib)
+    O2, L2 = oracle.forward(q.double(), k.double(), v.double(), True, 0.25, lib=oracle_lib)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+def test_rows_equal_forward(oracle_lib):
+    """A sampled row is exactly the row of the full forward (rows are independent)."""
+    from exact_attention_10_gb300.inputs import make_custom
+    q, k, v = make_custom(2, 2, 77, 32, "fp16", seed=4, qk_gain=4.0)
+    for causal in (False, True):
+        O, L = oracle.forward(q, k, v, causal, 0.1875, lib=oracle_lib)
+        bh = np.array([0, 0, 1, 2, 3, 3])
+        ri = np.array([0, 76, 5, 40, 1, 76])
+        Or, Lr = oracle.rows(q, k, v, causal, 0.1875, bh, ri, lib=oracle_lib)
+        Of, Lf = O.reshape(4, 77, 32), L.reshape(4, 77)
+        assert np.array_equal(Or, Of[bh, ri]) and np.array_equal(Lr, Lf[bh, ri])
+
+
+def test_rows_rejects_bad_indices(oracle_lib):
+    q = torch.zeros(1, 2, 4, 2, dtype=torch.float64)
+    with pytest.raises(ValueError):
+        oracle.rows(q, q, q, False, 1.0, [0], [4], lib=oracle_lib)      # row out of range
+    with pytest.raises(ValueError):
+        oracle.rows(q, q, q, False, 1.0, [1, 0], [0, 1], lib=oracle_lib)  # heads not non-decreasing
+
+
+# ---------------------------------------------------------------------------
+# A figure the pages print
+# ---------------------------------------------------------------------------
+
+def _golden(name):
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", name)
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, val = line.split("=", 1)
+                vals[key.strip()] = val.strip()
+    return vals
+
+
+@pytest.mark.slow
+def test_bf16_output_rounding_floor_matches_page(oracle_lib):
+    """At B*H = 32, N = 4096, D = 64, bf16 N(0,1) inputs, non-causal, scale 1/8,
+    rounding the exact output to bf16 costs a mean absolute error of 2.9e-5
+    ("How to profile and optimise kernels", the P cast section).  The oracle's
+    exact output, rounded to bf16, must show that figure: a dropped scale or a
+    wrong normalisation changes the output magnitudes and moves it."""
+    g = _golden("bf16_rounding_floor.txt")
+    from exact_attention_10_gb300.inputs import WORKLOADS, make_qkv
+    w = WORKLOADS["b2h16_n4096"]
+    q, k, v = make_qkv(w, seed=0)
+    heads = int(g["heads_sampled"])
+    qs, ks, vs = (x.reshape(32, w.N, w.D)[:heads] for x in (q, k, v))
+    O, _ = oracle.forward(qs, ks, vs, False, w.scale, lib=oracle_lib)
+    Ob = torch.from_numpy(O).to(torch.bfloat16).to(torch.float64).numpy()
+    mean_err = float(np.mean(np.abs(Ob - O)))
+    lo, hi = float(g["accept_low"]), float(g["accept_high"])
+    assert lo <= mean_err <= hi, mean_err
