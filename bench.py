@@ -1,0 +1,372 @@
+"""Benchmark of the attention forward (one JSON line on stdout).
+
+A step is one pass of the whole forward hot path over one batch of synthetic
+input: one non-causal and one causal fa_fwd call on the N = 4096 comparison
+workload of the pages (B=2, H=16, N=4096, D=64, bf16, scale 1/8).  ``value``
+is the pages' FLOP count (4*B*H*N^2*D non-causal, half causal) of all steps of
+all ranks divided by the summed device time of the calls, in TFLOP/s; each
+call is bracketed by CUDA events on the stream it is launched on, and L2 is
+flushed (a 256 MiB write) between calls, outside the events.
+
+Other keys: ``e2e`` (same metric through the C ABI with pinned host buffers,
+host->device and device->host copies inside the timed region), ``roofline``
+(the non-causal kernel against the measured bf16 tensor peak), ``clocks``
+(nvidia-smi samples taken during the timed region), ``cpu_baseline`` (the fp64
+CPU oracle on a bounded sample, timed on this host's cores).
+
+``--impl reference`` times the CPU oracle as the reference arm on the same
+metric.  Under torchrun every rank runs its own replica of the workload (weak
+scaling, no data-path collective); ranks only meet at the timing barriers.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s and ms/call on 1 GB300 (causal & non-causal), % of tensor peak"
+DEFAULT_WORKLOAD = "b2h16_n4096"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 1 <= r[0] <= (self.t1 or r[0]) + 1]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use)}
+
+
+def _traffic_record(kernel_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (matched by content hash); otherwise None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for rel in ("exact_attention_10_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_10_gb300/csrc/sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    entry = rec.get(kernel_name)
+    if not entry or entry.get("source_sha256") != h.hexdigest():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def cpu_oracle_sample(w, budget_s: float, rows_per_head: int | None = None):
+    """Time the fp64 oracle on sampled rows of the workload, both masks.
+
+    Rows are spread evenly over [0, N) so a causal sample has the average row
+    cost.  Returns (TFLOP/s in the pages' convention, description, threads)."""
+    import numpy as np
+    import oracle
+    from exact_attention_10_gb300.accounting import flops
+    from exact_attention_10_gb300.inputs import make_qkv
+    q, k, v = make_qkv(w, seed=0)
+    BH = w.B * w.H
+    per_row = {c: flops(1, 1, w.N, w.D, c) / w.N for c in (False, True)}
+    rows = rows_per_head or max(1, min(w.N, 64))
+    done_flops, spent, heads = 0.0, 0.0, 0
+    while spent < budget_s and heads < BH:
+        bh = np.full(rows, heads, dtype=np.int64)
+        ri = np.linspace(0, w.N - 1, rows).round().astype(np.int64)
+        for causal in (False, True):
+            t = time.perf_counter()
+            oracle.rows(q, k, v, causal, w.scale, bh, ri)
+            spent += time.perf_counter() - t
+            done_flops += per_row[causal] * rows
+        heads += 1
+    desc = (f"{heads} head(s) x {rows} rows spread over [0, N), non-causal and causal, of {w.describe()}; "
+            f"{spent:.1f} s of CPU time")
+    return done_flops / spent / 1e12, desc, oracle.num_threads(), spent
+
+
+def run_reference(args, w):
+    """Reference arm: the fp64 CPU oracle, timed as it stands."""
+    rank, world, _ = _dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from exact_attention_10_gb300.accounting import flops
+    from exact_attention_10_gb300.inputs import make_qkv
+    q, k, v = make_qkv(w, seed=0)
+    # size each step so warmup + steps take about a minute on this host
+    probe_rows = 32
+    ri = np.linspace(0, w.N - 1, probe_rows).round().astype(np.int64)
+    t = time.perf_counter()
+    for causal in (False, True):
+        oracle.rows(q, k, v, causal, w.scale, np.zeros(probe_rows, dtype=np.int64), ri)
+    per_row_s = (time.perf_counter() - t) / probe_rows
+    target = 60.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(w.N, target / max(per_row_s, 1e-9))))
+    BH = w.B * w.H
+    per_row = {c: flops(1, 1, w.N, w.D, c) / w.N for c in (False, True)}
+
+    def step(i):
+        bh = np.full(rows, i % BH, dtype=np.int64)
+        ri = np.linspace(0, w.N - 1, rows).round().astype(np.int64)
+        for causal in (False, True):
+            oracle.rows(q, k, v, causal, w.scale, bh, ri)
+
+    for i in range(args.warmup):
+        step(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t
+    fl = args.steps * rows * (per_row[False] + per_row[True])
+    value = fl / dt / 1e12
+    sample = (f"each step: {rows} query rows of one head (rows spread over [0, N)), non-causal and causal, "
+              f"of {w.describe()}")
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.describe() + ", causal + non-causal per step", "B": w.B, "H": w.H,
+                       "N": w.N, "D": w.D, "parallelism": "rank 0 only (CPU)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    args = ap.parse_args(argv)
+
+    from exact_attention_10_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    import torch
+    from exact_attention_10_gb300 import fa
+    from exact_attention_10_gb300.accounting import flops
+    from exact_attention_10_gb300.inputs import make_qkv
+
+    rank, world, local = _dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load()
+
+    q_h, k_h, v_h = make_qkv(w, seed=0)
+    q, k, v = (x.to(dev) for x in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    modes = (False, True)
+    F = {c: flops(w.B, w.H, w.N, w.D, c) for c in modes}
+    code = fa.FA_BF16 if w.dtype == "bf16" else fa.FA_FP16
+
+    def call(causal):
+        rc = fa.fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, w.N,
+                        w.D, int(causal), w.scale, code, sp)
+        if rc != 0:
+            raise fa.FAError(rc, "fa_fwd")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    for _ in range(args.warmup):
+        for c in modes:
+            flush.zero_()
+            call(c)
+    rc = fa.sync_status(sp)
+    if rc != 0:
+        raise fa.FAError(rc, "warm-up")
+
+    starts = {c: [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] for c in modes}
+    ends = {c: [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] for c in modes}
+    barrier()
+    clocks.mark_start()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        for c in modes:
+            flush.zero_()
+            starts[c][i].record(stream)
+            call(c)
+            ends[c][i].record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clocks.mark_end()
+    rc = fa.sync_status(sp)
+    if rc != 0:
+        raise fa.FAError(rc, "timed region")
+    ms = {c: [s.elapsed_time(e) for s, e in zip(starts[c], ends[c])] for c in modes}
+    total_ms = sum(sum(v) for v in ms.values())
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps * (F[False] + F[True]) / (total_ms * 1e-3) / 1e12
+    clk = clocks.finish()
+
+    # end to end through the C ABI: pinned host inputs in, O and LSE back out, every step
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    qp, kp, vp = (x.pin_memory() for x in (q_h, k_h, v_h))
+    op = torch.empty(q_h.shape, dtype=q_h.dtype).pin_memory()
+    lp = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp))
+    d2h = len(modes) * (op.numel() * op.element_size() + lp.numel() * lp.element_size())
+
+    def e2e_step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        for c in modes:
+            call(c)
+            op.copy_(o, non_blocking=True)
+            lp.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * e2e_steps * (F[False] + F[True]) / (e2e_ms * 1e-3) / 1e12
+
+    peak, peak_sus, _, peak_src = _peaks()
+    mode_info = {}
+    for c in modes:
+        avg = statistics.mean(ms[c])
+        tf = F[c] / (avg * 1e-3) / 1e12
+        mode_info["causal" if c else "noncausal"] = {
+            "ms_mean": avg, "ms_median": statistics.median(ms[c]), "tflops": tf,
+            "frac_of_measured_peak": tf / peak, "flops_per_call": F[c]}
+    nc = mode_info["noncausal"]
+    kernel_name = f"fa_fwd_sm103<{w.D},{'bf16' if w.dtype == 'bf16' else 'fp16'},noncausal>"
+    roofline = {"bound": "tensor", "achieved": nc["tflops"], "peak": peak, "unit": "TFLOP/s",
+                "frac": nc["tflops"] / peak, "traffic": _traffic_record(kernel_name),
+                "kernel": kernel_name, "peak_source": f"bf16_tflops (burst, {peak_src})",
+                "frac_of_sustained": nc["tflops"] / peak_sus}
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.describe() + ", one non-causal + one causal call per step", "B": w.B,
+                       "H": w.H, "N": w.N, "D": w.D, "l2": "flushed between timed calls (256 MiB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "modes": mode_info, "roofline": roofline,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
+            "clocks": clk, "gpu_launches": args.steps * len(modes), "wall_s_timed_region": wall}
+    if rank == 0 and not args.no_cpu_baseline:
+        v_cpu, desc, cores, spent = cpu_oracle_sample(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

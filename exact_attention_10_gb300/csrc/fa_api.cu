@@ -1,0 +1,250 @@
+// fa_api.cu -- host side of the C ABI declared in include/fa.h: argument
+// validation, TMA descriptor encoding, kernel selection and launch, and the
+// device status word.
+//
+// The problem statement follows "Building a Verifiable FlashAttention Forward
+// from PyTorch to Triton" (Scope: contiguous [B, H, N, D] self-attention,
+// FP16/BF16, causal or not, D in {64, 128}) with the caller's softmax scale.
+#include "fa.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, resolved through the runtime so the
+// library has no link-time dependency on the driver library.
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<EncodeTiledFn>(nullptr);
+        }
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+constexpr int kMaxDevices = 64;
+constexpr int kVariants = 8;   // D x dtype x causal
+
+struct DeviceInfo {
+    bool probed = false;
+    bool supported = false;
+    int sms = 0;
+    bool smem_attr_set[kVariants] = {};
+};
+
+std::mutex g_mu;
+DeviceInfo g_devices[kMaxDevices];
+
+// Probe the current device once: compute capability 10.3 is required because
+// the kernels are built for sm_103a only.
+const DeviceInfo *device_info(int dev)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
+            d.supported = (major == 10 && minor == 3);
+            d.sms = sms;
+        } else {
+            cudaGetLastError();
+        }
+        d.probed = true;
+    }
+    return &d;
+}
+
+bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Device (or managed) memory of the current device.
+bool is_device_pointer(const void *p, int dev)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeManaged)
+        return true;
+    return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
+// Rank-3 map over [B*H, N, D] (innermost first): per-head row bounds, so a
+// box that runs past N is zero-filled instead of reading the next head.
+// Box = 64 columns (128 bytes, the 128-byte swizzle width) x 128 rows.
+bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D, bool bf16)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)fa::kBM, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                           const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+fa_status launch_variant(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const fa::FwdParams &p,
+                         int grid, cudaStream_t stream, int dev)
+{
+    auto kern = fa::fa_fwd_sm103<D, BF16, CAUSAL>;
+    const int variant = (D == 128 ? 4 : 0) + (BF16 ? 0 : 2) + (CAUSAL ? 1 : 0);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        bool &set = g_devices[dev].smem_attr_set[variant];
+        if (!set) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fa::Cfg<D>::kSmemBytes) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return FA_ERR_CUDA;
+            }
+            set = true;
+        }
+    }
+    kern<<<grid, fa::kThreads, fa::Cfg<D>::kSmemBytes, stream>>>(q, k, v, p);
+    if (cudaGetLastError() != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+template <int D>
+fa_status dispatch_dtype(bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                         const fa::FwdParams &p, int grid, cudaStream_t s, int dev)
+{
+    if (bf16)
+        return causal ? launch_variant<D, true, true>(q, k, v, p, grid, s, dev)
+                      : launch_variant<D, true, false>(q, k, v, p, grid, s, dev);
+    return causal ? launch_variant<D, false, true>(q, k, v, p, grid, s, dev)
+                  : launch_variant<D, false, false>(q, k, v, p, grid, s, dev);
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
+                            int D, int causal, float scale, fa_dtype dtype, fa_stream_t stream)
+{
+    // Arguments first: nothing below touches the device until they are sound.
+    if (dtype != FA_BF16 && dtype != FA_FP16)
+        return FA_ERR_INVALID_VALUE;
+    if (D != 64 && D != 128)
+        return FA_ERR_INVALID_VALUE;
+    if (B < 1 || H < 1 || N < 1 || (causal != 0 && causal != 1))
+        return FA_ERR_INVALID_VALUE;
+    if (!std::isfinite(scale) || !(scale > 0.f))
+        return FA_ERR_INVALID_VALUE;
+    const long long BH = (long long)B * H;
+    if (BH * N >= (1ll << 31))
+        return FA_ERR_INVALID_VALUE;
+    if (!Q || !K || !V || !O || !LSE)
+        return FA_ERR_INVALID_VALUE;
+    const uintptr_t any = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                          reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
+                          reinterpret_cast<uintptr_t>(LSE);
+    if (any & 15u)
+        return FA_ERR_MISALIGNED;
+    const size_t tbytes = (size_t)BH * N * D * 2, lbytes = (size_t)BH * N * sizeof(float);
+    if (ranges_overlap(O, tbytes, Q, tbytes) || ranges_overlap(O, tbytes, K, tbytes) ||
+        ranges_overlap(O, tbytes, V, tbytes) || ranges_overlap(LSE, lbytes, Q, tbytes) ||
+        ranges_overlap(LSE, lbytes, K, tbytes) || ranges_overlap(LSE, lbytes, V, tbytes) ||
+        ranges_overlap(LSE, lbytes, O, tbytes))
+        return FA_ERR_INVALID_VALUE;
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_UNSUPPORTED_DEVICE;
+    }
+    const DeviceInfo *di = device_info(dev);
+    if (!di || !di->supported)
+        return FA_ERR_UNSUPPORTED_DEVICE;
+    if (!is_device_pointer(Q, dev) || !is_device_pointer(K, dev) || !is_device_pointer(V, dev) ||
+        !is_device_pointer(O, dev) || !is_device_pointer(LSE, dev))
+        return FA_ERR_INVALID_VALUE;
+
+    const bool bf16 = dtype == FA_BF16;
+    alignas(64) CUtensorMap tq, tk, tv;
+    if (!encode_map(&tq, Q, (int)BH, N, D, bf16) || !encode_map(&tk, K, (int)BH, N, D, bf16) ||
+        !encode_map(&tv, V, (int)BH, N, D, bf16))
+        return FA_ERR_CUDA;
+
+    fa::FwdParams p;
+    p.O = O;
+    p.LSE = LSE;
+    p.N = N;
+    p.BH = (int)BH;
+    p.ctiles_per_bh = (N + fa::kCtaRows - 1) / fa::kCtaRows;
+    p.total_tiles = p.BH * p.ctiles_per_bh;
+    p.qk_scale = scale * 1.4426950408889634f;   // scale * log2(e)
+    const int grid = p.total_tiles < di->sms ? p.total_tiles : di->sms;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (D == 64)
+        return dispatch_dtype<64>(bf16, causal != 0, tq, tk, tv, p, grid, s, dev);
+    return dispatch_dtype<128>(bf16, causal != 0, tq, tk, tv, p, grid, s, dev);
+}
+
+extern "C" fa_status fa_sync_status(fa_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, fa::g_status_word, sizeof word) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(fa::g_status_word, &zero, sizeof zero) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_CUDA;
+        }
+        return FA_ERR_DEVICE_TIMEOUT;
+    }
+    return FA_OK;
+}
+
+extern "C" const char *fa_status_string(fa_status s)
+{
+    switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_VALUE: return "invalid argument";
+    case FA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FA_ERR_UNSUPPORTED_DEVICE: return "no compute capability 10.3 device";
+    case FA_ERR_CUDA: return "CUDA runtime or launch error";
+    case FA_ERR_DEVICE_TIMEOUT: return "a bounded wait inside the kernel expired";
+    }
+    return "unknown status";
+}

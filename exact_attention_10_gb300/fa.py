@@ -1,0 +1,103 @@
+"""ctypes binding of include/fa.h (argument marshalling only).
+
+Every compute step runs in the CUDA library; if it is missing this module
+raises instead of falling back to anything else.  torch is used for device
+memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+FA_BF16, FA_FP16 = 0, 1
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_MISALIGNED", 3: "FA_ERR_UNSUPPORTED_DEVICE",
+          4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
+EXPORTS = ("fa_fwd", "fa_sync_status", "fa_status_string")
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise OSError(f"CUDA library not built: {path} is missing (run exact_attention_10_gb300.build)")
+    lib = ctypes.CDLL(path)
+    vp, c_int = ctypes.c_void_p, ctypes.c_int
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, ctypes.c_float, c_int, vp]
+    lib.fa_fwd.restype = c_int
+    lib.fa_sync_status.argtypes = [vp]
+    lib.fa_sync_status.restype = c_int
+    lib.fa_status_string.argtypes = [c_int]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().fa_status_string(int(status)).decode()
+    except OSError:
+        return "library not loaded"
+
+
+def fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int, N: int, D: int,
+            causal: int, scale: float, dtype: int, stream: int = 0) -> int:
+    """Call fa_fwd with raw integer pointers; returns the status code unchanged."""
+    return load().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, D, causal, scale, dtype, stream)
+
+
+def sync_status(stream: int = 0) -> int:
+    return load().fa_sync_status(stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float16:
+        return FA_FP16
+    raise TypeError(f"fa_fwd takes bfloat16 or float16 tensors, got {t.dtype}")
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+    """Attention forward on CUDA tensors [B, H, N, D]; returns (O, LSE).
+
+    ``out`` / ``lse`` may be given to write into existing buffers.  Raises
+    FAError on any non-OK status.  Asynchronous on ``stream`` (default: the
+    current torch stream).
+    """
+    import torch
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one [B, H, N, D] shape")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    code = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    rc = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D,
+                 int(bool(causal)), float(scale), code, st)
+    if rc != 0:
+        raise FAError(rc, "fa_fwd")
+    return out, lse

@@ -1,0 +1,101 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 forward library.
+ *
+ * The operation is exact scaled-dot-product attention with an optional
+ * causal mask and the per-row log-sum-exp:
+ *
+ *   O[b,h,i,:] = sum_j softmax_j( scale * Q[b,h,i,:] . K[b,h,j,:] ) V[b,h,j,:]
+ *   LSE[b,h,i] = log sum_j exp( scale * Q[b,h,i,:] . K[b,h,j,:] )
+ *
+ * where j runs over all N keys, or over j <= i when causal.  It is computed
+ * with the FlashAttention-2 forward recurrence: K/V tiles stream past an
+ * on-chip Q tile, a running row max m and row sum l rescale an fp32 output
+ * accumulator by exp(m_old - m_new), and the accumulator is divided by l once
+ * at the end; the N x N score matrix is never written to memory.
+ *
+ * Sources (page title, section):
+ *  - "FlashAttention 2 from PyTorch to Triton", What I am building: the
+ *    recurrence, L = m + log(l) in natural-log units.
+ *  - "A09 - Advanced Triton & FlashAttention", 3. Deep Dive: the rescaling
+ *    update and its exactness; causal masking by block skipping.
+ *  - "Building a Verifiable FlashAttention Forward from PyTorch to Triton",
+ *    Scope: contiguous [B, H, N, D] self-attention, FP16/BF16, causal and
+ *    non-causal, head dimension 64 or 128.
+ *
+ * Every call is asynchronous on the caller's stream and stream-ordered like a
+ * kernel launch.  The library allocates no device memory per call; nothing
+ * in this header throws.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *fa_stream_t;
+
+/* Element type of Q, K, V and O. */
+typedef enum {
+    FA_BF16 = 0,   /* bfloat16 */
+    FA_FP16 = 1    /* IEEE binary16 */
+} fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_VALUE = 1,      /* bad size, dtype, flag, scale, NULL, host pointer or overlapping output */
+    FA_ERR_MISALIGNED = 2,         /* a pointer is not 16-byte aligned (the tensor-copy engine needs it) */
+    FA_ERR_UNSUPPORTED_DEVICE = 3, /* no device, or the current device is not compute capability 10.3 */
+    FA_ERR_CUDA = 4,               /* a CUDA runtime call or the launch failed */
+    FA_ERR_DEVICE_TIMEOUT = 5      /* a bounded in-kernel wait expired (reported by fa_sync_status) */
+} fa_status;
+
+/*
+ * fa_fwd -- attention forward for B*H independent heads.
+ *
+ * Q, K, V : device pointers to contiguous [B, H, N, D] tensors of `dtype`.
+ *           They may alias one another (they are only read).
+ * O       : device pointer to a contiguous [B, H, N, D] tensor of `dtype`;
+ *           every element is written.  Must not overlap Q, K, V or LSE.
+ * LSE     : device pointer to a contiguous [B, H, N] float32 tensor; row i
+ *           receives log sum_j exp(scale * q_i . k_j) (natural log) over its
+ *           visible keys.  Must not overlap Q, K, V or O.
+ * B, H, N : batch, heads, sequence length (queries = keys = N); each >= 1 and
+ *           B*H*N < 2^31.
+ * D       : head dimension, 64 or 128.
+ * causal  : 0 = every query sees all N keys; 1 = query i sees keys j <= i.
+ *           Key tiles wholly above the diagonal are skipped, not masked.
+ * scale   : softmax scale applied to q.k (usually 1/sqrt(D)); must be finite
+ *           and > 0 (the kernel takes row maxima on unscaled scores).
+ * stream  : CUDA stream the work is ordered on.
+ *
+ * All pointers belong to the caller and must stay valid until the work on
+ * `stream` completes.  The device is the caller's current CUDA device.
+ *
+ * Returns FA_OK once the kernel is enqueued.  Argument errors are detected
+ * before anything is enqueued and leave O and LSE untouched.  Errors raised
+ * inside the kernel (a bounded wait that expired) are recorded in a
+ * per-device status word and returned by fa_sync_status().
+ */
+fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                 int B, int H, int N, int D, int causal, float scale,
+                 fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * fa_sync_status -- synchronise `stream`, then return and clear the device
+ * status word of the current device: FA_OK, FA_ERR_DEVICE_TIMEOUT if a kernel
+ * gave up on a wait since the last call, or FA_ERR_CUDA if the synchronise
+ * itself failed.
+ */
+fa_status fa_sync_status(fa_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

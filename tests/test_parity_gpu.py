@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA path against the fp64 oracle, through the C ABI.
+
+Tolerances (max over every compared element), as the task states them:
+  bf16: max|O - O_ref| <= 1e-2;  fp16: max|O - O_ref| <= 2e-3;  |LSE - LSE_ref| <= 1e-3.
+O_ref is the unrounded fp64 oracle output, so the kernel's own output
+rounding counts against the tolerance.
+
+Workloads: the five named in exact_attention_10_gb300.inputs, compared in full
+where the oracle finishes in seconds and on sampled rows (rows 0, 1, tile
+edges, N-1 and random rows of every head) at the long-context sizes, in the
+same launch configuration bench.py times.  Edge cases: N around tile edges,
+one key, several heads, both dtypes and head sizes, large logits.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_10_gb300 import fa
+from exact_attention_10_gb300.inputs import WORKLOADS, make_custom, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = {"bf16": 1e-2, "fp16": 2e-3}
+TOL_LSE = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fa.load()
+
+
+def _run(q, k, v, causal, scale):
+    dev = torch.device("cuda:0")
+    qd, kd, vd = (x.to(dev) for x in (q, k, v))
+    o, lse = fa.forward(qd, kd, vd, causal=causal, scale=scale)
+    rc = fa.sync_status(torch.cuda.current_stream(dev).cuda_stream)
+    assert rc == 0, fa.status_string(rc)
+    return o.cpu(), lse.cpu()
+
+
+def _report(o, lse, o_ref, lse_ref):
+    od = o.double().numpy().reshape(o_ref.shape)
+    ld = lse.double().numpy().reshape(lse_ref.shape)
+    err = np.abs(od - o_ref)
+    lerr = np.abs(ld - lse_ref)
+    return float(err.max()), float(err.mean()), float(lerr.max()), err
+
+
+def _check_full(q, k, v, causal, scale, dtype, label=""):
+    o, lse = _run(q, k, v, causal, scale)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all(), label
+    o_ref, lse_ref = oracle.forward(q, k, v, causal, scale)
+    emax, emean, lmax, err = _report(o, lse, o_ref, lse_ref)
+    where = np.unravel_index(int(err.argmax()), err.shape)
+    print(f"{label} causal={int(causal)}: max|dO|={emax:.3e} mean|dO|={emean:.3e} max|dLSE|={lmax:.3e} "
+          f"worst at {tuple(int(i) for i in where)} (|O_ref|={abs(o_ref[where]):.3f})")
+    assert emax <= TOL_O[dtype], (label, emax)
+    assert lmax <= TOL_LSE, (label, lmax)
+    return emax, emean, lmax
+
+
+@pytest.mark.parametrize("name", ["tiny_n256", "b4h16_n1024", "ragged_n3000_d128_fp16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_workload_full(name, causal):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, seed=0)
+    _check_full(q, k, v, causal, w.scale, w.dtype, name)
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+@pytest.mark.parametrize("name", ["tiny_n256", "b4h16_n1024"])
+def test_workload_extra_seeds(name, seed):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, seed=seed)
+    for causal in (False, True):
+        _check_full(q, k, v, causal, w.scale, w.dtype, f"{name}/seed{seed}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_n4096_full_and_error_magnitude(causal):
+    """The pages' N = 4096 comparison scale, compared in full.  Non-causal, the
+    mean |O - O_f64| should sit near the 4.52e-5 the pages measured for a
+    kernel that sums l from fp32 P and rounds P to bf16 ("How to profile and
+    optimise kernels", the P cast section), and cannot beat the 2.9e-5 floor of
+    bf16 output rounding."""
+    w = WORKLOADS["b2h16_n4096"]
+    q, k, v = make_qkv(w, seed=0)
+    _, emean, _ = _check_full(q, k, v, causal, w.scale, w.dtype, w.name)
+    if not causal:
+        assert 2.8e-5 <= emean <= 6.0e-5, emean
+
+
+def _sample_rows(BH, N, per_head, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, 255, 256, N // 2, N - 2, N - 1]
+    bh_idx, row_idx = [], []
+    for h in range(BH):
+        rows = set(r for r in fixed if 0 <= r < N)
+        rows.update(int(r) for r in rng.integers(0, N, per_head - len(rows)))
+        for r in sorted(rows):
+            bh_idx.append(h)
+            row_idx.append(r)
+    return np.array(bh_idx), np.array(row_idx)
+
+
+@pytest.mark.parametrize("name", ["long_n32768_d128", "long_n16384_d128"])
+def test_long_context_sampled_rows(name):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, seed=0)
+    causal = w.masks[0]
+    o, lse = _run(q, k, v, causal, w.scale)
+    assert torch.isfinite(lse).all()
+    BH = w.B * w.H
+    bh_idx, row_idx = _sample_rows(BH, w.N, 48, seed=5)
+    o_ref, lse_ref = oracle.rows(q, k, v, causal, w.scale, bh_idx, row_idx)
+    of = o.reshape(BH, w.N, w.D).double().numpy()[bh_idx, row_idx]
+    lf = lse.reshape(BH, w.N).double().numpy()[bh_idx, row_idx]
+    emax = float(np.abs(of - o_ref).max())
+    lmax = float(np.abs(lf - lse_ref).max())
+    print(f"{name}: {len(bh_idx)} rows, max|dO|={emax:.3e} max|dLSE|={lmax:.3e}")
+    assert emax <= TOL_O[w.dtype] and lmax <= TOL_LSE
+    # every output row is a convex combination of V rows: finite and bounded by max|V|
+    assert torch.isfinite(o.float()).all()
+    assert float(o.float().abs().max()) <= float(v.float().abs().max()) * 1.01
+
+
+EDGE_N = [1, 2, 3, 64, 127, 128, 129, 255, 256, 257, 383, 384, 513]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("N", EDGE_N)
+def test_edge_lengths(N, dtype, D):
+    q, k, v = make_custom(2, 3, N, D, dtype, seed=N + D)
+    for causal in (False, True):
+        _check_full(q, k, v, causal, 1.0 / math.sqrt(D), dtype, f"N{N} D{D} {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_large_logits_stay_finite(dtype):
+    """Q and K amplified 4x at N = 513 ("Building a Verifiable FlashAttention
+    Forward from PyTorch to Triton", Part 4: the stability case): finite
+    everywhere and within tolerance.
+
+    In bf16 this case produces outputs with |O_ref| >= 4, where the spacing of
+    bf16 values is 2^-5: the exact answer rounded to bf16 can itself be more
+    than 1e-2 away from O_ref (4.208 -> 4.21875 is 0.0107).  So for bf16 the
+    1e-2 bound is applied strictly where |O_ref| < 4 (half a bf16 step there is
+    at most 2^-8), and elsewhere to the error in excess of that unavoidable
+    output-rounding floor.  fp16 is held to 2e-3 everywhere."""
+    q, k, v = make_custom(1, 4, 513, 64, dtype, seed=7, qk_gain=4.0)
+    for causal in (False, True):
+        o, lse = _run(q, k, v, causal, 1.0 / 8)
+        assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+        o_ref, lse_ref = oracle.forward(q, k, v, causal, 1.0 / 8)
+        emax, _, lmax, err = _report(o, lse, o_ref, lse_ref)
+        assert lmax <= TOL_LSE
+        if dtype == "fp16":
+            assert emax <= TOL_O["fp16"], emax
+            continue
+        floor = np.abs(torch.from_numpy(o_ref).to(torch.bfloat16).double().numpy() - o_ref)
+        small = np.abs(o_ref) < 4.0
+        print(f"amplified bf16 causal={int(causal)}: max|dO|={emax:.3e}, "
+              f"max over |O_ref|<4: {err[small].max():.3e}, max excess over rounding floor: "
+              f"{(err - floor).max():.3e}")
+        assert err[small].max() <= TOL_O["bf16"]
+        assert (err - floor).max() <= TOL_O["bf16"]
+
+
+def test_deterministic_and_no_out_of_bounds_writes():
+    """Two launches give identical bits; bytes just outside O and LSE are untouched."""
+    B, H, N, D = 2, 4, 777, 128
+    q, k, v = (x.cuda() for x in make_custom(B, H, N, D, "bf16", seed=11))
+    pad = 4096
+    o_buf = torch.full((B * H * N * D + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((B * H * N + 2 * pad,), 7.0, dtype=torch.float32, device="cuda")
+    o = o_buf[pad:pad + B * H * N * D].view(B, H, N, D)
+    lse = l_buf[pad:pad + B * H * N].view(B, H, N)
+    for causal in (False, True):
+        fa.forward(q, k, v, causal=causal, out=o, lse=lse)
+        first = (o.clone(), lse.clone())
+        fa.forward(q, k, v, causal=causal, out=o, lse=lse)
+        torch.cuda.synchronize()
+        assert torch.equal(first[0], o) and torch.equal(first[1], lse)
+        for buf in (o_buf, l_buf):
+            assert bool((buf[:pad].float() == 7.0).all()) and bool((buf[-pad:].float() == 7.0).all())
+
+
+def test_side_stream_and_status():
+    w = WORKLOADS["tiny_n256"]
+    q, k, v = (x.cuda() for x in make_qkv(w, seed=0))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = fa.forward(q, k, v, causal=True, scale=w.scale)
+    assert fa.sync_status(s.cuda_stream) == 0
+    o_ref, _ = oracle.forward(q.cpu(), k.cpu(), v.cpu(), True, w.scale)
+    assert float(np.abs(o.cpu().double().numpy() - o_ref).max()) <= TOL_O["bf16"]
+
+
+def test_rejects_host_memory():
+    w = WORKLOADS["tiny_n256"]
+    q, k, v = make_qkv(w, seed=0)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32)
+    rc = fa.fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 256, 64, 0,
+                    0.125, 0, 0)
+    assert rc == 1   # FA_ERR_INVALID_VALUE
