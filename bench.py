@@ -140,7 +140,7 @@ def cpu_oracle_sample(w, budget_s: float, rows_per_head: int | None = None):
     q, k, v = make_qkv(w, seed=0)
     BH = w.B * w.H
     per_row = {c: flops(1, 1, w.N, w.D, c) / w.N for c in (False, True)}
-    rows = rows_per_head or max(1, min(w.N, 64))
+    rows = rows_per_head or w.N
     done_flops, spent, heads = 0.0, 0.0, 0
     while spent < budget_s and heads < BH:
         bh = np.full(rows, heads, dtype=np.int64)
@@ -151,7 +151,8 @@ def cpu_oracle_sample(w, budget_s: float, rows_per_head: int | None = None):
             spent += time.perf_counter() - t
             done_flops += per_row[causal] * rows
         heads += 1
-    desc = (f"{heads} head(s) x {rows} rows spread over [0, N), non-causal and causal, of {w.describe()}; "
+    what = "all rows" if rows == w.N else f"{rows} rows spread over [0, N)"
+    desc = (f"{heads} of {BH} heads x {what}, non-causal and causal, of {w.describe()}; "
             f"{spent:.1f} s of CPU time")
     return done_flops / spent / 1e12, desc, oracle.num_threads(), spent
 

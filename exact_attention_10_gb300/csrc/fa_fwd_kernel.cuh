@@ -14,22 +14,30 @@
 // walk the CTA tiles; causal launches take the longest tiles first, heads
 // interleaved ("How to profile and optimise kernels", causal launch order).
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax/correction/epilogue for Q tile 0 (one thread per row)
-//   warps 4-7  the same for Q tile 1
-//   warp  8    TMA producer: Q tiles, then K_j, V_j into a ring of smem slots
-//   warp  9    tcgen05 MMA issuer (one thread) and TMEM owner
+// Warp roles (512 threads, four warpgroups):
+//   warpgroup 0  softmax of Q tile 0: S -> P, running max m and sum l (a row per thread)
+//   warpgroup 1  the same for Q tile 1
+//   warpgroup 2  correction (O_w *= exp2(m_old - m_new) before each P.V) and the
+//                epilogue (O = acc / l, LSE) for both Q tiles
+//   warpgroup 3  warp 12: TMA producer (Q tiles, then K_j, V_j into a smem ring)
+//                warp 13: tcgen05 MMA issuer (one thread) and TMEM owner
+// Registers are rebalanced with setmaxnreg: the softmax warpgroups hold a
+// 128-score row per thread, the other two need little.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D)
-//   P_w (16-bit, two per column) overwrites columns [0,64) of S_w once the
-//   softmax warps have read S_w, and feeds the P.V MMA as its TMEM A operand.
+//   D = 64:  P0 [384,448) and P1 [448,512) hold P (two 16-bit values per
+//            column), so S_{j+1} may be computed while softmax still works on
+//            S_j: the softmax releases S_w as soon as it has loaded it.
+//   D = 128: no room for separate P: P_w overwrites columns [0,64) of S_w,
+//            and S_w of step j+1 is issued after the MMA that reads P_w(j)
+//            (tcgen05 MMAs from one thread execute in issue order).
+// P feeds the P.V MMA as its TMEM A operand.
 //
-// MMA issue order per K/V step j (w = Q tile):
-//   S0_j = Q0 K_j^T,  O1 += P1_{j-1} V_{j-1},  S1_j = Q1 K_j^T,  O0 += P0_j V_j
-// so each softmax warpgroup has two MMAs' worth of time to turn S into P.
-// tcgen05 MMAs from one thread execute in issue order, so S_w of step j+1 may
-// be issued right after the MMA that reads P_w of step j.
+// MMA issue order per K/V step j:
+//   D = 64:  S0_{j+1}, S1_{j+1}, O0 += P0_j V_j, O1 += P1_j V_j
+//   D = 128: S0_j, O1 += P1_{j-1} V_{j-1}, S1_j, O0 += P0_j V_j
+// so each softmax warpgroup's work overlaps the other tile's MMAs.
 //
 // Softmax follows the exp2 form ("How to profile and optimise kernels", exp2):
 // qk_scale = scale*log2(e) is folded once, the row max is taken on raw scores
@@ -64,21 +72,28 @@ constexpr int kBM = 128;        // query rows per Q tile (one TMEM lane each)
 constexpr int kBN = 128;        // keys per K/V tile
 constexpr int kQTiles = 2;      // Q tiles per CTA tile
 constexpr int kCtaRows = kBM * kQTiles;
-constexpr int kThreads = 320;
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 512;
+constexpr int kCorrWarpgroup = 2;
+constexpr int kLoadWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr uint32_t kRegsSoftmax = 184;   // 2 x 128 x 184 + 128 x 80 + 128 x 64 = 65536
+constexpr uint32_t kRegsCorrection = 80;
+constexpr uint32_t kRegsProducer = 64;
+constexpr int kPerTileBars = 7;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // Wait sites recorded in the status word.
 enum : uint32_t {
-    kSiteLoadQEmpty = 1, kSiteLoadSlotEmpty, kSiteMmaQFull, kSiteMmaSlotFull, kSiteMmaPFull,
-    kSiteSoftSFull, kSiteSoftODone, kSiteDrain, kSiteTail
+    kSiteLoadQEmpty = 1, kSiteLoadSlotEmpty, kSiteMmaQFull, kSiteMmaSlotFull, kSiteMmaPFull, kSiteMmaOReady,
+    kSiteMmaSFree, kSiteSoftSFull, kSiteSoftODone, kSiteSoftAFree, kSiteCorrAReady, kSiteCorrODone, kSiteDrain,
+    kSiteTail
 };
 
 template <int D>
 struct Cfg {
     static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+    static constexpr bool kSeparateP = (D == 64);
     static constexpr int kBoxes = D / 64;              // 128-byte-wide TMA boxes per tile row
     static constexpr int kBoxBytes = kBM * 128;        // one [128 rows, 64 cols] 16-bit box
     static constexpr int kTileBytes = kBM * D * 2;     // one [128, D] 16-bit tile
@@ -86,12 +101,16 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kSlotOff = kQTiles * kTileBytes;
     static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
-    // full[kSlots], empty[kSlots], q_full, q_empty, s_full[2], p_full[2], o_done[2], drain
-    static constexpr int kNumBars = 2 * kSlots + 9;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    // full[kSlots], empty[kSlots], q_full, q_empty, then per Q tile: s_full,
+    // s_free, p_full, a_ready, a_free, o_ready, o_done; then drain
+    static constexpr int kNumBars = 2 * kSlots + 2 + kPerTileBars * kQTiles + 1;
+    static constexpr int kHandOff = kBarOff + kNumBars * 8;            // float2 [2 tiles][128]
+    static constexpr int kMiscOff = kHandOff + kQTiles * kBM * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + slack to align the base to 1024
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+    __host__ __device__ static constexpr uint32_t col_s(int w) { return w ? 128u : 0u; }
+    __host__ __device__ static constexpr uint32_t col_o(int w) { return w ? 256u + D : 256u; }
+    __host__ __device__ static constexpr uint32_t col_p(int w) { return kSeparateP ? (w ? 448u : 384u) : col_s(w); }
 };
 
 struct FwdParams {
@@ -188,10 +207,15 @@ struct Bars {
     __device__ uint32_t empty(int s) const { return base + 8u * (Cfg<D>::kSlots + s); }
     __device__ uint32_t q_full() const { return base + 8u * (2 * Cfg<D>::kSlots); }
     __device__ uint32_t q_empty() const { return q_full() + 8u; }
-    __device__ uint32_t s_full(int w) const { return q_full() + 16u + 8u * w; }
-    __device__ uint32_t p_full(int w) const { return q_full() + 32u + 8u * w; }
-    __device__ uint32_t o_done(int w) const { return q_full() + 48u + 8u * w; }
-    __device__ uint32_t drain() const { return q_full() + 64u; }
+    __device__ uint32_t per_tile(int w, int k) const { return q_full() + 16u + 8u * (kPerTileBars * w + k); }
+    __device__ uint32_t s_full(int w) const { return per_tile(w, 0); }    // MMA -> softmax: S_w ready
+    __device__ uint32_t s_free(int w) const { return per_tile(w, 1); }    // softmax -> MMA: S_w loaded
+    __device__ uint32_t p_full(int w) const { return per_tile(w, 2); }    // softmax -> MMA: P_w written
+    __device__ uint32_t a_ready(int w) const { return per_tile(w, 3); }   // softmax -> correction: handoff written
+    __device__ uint32_t a_free(int w) const { return per_tile(w, 4); }    // correction -> softmax: handoff read
+    __device__ uint32_t o_ready(int w) const { return per_tile(w, 5); }   // correction -> MMA: O_w rescaled
+    __device__ uint32_t o_done(int w) const { return per_tile(w, 6); }    // MMA -> softmax, correction: P.V done
+    __device__ uint32_t drain() const { return q_full() + 16u + 8u * (kPerTileBars * kQTiles); }
 };
 
 // ------------------------------------------------------------------ producer
@@ -253,89 +277,110 @@ __device__ void mma_role(const FwdParams &p, uint32_t sQ, uint32_t sSlot, uint32
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = instr_desc_f16(BF16, kBM, kBN, false);   // S = Q K^T, both K-major
     constexpr uint32_t kIdescPV = instr_desc_f16(BF16, kBM, D, true);      // O += P V, V is MN-major
-    const uint32_t tS[2] = {tmem + C::kColS0, tmem + C::kColS1};
-    const uint32_t tO[2] = {tmem + C::kColO0, tmem + C::kColO1};
-    uint32_t p_phase[2] = {0u, 0u};
+    uint32_t n_s[2] = {0u, 0u};    // S MMAs issued per Q tile (all CTA tiles)
+    uint32_t n_pv[2] = {0u, 0u};   // P.V MMAs issued per Q tile
     int item = 0, it = 0;
     bool ok = true;
 
+    auto slot_wait = [&](int idx, int &slot) -> bool {   // K/V item idx of this CTA
+        slot = idx % C::kSlots;
+        if (!wait_bounded(b.full(slot), (uint32_t)(idx / C::kSlots) & 1u, c, kSiteMmaSlotFull))
+            return false;
+        ptx::tc_fence_after_sync();
+        return true;
+    };
     // S_w = Q_w K^T over D/16 k-steps; K-major operands advance 32 bytes per
     // step inside a 128-byte swizzle row, and 16 KB per 64-column box.
-    auto issue_s = [&](int w, int kslot) {
+    auto issue_s = [&](int w, int kslot) -> bool {
+        if (C::kSeparateP && n_s[w] > 0) {   // softmax has loaded the previous S_w
+            if (!wait_bounded(b.s_free(w), (n_s[w] - 1) & 1u, c, kSiteMmaSFree))
+                return false;
+            ptx::tc_fence_after_sync();
+        }
         const uint32_t qa = sQ + w * C::kTileBytes;
         const uint32_t ka = sSlot + kslot * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-            ptx::mma_ss(tS[w], smem_desc_sw128(qa + off, 16), smem_desc_sw128(ka + off, 16), kIdescQK,
-                        kk > 0 ? 1u : 0u);
+            ptx::mma_ss(tmem + C::col_s(w), smem_desc_sw128(qa + off, 16), smem_desc_sw128(ka + off, 16),
+                        kIdescQK, kk > 0 ? 1u : 0u);
         }
+        ptx::mma_commit(b.s_full(w));
+        ++n_s[w];
+        return true;
     };
     // O_w (+)= P_w V over 128/16 k-steps; P from TMEM (8 columns per step),
     // V MN-major: 16 key rows = 2 KB per step, 64-column boxes 16 KB apart.
-    auto issue_pv = [&](int w, int vslot, bool accumulate) {
+    auto issue_pv = [&](int w, int vslot, bool accumulate) -> bool {
+        const uint32_t ph = n_pv[w] & 1u;
+        if (!wait_bounded(b.p_full(w), ph, c, kSiteMmaPFull) || !wait_bounded(b.o_ready(w), ph, c, kSiteMmaOReady))
+            return false;
+        ptx::tc_fence_after_sync();
         const uint32_t va = sSlot + vslot * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-            ptx::mma_ts(tO[w], tS[w] + kk * 8, smem_desc_sw128(va + kk * 2048, C::kBoxBytes), kIdescPV,
-                        (accumulate || kk > 0) ? 1u : 0u);
+            ptx::mma_ts(tmem + C::col_o(w), tmem + C::col_p(w) + kk * 8,
+                        smem_desc_sw128(va + kk * 2048, C::kBoxBytes), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(b.o_done(w));
+        ++n_pv[w];
+        return true;
     };
 
     for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
         int bh, ct;
         decode_tile<CAUSAL>(t, p, bh, ct);
-        const int n0 = kv_tiles<CAUSAL>(ct, 0, p.N), n1 = kv_tiles<CAUSAL>(ct, 1, p.N);
-        const int n = max(n0, n1);
+        const int nw[2] = {kv_tiles<CAUSAL>(ct, 0, p.N), kv_tiles<CAUSAL>(ct, 1, p.N)};
+        const int n = max(nw[0], nw[1]);
         if (!wait_bounded(b.q_full(), (uint32_t)(it & 1), c, kSiteMmaQFull)) { ok = false; break; }
         ptx::tc_fence_after_sync();
-        int vprev = -1;
-        for (int j = 0; j < n; ++j) {
-            const int kslot = item % C::kSlots;
-            if (!wait_bounded(b.full(kslot), (uint32_t)(item / C::kSlots) & 1u, c, kSiteMmaSlotFull)) { ok = false; break; }
-            ptx::tc_fence_after_sync();
-            ++item;
-            if (j < n0) {
-                issue_s(0, kslot);
-                ptx::mma_commit(b.s_full(0));
-            }
-            if (j >= 1) {
-                if (j - 1 < n1) {
-                    if (!wait_bounded(b.p_full(1), p_phase[1] & 1u, c, kSiteMmaPFull)) { ok = false; break; }
-                    ++p_phase[1];
-                    ptx::tc_fence_after_sync();
-                    issue_pv(1, vprev, j - 1 > 0);
-                    ptx::mma_commit(b.o_done(1));
+        const int item0 = item;
+        item += 2 * n;
+        int slot;
+        if (C::kSeparateP) {
+            // prologue: S_0 of both tiles
+            if (!(ok = slot_wait(item0, slot))) break;
+            for (int w = 0; w < kQTiles && ok; ++w)
+                if (nw[w] > 0)
+                    ok = issue_s(w, slot);
+            if (!ok) break;
+            ptx::mma_commit(b.empty(slot));
+            for (int j = 0; j < n && ok; ++j) {
+                if (j + 1 < n) {   // S of the next step first: it only needs the softmax to have loaded S_j
+                    if (!(ok = slot_wait(item0 + 2 * (j + 1), slot))) break;
+                    for (int w = 0; w < kQTiles && ok; ++w)
+                        if (j + 1 < nw[w])
+                            ok = issue_s(w, slot);
+                    if (!ok) break;
+                    ptx::mma_commit(b.empty(slot));
                 }
-                ptx::mma_commit(b.empty(vprev));   // V_{j-1} read by both P.V MMAs
+                if (!(ok = slot_wait(item0 + 2 * j + 1, slot))) break;
+                for (int w = 0; w < kQTiles && ok; ++w)
+                    if (j < nw[w])
+                        ok = issue_pv(w, slot, j > 0);
+                if (!ok) break;
+                ptx::mma_commit(b.empty(slot));
             }
-            if (j < n1) {
-                issue_s(1, kslot);
-                ptx::mma_commit(b.s_full(1));
+        } else {
+            int vprev = -1;
+            for (int j = 0; j < n && ok; ++j) {
+                int kslot, vslot;
+                if (!(ok = slot_wait(item0 + 2 * j, kslot))) break;
+                if (j < nw[0] && !(ok = issue_s(0, kslot))) break;
+                if (j >= 1) {
+                    if (j - 1 < nw[1] && !(ok = issue_pv(1, vprev, j - 1 > 0))) break;
+                    ptx::mma_commit(b.empty(vprev));   // V_{j-1} read by both P.V MMAs
+                }
+                if (j < nw[1] && !(ok = issue_s(1, kslot))) break;
+                ptx::mma_commit(b.empty(kslot));       // K_j read by both S MMAs
+                if (!(ok = slot_wait(item0 + 2 * j + 1, vslot))) break;
+                if (j < nw[0] && !(ok = issue_pv(0, vslot, j > 0))) break;
+                vprev = vslot;
             }
-            ptx::mma_commit(b.empty(kslot));       // K_j read by both S MMAs
-            const int vslot = item % C::kSlots;
-            if (!wait_bounded(b.full(vslot), (uint32_t)(item / C::kSlots) & 1u, c, kSiteMmaSlotFull)) { ok = false; break; }
-            ptx::tc_fence_after_sync();
-            ++item;
-            if (j < n0) {
-                if (!wait_bounded(b.p_full(0), p_phase[0] & 1u, c, kSiteMmaPFull)) { ok = false; break; }
-                ++p_phase[0];
-                ptx::tc_fence_after_sync();
-                issue_pv(0, vslot, j > 0);
-                ptx::mma_commit(b.o_done(0));
-            }
-            vprev = vslot;
+            if (!ok) break;
+            if (n - 1 < nw[1] && !(ok = issue_pv(1, vprev, n - 1 > 0))) break;
+            ptx::mma_commit(b.empty(vprev));
         }
-        if (!ok)
-            break;
-        if (n - 1 < n1) {
-            if (!wait_bounded(b.p_full(1), p_phase[1] & 1u, c, kSiteMmaPFull)) { ok = false; break; }
-            ++p_phase[1];
-            ptx::tc_fence_after_sync();
-            issue_pv(1, vprev, n - 1 > 0);
-            ptx::mma_commit(b.o_done(1));
-        }
-        ptx::mma_commit(b.empty(vprev));
+        if (!ok) break;
         ptx::mma_commit(b.q_empty());
     }
     // Drain: all MMAs this thread issued have completed before TMEM is freed.
@@ -346,25 +391,38 @@ __device__ void mma_role(const FwdParams &p, uint32_t sQ, uint32_t sSlot, uint32
 // ------------------------------------------------------------------ softmax
 
 template <int D, bool BF16, bool CAUSAL>
-__device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c)
+__device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, float2 *handoff)
 {
     using C = Cfg<D>;
     const int w = threadIdx.x / 128;              // Q tile of this warpgroup
-    const int wq = (threadIdx.x / 32) % 4;        // warp within the warpgroup: TMEM lanes 32*wq..
-    const int lane = threadIdx.x % 32;
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + (w ? C::kColS1 : C::kColS0) + lane_off;
-    const uint32_t tO = tmem + (w ? C::kColO1 : C::kColO0) + lane_off;
-    const float qk = p.qk_scale;
+    const int t = threadIdx.x % 128;              // row within the Q tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(t & ~31) << 16;
+    const uint32_t tS = tmem + C::col_s(w) + lane_off;
+    const uint32_t tP = tmem + C::col_p(w) + lane_off;
+    const uint64_t qk2 = ptx::f2_pack(p.qk_scale, p.qk_scale);
     uint32_t s_phase = 0, o_phase = 0;
+    uint32_t n_hand = 0;   // handoffs to the correction warps so far
+    // Publish one value pair to this row's correction thread.  The handoff
+    // slot is reused only after the correction thread has read it (a_free),
+    // so a_ready is never more than one phase ahead of its waiter.
+    auto hand_over = [&](float x, float y) -> bool {
+        if (n_hand > 0) {
+            if (!warp_wait(b.a_free(w), (n_hand - 1) & 1u, c, kSiteSoftAFree))
+                return false;
+        }
+        handoff[w * kBM + t] = make_float2(x, y);
+        ++n_hand;
+        ptx::mbar_arrive(b.a_ready(w));
+        return true;
+    };
 
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
         int bh, ct;
-        decode_tile<CAUSAL>(t, p, bh, ct);
+        decode_tile<CAUSAL>(tile, p, bh, ct);
         const int nw = kv_tiles<CAUSAL>(ct, w, p.N);
         if (nw == 0)
             continue;
-        const int row = ct * kCtaRows + w * kBM + wq * 32 + lane;   // query index (may be >= N: padding)
+        const int row = ct * kCtaRows + w * kBM + t;                // query index (may be >= N: padding)
         const int row_limit = CAUSAL ? min(p.N, row + 1) : p.N;     // keys < row_limit are visible
         float m = -INFINITY, l = 0.f;
 
@@ -379,6 +437,10 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             for (int q = 0; q < 4; ++q)
                 ptx::tmem_ld32(tS + q * 32, r[q]);
             ptx::tmem_wait_ld();
+            if (C::kSeparateP) {   // S_w may now be overwritten by the next step's MMA
+                ptx::tc_fence_before_sync();
+                ptx::mbar_arrive(b.s_free(w));
+            }
 
             float s[128];
 #pragma unroll
@@ -403,83 +465,166 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
                 mx[i & 7] = fmaxf(mx[i & 7], s[i]);
             const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            const float m_new = fmaxf(m, tile_max * qk);
+            const float m_new = fmaxf(m, tile_max * p.qk_scale);
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float alpha = ptx::ex2(m - m_use);      // 0 on the first tile (m = -inf)
-            const float neg_m = -m_use;
+            if (!hand_over(alpha, 0.f))                   // the correction warps may rescale O_w now
+                return;
+            const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
 
-            float sum[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                sum[i] = 0.f;
+            if (C::kSeparateP && j > 0) {   // P_w of the previous step has been consumed
+                if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
+                    return;
+                ++o_phase;
+                ptx::tc_fence_after_sync();
+            }
+
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p0 = ptx::ex2(fmaf(s[h * 64 + 2 * i], qk, neg_m));
-                    const float p1 = ptx::ex2(fmaf(s[h * 64 + 2 * i + 1], qk, neg_m));
-                    sum[i & 7] += p0 + p1;
+                    const uint64_t x = ptx::f2_fma(ptx::f2_pack(s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1]), qk2, negm2);
+                    float x0, x1;
+                    ptx::f2_unpack(x, x0, x1);
+                    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                    acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
                     pk[i] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
                 }
-                ptx::tmem_st32(tS + h * 32, pk);
+                ptx::tmem_st32(tP + h * 32, pk);
             }
-            const float rowsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-            l = l * alpha + rowsum;
+            const uint64_t a2 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
+            float a_lo, a_hi;
+            ptx::f2_unpack(a2, a_lo, a_hi);
+            l = l * alpha + (a_lo + a_hi);
             m = m_new;
-
-            if (j > 0) {   // rescale O_w (after P.V of step j-1 completed)
-                if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
-                    return;
-                ++o_phase;
-                ptx::tc_fence_after_sync();
-                if (!__all_sync(0xffffffffu, alpha == 1.f)) {
-#pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
-                        uint32_t o[32];
-                        ptx::tmem_ld32(tO + q * 32, o);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        ptx::tmem_st32(tO + q * 32, o);
-                    }
-                }
-            }
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(b.p_full(w));
         }
-
-        // Epilogue: O = acc / l in the input type, LSE = (m + log2 l) ln 2.
-        if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
+        // Final row statistics for the epilogue.
+        if (!hand_over(m, l))
             return;
-        ++o_phase;
-        ptx::tc_fence_after_sync();
-        const float inv_l = 1.f / l;
-        const bool valid = row < p.N;
-        uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) + ((size_t)bh * p.N + (size_t)(valid ? row : 0)) * D * 2;
+        if (C::kSeparateP) {   // account for the last P.V of this tile
+            if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
+                return;
+            ++o_phase;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ correction + epilogue
+
+template <int D, bool BF16, bool CAUSAL>
+__device__ void correction_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, const float2 *handoff)
+{
+    using C = Cfg<D>;
+    const int t = threadIdx.x % 128;              // row within a Q tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(t & ~31) << 16;
+    uint32_t a_phase[2] = {0u, 0u}, o_phase[2] = {0u, 0u};
+    // Take one value pair from this row's softmax thread and release the slot.
+    auto take = [&](int w, float2 &v) -> bool {
+        if (!warp_wait(b.a_ready(w), a_phase[w] & 1u, c, kSiteCorrAReady))
+            return false;
+        ++a_phase[w];
+        v = handoff[w * kBM + t];
+        ptx::mbar_arrive(b.a_free(w));
+        return true;
+    };
+
+    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+        int bh, ct;
+        decode_tile<CAUSAL>(tile, p, bh, ct);
+        const int nw[2] = {kv_tiles<CAUSAL>(ct, 0, p.N), kv_tiles<CAUSAL>(ct, 1, p.N)};
+        const int n = max(nw[0], nw[1]);
+        // Step j of Q tile w: O_w *= alpha before O_w += P_w(j) V_j.  Step 0
+        // needs no rescale (that MMA overwrites O_w) but still signals that the
+        // previous tile's epilogue has finished reading O_w.
+        for (int j = 0; j < n; ++j) {
+            for (int w = 0; w < kQTiles; ++w) {
+                if (j >= nw[w])
+                    continue;
+                float2 hv;
+                if (!take(w, hv))
+                    return;
+                if (j > 0) {
+                    const float alpha = hv.x;
+                    if (!warp_wait(b.o_done(w), o_phase[w] & 1u, c, kSiteCorrODone))
+                        return;
+                    ++o_phase[w];
+                    ptx::tc_fence_after_sync();
+                    if (!__all_sync(0xffffffffu, alpha == 1.f)) {
+                        const uint64_t a2 = ptx::f2_pack(alpha, alpha);
+                        const uint32_t tO = tmem + C::col_o(w) + lane_off;
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + q * 32, o);
-            ptx::tmem_wait_ld();
-            uint32_t pk[16];
+                        for (int q = 0; q < D / 32; ++q) {
+                            uint32_t o[32];
+                            ptx::tmem_ld32(tO + q * 32, o);
+                            ptx::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float a = __uint_as_float(o[2 * i]) * inv_l;
-                const float z = __uint_as_float(o[2 * i + 1]) * inv_l;
-                pk[i] = BF16 ? ptx::pack_bf16x2(a, z) : ptx::pack_f16x2(a, z);
-            }
-            if (valid) {
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    ptx::st_global_v4(orow + q * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                            for (int i = 0; i < 16; ++i) {
+                                uint64_t v = ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]),
+                                                                      __uint_as_float(o[2 * i + 1])), a2);
+                                float lo, hi;
+                                ptx::f2_unpack(v, lo, hi);
+                                o[2 * i] = __float_as_uint(lo);
+                                o[2 * i + 1] = __float_as_uint(hi);
+                            }
+                            ptx::tmem_st32(tO + q * 32, o);
+                        }
+                        ptx::tmem_wait_st();
+                    }
+                }
+                ptx::tc_fence_before_sync();
+                ptx::mbar_arrive(b.o_ready(w));
             }
         }
-        if (valid)
-            p.LSE[(size_t)bh * p.N + row] = (m + log2f(l)) * kLn2;
-        ptx::tc_fence_before_sync();
+        // Epilogue: O = acc / l in the input type, LSE = (m + log2 l) ln 2.
+        for (int w = 0; w < kQTiles; ++w) {
+            if (nw[w] == 0)
+                continue;
+            float2 st;
+            if (!take(w, st))
+                return;
+            const float m = st.x;
+            const float l = st.y;
+            if (!warp_wait(b.o_done(w), o_phase[w] & 1u, c, kSiteCorrODone))
+                return;
+            ++o_phase[w];
+            ptx::tc_fence_after_sync();
+            const float inv_l = 1.f / l;
+            const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
+            const int row = ct * kCtaRows + w * kBM + t;
+            const bool valid = row < p.N;
+            uint8_t *orow =
+                reinterpret_cast<uint8_t *>(p.O) + ((size_t)bh * p.N + (size_t)(valid ? row : 0)) * D * 2;
+            const uint32_t tO = tmem + C::col_o(w) + lane_off;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                ptx::tmem_ld32(tO + q * 32, o);
+                ptx::tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float a, z;
+                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                                               il2),
+                                   a, z);
+                    pk[i] = BF16 ? ptx::pack_bf16x2(a, z) : ptx::pack_f16x2(a, z);
+                }
+                if (valid) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        ptx::st_global_v4(orow + q * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                          pk[4 * v + 3]);
+                }
+            }
+            if (valid)
+                p.LSE[(size_t)bh * p.N + row] = (m + log2f(l)) * kLn2;
+            ptx::tc_fence_before_sync();
+        }
     }
 }
 
@@ -498,11 +643,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = base + C::kQOff;
     const uint32_t sSlot = base + C::kSlotOff;
     Bars<D> b{base + C::kBarOff};
+    float2 *handoff = reinterpret_cast<float2 *>(base_ptr + C::kHandOff);
     uint32_t *misc = reinterpret_cast<uint32_t *>(base_ptr + C::kMiscOff);
     Ctl c{reinterpret_cast<volatile int *>(misc + 1)};
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    const int wg = warp / 4;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kSlots; ++s) {
@@ -513,7 +660,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(b.q_empty(), 1);
         for (int w = 0; w < kQTiles; ++w) {
             ptx::mbar_init(b.s_full(w), 1);
+            ptx::mbar_init(b.s_free(w), kBM);
             ptx::mbar_init(b.p_full(w), kBM);
+            ptx::mbar_init(b.a_ready(w), kBM);
+            ptx::mbar_init(b.a_free(w), kBM);
+            ptx::mbar_init(b.o_ready(w), kBM);
             ptx::mbar_init(b.o_done(w), 1);
         }
         ptx::mbar_init(b.drain(), 1);
@@ -534,16 +685,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc);
 
-    if (warp < kLoadWarp) {
-        softmax_role<D, BF16, CAUSAL>(p, tmem, b, c);
-    } else if (warp == kLoadWarp) {
-        if (lane == 0)
-            load_role<D, CAUSAL>(&tmQ, &tmK, &tmV, p, sQ, sSlot, b, c);
-        __syncwarp();
+    if (wg < kCorrWarpgroup) {
+        ptx::regs_increase<kRegsSoftmax>();
+        softmax_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff);
+    } else if (wg == kCorrWarpgroup) {
+        ptx::regs_decrease<kRegsCorrection>();
+        correction_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff);
     } else {
-        if (lane == 0)
-            mma_role<D, BF16, CAUSAL>(p, sQ, sSlot, tmem, b, c);
-        __syncwarp();
+        ptx::regs_decrease<kRegsProducer>();
+        if (warp == kLoadWarp) {
+            if (lane == 0)
+                load_role<D, CAUSAL>(&tmQ, &tmK, &tmV, p, sQ, sSlot, b, c);
+            __syncwarp();
+        } else if (warp == kMmaWarp) {
+            if (lane == 0)
+                mma_role<D, BF16, CAUSAL>(p, sQ, sSlot, tmem, b, c);
+            __syncwarp();
+        }
     }
 
     ptx::tc_fence_before_sync();
