@@ -76,9 +76,9 @@ constexpr int kThreads = 512;
 constexpr int kCorrWarpgroup = 2;
 constexpr int kLoadWarp = 12;
 constexpr int kMmaWarp = 13;
-constexpr uint32_t kRegsSoftmax = 184;   // 2 x 128 x 184 + 128 x 80 + 128 x 64 = 65536
-constexpr uint32_t kRegsCorrection = 80;
-constexpr uint32_t kRegsProducer = 64;
+constexpr uint32_t kRegsSoftmax = 184;   // 2 x 128 x 184 + 128 x 56 + 128 x 88 = 65536
+constexpr uint32_t kRegsCorrection = 56;
+constexpr uint32_t kRegsProducer = 88;
 constexpr int kPerTileBars = 7;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -97,13 +97,14 @@ struct Cfg {
     static constexpr int kBoxes = D / 64;              // 128-byte-wide TMA boxes per tile row
     static constexpr int kBoxBytes = kBM * 128;        // one [128 rows, 64 cols] 16-bit box
     static constexpr int kTileBytes = kBM * D * 2;     // one [128, D] 16-bit tile
-    static constexpr int kSlots = (D == 64) ? 8 : 4;   // K/V ring depth (K and V tiles alternate)
+    static constexpr int kStages = (D == 64) ? 4 : 2;  // K/V ring depth; a stage holds K_j and V_j
+    static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQOff = 0;
-    static constexpr int kSlotOff = kQTiles * kTileBytes;
-    static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
-    // full[kSlots], empty[kSlots], q_full, q_empty, then per Q tile: s_full,
+    static constexpr int kStageOff = kQTiles * kTileBytes;
+    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    // full[kStages], empty[kStages], q_full, q_empty, then per Q tile: s_full,
     // s_free, p_full, a_ready, a_free, o_ready, o_done; then drain
-    static constexpr int kNumBars = 2 * kSlots + 2 + kPerTileBars * kQTiles + 1;
+    static constexpr int kNumBars = 2 * kStages + 2 + kPerTileBars * kQTiles + 1;
     static constexpr int kHandOff = kBarOff + kNumBars * 8;            // float2 [2 tiles][128]
     static constexpr int kMiscOff = kHandOff + kQTiles * kBM * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + slack to align the base to 1024
@@ -203,9 +204,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c, 
 template <int D>
 struct Bars {
     uint32_t base;
-    __device__ uint32_t full(int s) const { return base + 8u * s; }
-    __device__ uint32_t empty(int s) const { return base + 8u * (Cfg<D>::kSlots + s); }
-    __device__ uint32_t q_full() const { return base + 8u * (2 * Cfg<D>::kSlots); }
+    __device__ uint32_t full(int s) const { return base + 8u * s; }                          // TMA -> MMA: stage s landed
+    __device__ uint32_t empty(int s) const { return base + 8u * (Cfg<D>::kStages + s); }     // MMA -> TMA: stage s read
+    __device__ uint32_t q_full() const { return base + 8u * (2 * Cfg<D>::kStages); }
     __device__ uint32_t q_empty() const { return q_full() + 8u; }
     __device__ uint32_t per_tile(int w, int k) const { return q_full() + 16u + 8u * (kPerTileBars * w + k); }
     __device__ uint32_t s_full(int w) const { return per_tile(w, 0); }    // MMA -> softmax: S_w ready
@@ -220,172 +221,248 @@ struct Bars {
 
 // ------------------------------------------------------------------ producer
 
+// TMA producer, run by a whole warp; one elected lane issues the copies.
+// Per CTA tile: both Q tiles into the Q buffer, then for each step j the
+// pair K_j, V_j into the next stage of the ring.
 template <int D, bool CAUSAL>
 __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
-                          const FwdParams &p, uint32_t sQ, uint32_t sSlot, Bars<D> b, Ctl c)
+                          const FwdParams &p, uint32_t sQ, uint32_t sStage, Bars<D> b, Ctl c)
 {
     using C = Cfg<D>;
-    int item = 0;   // K/V tiles issued so far (K_0, V_0, K_1, ...)
+    int step = 0;   // K/V stages filled so far
     int it = 0;     // CTA tiles started by this CTA
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
         int bh, ct;
         decode_tile<CAUSAL>(t, p, bh, ct);
         const int n = max(kv_tiles<CAUSAL>(ct, 0, p.N), kv_tiles<CAUSAL>(ct, 1, p.N));
-        if (!wait_bounded(b.q_empty(), (it & 1) ^ 1, c, kSiteLoadQEmpty)) { ok = false; break; }
-        ptx::mbar_arrive_expect_tx(b.q_full(), kQTiles * C::kTileBytes);
-        for (int w = 0; w < kQTiles; ++w)
-            for (int x = 0; x < C::kBoxes; ++x)
-                ptx::tma_load_3d(sQ + w * C::kTileBytes + x * C::kBoxBytes, tmQ, b.q_full(), x * 64,
-                                 ct * kCtaRows + w * kBM, bh);
-        for (int j = 0; ok && j < n; ++j) {
-            for (int kv = 0; kv < 2; ++kv) {
-                const int slot = item % C::kSlots;
-                const uint32_t use = (uint32_t)(item / C::kSlots);
-                if (!wait_bounded(b.empty(slot), (use & 1u) ^ 1u, c, kSiteLoadSlotEmpty)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(b.full(slot), C::kTileBytes);
-                const CUtensorMap *tm = kv ? tmV : tmK;
+        if (!warp_wait(b.q_empty(), (it & 1) ^ 1, c, kSiteLoadQEmpty)) { ok = false; break; }
+        if (ptx::elect_one()) {
+            ptx::mbar_arrive_expect_tx(b.q_full(), kQTiles * C::kTileBytes);
+            for (int w = 0; w < kQTiles; ++w)
                 for (int x = 0; x < C::kBoxes; ++x)
-                    ptx::tma_load_3d(sSlot + slot * C::kTileBytes + x * C::kBoxBytes, tm, b.full(slot), x * 64,
-                                     j * kBN, bh);
-                ++item;
+                    ptx::tma_load_3d(sQ + w * C::kTileBytes + x * C::kBoxBytes, tmQ, b.q_full(), x * 64,
+                                     ct * kCtaRows + w * kBM, bh);
+        }
+        __syncwarp();
+        for (int j = 0; j < n; ++j, ++step) {
+            const int st = step % C::kStages;
+            const uint32_t use = (uint32_t)(step / C::kStages);
+            if (!warp_wait(b.empty(st), (use & 1u) ^ 1u, c, kSiteLoadSlotEmpty)) { ok = false; break; }
+            if (ptx::elect_one()) {
+                const uint32_t dst = sStage + st * C::kStageBytes;
+                ptx::mbar_arrive_expect_tx(b.full(st), C::kStageBytes);
+                for (int x = 0; x < C::kBoxes; ++x)
+                    ptx::tma_load_3d(dst + x * C::kBoxBytes, tmK, b.full(st), x * 64, j * kBN, bh);
+                for (int x = 0; x < C::kBoxes; ++x)
+                    ptx::tma_load_3d(dst + C::kTileBytes + x * C::kBoxBytes, tmV, b.full(st), x * 64, j * kBN, bh);
             }
+            __syncwarp();
         }
     }
-    // Tail: every copy this thread issued has landed and (unless aborting)
-    // every slot and the Q buffer have been released by the MMA warp, so no
-    // asynchronous write or arrive targets this CTA's shared memory after exit.
-    for (int s = 0; s < C::kSlots && s < item; ++s) {
-        const int last = item - 1 - ((item - 1 - s) % C::kSlots);   // last item that used slot s
-        const uint32_t use = (uint32_t)(last / C::kSlots);
-        wait_bounded(b.full(s), use & 1u, c, kSiteTail);
+    // Tail: every copy issued has landed and (unless aborting) every stage and
+    // the Q buffer have been released by the MMA warp, so no asynchronous
+    // write or arrive targets this CTA's shared memory after exit.
+    for (int s = 0; s < C::kStages && s < step; ++s) {
+        const int last = step - 1 - ((step - 1 - s) % C::kStages);   // last step that used stage s
+        const uint32_t use = (uint32_t)(last / C::kStages);
+        warp_wait(b.full(s), use & 1u, c, kSiteTail);
         if (!*c.abort_flag)
-            wait_bounded(b.empty(s), use & 1u, c, kSiteTail);
+            warp_wait(b.empty(s), use & 1u, c, kSiteTail);
     }
     if (it > 0) {
-        wait_bounded(b.q_full(), (uint32_t)((it - 1) & 1), c, kSiteTail);
+        warp_wait(b.q_full(), (uint32_t)((it - 1) & 1), c, kSiteTail);
         if (!*c.abort_flag)
-            wait_bounded(b.q_empty(), (uint32_t)((it - 1) & 1), c, kSiteTail);
+            warp_wait(b.q_empty(), (uint32_t)((it - 1) & 1), c, kSiteTail);
     }
 }
 
 // ------------------------------------------------------------------ MMA issuer
 
-template <int D, bool BF16, bool CAUSAL>
-__device__ void mma_role(const FwdParams &p, uint32_t sQ, uint32_t sSlot, uint32_t tmem, Bars<D> b, Ctl c)
-{
-    using C = Cfg<D>;
-    constexpr uint32_t kIdescQK = instr_desc_f16(BF16, kBM, kBN, false);   // S = Q K^T, both K-major
-    constexpr uint32_t kIdescPV = instr_desc_f16(BF16, kBM, D, true);      // O += P V, V is MN-major
-    uint32_t n_s[2] = {0u, 0u};    // S MMAs issued per Q tile (all CTA tiles)
-    uint32_t n_pv[2] = {0u, 0u};   // P.V MMAs issued per Q tile
-    int item = 0, it = 0;
-    bool ok = true;
+// Upper word of every shared-memory descriptor used here: stride byte offset
+// 1024 (8 rows of 128 bytes), descriptor version 1, 128-byte swizzle.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
 
-    auto slot_wait = [&](int idx, int &slot) -> bool {   // K/V item idx of this CTA
-        slot = idx % C::kSlots;
-        if (!wait_bounded(b.full(slot), (uint32_t)(idx / C::kSlots) & 1u, c, kSiteMmaSlotFull))
+__device__ __forceinline__ uint64_t desc_from_lo(uint32_t lo)
+{
+    return ((uint64_t)kDescHi << 32) | lo;
+}
+
+// Lower descriptor word: start address and leading byte offset (both >> 4).
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo)
+{
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+
+// The MMA-issuing warp.  The whole warp runs the control flow and the waits,
+// so loop state and descriptors stay warp-uniform; one elected lane (the
+// same lane every time, as tcgen05.commit tracks the MMAs of the lane that
+// issued them) issues the tcgen05.mma and tcgen05.commit instructions.
+// Everything per step is kept in scalar registers (tile indices are
+// compile-time): this warp's issue rate bounds the tensor pipe.
+template <int D, bool BF16>
+struct MmaIssuer {
+    using C = Cfg<D>;
+    static constexpr uint32_t kIdescQK = instr_desc_f16(BF16, kBM, kBN, false);   // S = Q K^T, both K-major
+    static constexpr uint32_t kIdescPV = instr_desc_f16(BF16, kBM, D, true);      // O += P V, V is MN-major
+    uint32_t q_lo;       // descriptor lower word of Q tile 0 (tile 1 is kTileBytes further)
+    uint32_t k_lo;       // descriptor lower word of K in stage 0, K-major (leading byte offset unused)
+    uint32_t v_lo;       // same for V in stage 0 (MN-major: leading byte offset = box stride)
+    uint32_t tmem;
+    Bars<D> b;
+    Ctl c;
+    uint32_t n_s0, n_s1, n_pv0, n_pv1;   // S and P.V MMAs issued per Q tile
+
+    __device__ bool stage_wait(int step, int &st) const
+    {
+        st = step % C::kStages;
+        if (!warp_wait(b.full(st), (uint32_t)(step / C::kStages) & 1u, c, kSiteMmaSlotFull))
             return false;
         ptx::tc_fence_after_sync();
         return true;
-    };
-    // S_w = Q_w K^T over D/16 k-steps; K-major operands advance 32 bytes per
-    // step inside a 128-byte swizzle row, and 16 KB per 64-column box.
-    auto issue_s = [&](int w, int kslot) -> bool {
-        if (C::kSeparateP && n_s[w] > 0) {   // softmax has loaded the previous S_w
-            if (!wait_bounded(b.s_free(w), (n_s[w] - 1) & 1u, c, kSiteMmaSFree))
+    }
+
+    __device__ void release(int st) const
+    {
+        if (ptx::elect_one())
+            ptx::mma_commit(b.empty(st));
+        __syncwarp();
+    }
+
+    // S_w = Q_w K^T over D/16 k-steps: K-major operands advance 32 bytes per
+    // step inside a 128-byte swizzle row and 16 KB per 64-column box.
+    template <int W>
+    __device__ bool issue_s(int st)
+    {
+        uint32_t &n = W ? n_s1 : n_s0;
+        if (C::kSeparateP && n > 0) {   // the softmax has loaded the previous S_w
+            if (!warp_wait(b.s_free(W), (n - 1) & 1u, c, kSiteMmaSFree))
                 return false;
             ptx::tc_fence_after_sync();
         }
-        const uint32_t qa = sQ + w * C::kTileBytes;
-        const uint32_t ka = sSlot + kslot * C::kTileBytes;
+        const uint32_t qa = q_lo + (uint32_t)(W * C::kTileBytes >> 4);
+        const uint32_t ka = k_lo + (uint32_t)(st * (C::kStageBytes >> 4));
+        if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-            ptx::mma_ss(tmem + C::col_s(w), smem_desc_sw128(qa + off, 16), smem_desc_sw128(ka + off, 16),
-                        kIdescQK, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)((kk / 4) * (C::kBoxBytes >> 4) + (kk % 4) * 2);
+                ptx::mma_ss(tmem + C::col_s(W), desc_from_lo(qa + off), desc_from_lo(ka + off), kIdescQK,
+                            kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(b.s_full(W));
         }
-        ptx::mma_commit(b.s_full(w));
-        ++n_s[w];
+        __syncwarp();
+        ++n;
         return true;
-    };
-    // O_w (+)= P_w V over 128/16 k-steps; P from TMEM (8 columns per step),
-    // V MN-major: 16 key rows = 2 KB per step, 64-column boxes 16 KB apart.
-    auto issue_pv = [&](int w, int vslot, bool accumulate) -> bool {
-        const uint32_t ph = n_pv[w] & 1u;
-        if (!wait_bounded(b.p_full(w), ph, c, kSiteMmaPFull) || !wait_bounded(b.o_ready(w), ph, c, kSiteMmaOReady))
+    }
+
+    // O_w (+)= P_w V over 128/16 k-steps: P from TMEM (8 columns per step),
+    // V MN-major: 16 key rows = 2 KB per step.
+    template <int W>
+    __device__ bool issue_pv(int st, bool accumulate)
+    {
+        uint32_t &n = W ? n_pv1 : n_pv0;
+        if (!warp_wait(b.p_full(W), n & 1u, c, kSiteMmaPFull) ||
+            !warp_wait(b.o_ready(W), n & 1u, c, kSiteMmaOReady))
             return false;
         ptx::tc_fence_after_sync();
-        const uint32_t va = sSlot + vslot * C::kTileBytes;
+        const uint32_t va = v_lo + (uint32_t)(st * (C::kStageBytes >> 4));
+        if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-            ptx::mma_ts(tmem + C::col_o(w), tmem + C::col_p(w) + kk * 8,
-                        smem_desc_sw128(va + kk * 2048, C::kBoxBytes), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(b.o_done(w));
-        ++n_pv[w];
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                ptx::mma_ts(tmem + C::col_o(W), tmem + C::col_p(W) + kk * 8, desc_from_lo(va + kk * (2048 >> 4)),
+                            kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(b.o_done(W));
+        }
+        __syncwarp();
+        ++n;
         return true;
-    };
+    }
 
-    for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
+    // D = 64 order: S of step j+1 for both tiles, then P.V of step j.
+    __device__ bool tile_separate_p(int step0, int n, int n0, int n1)
+    {
+        int st, st_next;
+        if (!stage_wait(step0, st))
+            return false;
+        if (n0 > 0 && !issue_s<0>(st))
+            return false;
+        if (n1 > 0 && !issue_s<1>(st))
+            return false;
+        for (int j = 0; j < n; ++j) {
+            if (j + 1 < n) {
+                if (!stage_wait(step0 + j + 1, st_next))
+                    return false;
+                if (j + 1 < n0 && !issue_s<0>(st_next))
+                    return false;
+                if (j + 1 < n1 && !issue_s<1>(st_next))
+                    return false;
+            }
+            if (j < n0 && !issue_pv<0>(st, j > 0))
+                return false;
+            if (j < n1 && !issue_pv<1>(st, j > 0))
+                return false;
+            release(st);   // K_j and V_j both read
+            st = st_next;
+        }
+        return true;
+    }
+
+    // D = 128 order: S0_j, P.V1_{j-1}, S1_j, P.V0_j (P overwrites S in TMEM).
+    __device__ bool tile_aliased_p(int step0, int n, int n0, int n1)
+    {
+        int st, prev = -1;
+        for (int j = 0; j < n; ++j) {
+            if (!stage_wait(step0 + j, st))
+                return false;
+            if (j < n0 && !issue_s<0>(st))
+                return false;
+            if (j >= 1) {
+                if (j - 1 < n1 && !issue_pv<1>(prev, j - 1 > 0))
+                    return false;
+                release(prev);   // K_{j-1} and V_{j-1} both read
+            }
+            if (j < n1 && !issue_s<1>(st))
+                return false;
+            if (j < n0 && !issue_pv<0>(st, j > 0))
+                return false;
+            prev = st;
+        }
+        if (n - 1 < n1 && !issue_pv<1>(prev, n - 1 > 0))
+            return false;
+        release(prev);
+        return true;
+    }
+};
+
+template <int D, bool BF16, bool CAUSAL>
+__device__ void mma_role(const FwdParams &p, uint32_t sQ, uint32_t sStage, uint32_t tmem, Bars<D> b, Ctl c)
+{
+    using C = Cfg<D>;
+    MmaIssuer<D, BF16> m{desc_lo(sQ, 16), desc_lo(sStage, 16), desc_lo(sStage + C::kTileBytes, C::kBoxBytes),
+                         tmem, b, c, 0u, 0u, 0u, 0u};
+    int step = 0, it = 0;
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
         int bh, ct;
         decode_tile<CAUSAL>(t, p, bh, ct);
-        const int nw[2] = {kv_tiles<CAUSAL>(ct, 0, p.N), kv_tiles<CAUSAL>(ct, 1, p.N)};
-        const int n = max(nw[0], nw[1]);
-        if (!wait_bounded(b.q_full(), (uint32_t)(it & 1), c, kSiteMmaQFull)) { ok = false; break; }
+        const int n0 = kv_tiles<CAUSAL>(ct, 0, p.N), n1 = kv_tiles<CAUSAL>(ct, 1, p.N);
+        const int n = max(n0, n1);
+        if (!warp_wait(b.q_full(), (uint32_t)(it & 1), c, kSiteMmaQFull))
+            break;
         ptx::tc_fence_after_sync();
-        const int item0 = item;
-        item += 2 * n;
-        int slot;
-        if (C::kSeparateP) {
-            // prologue: S_0 of both tiles
-            if (!(ok = slot_wait(item0, slot))) break;
-            for (int w = 0; w < kQTiles && ok; ++w)
-                if (nw[w] > 0)
-                    ok = issue_s(w, slot);
-            if (!ok) break;
-            ptx::mma_commit(b.empty(slot));
-            for (int j = 0; j < n && ok; ++j) {
-                if (j + 1 < n) {   // S of the next step first: it only needs the softmax to have loaded S_j
-                    if (!(ok = slot_wait(item0 + 2 * (j + 1), slot))) break;
-                    for (int w = 0; w < kQTiles && ok; ++w)
-                        if (j + 1 < nw[w])
-                            ok = issue_s(w, slot);
-                    if (!ok) break;
-                    ptx::mma_commit(b.empty(slot));
-                }
-                if (!(ok = slot_wait(item0 + 2 * j + 1, slot))) break;
-                for (int w = 0; w < kQTiles && ok; ++w)
-                    if (j < nw[w])
-                        ok = issue_pv(w, slot, j > 0);
-                if (!ok) break;
-                ptx::mma_commit(b.empty(slot));
-            }
-        } else {
-            int vprev = -1;
-            for (int j = 0; j < n && ok; ++j) {
-                int kslot, vslot;
-                if (!(ok = slot_wait(item0 + 2 * j, kslot))) break;
-                if (j < nw[0] && !(ok = issue_s(0, kslot))) break;
-                if (j >= 1) {
-                    if (j - 1 < nw[1] && !(ok = issue_pv(1, vprev, j - 1 > 0))) break;
-                    ptx::mma_commit(b.empty(vprev));   // V_{j-1} read by both P.V MMAs
-                }
-                if (j < nw[1] && !(ok = issue_s(1, kslot))) break;
-                ptx::mma_commit(b.empty(kslot));       // K_j read by both S MMAs
-                if (!(ok = slot_wait(item0 + 2 * j + 1, vslot))) break;
-                if (j < nw[0] && !(ok = issue_pv(0, vslot, j > 0))) break;
-                vprev = vslot;
-            }
-            if (!ok) break;
-            if (n - 1 < nw[1] && !(ok = issue_pv(1, vprev, n - 1 > 0))) break;
-            ptx::mma_commit(b.empty(vprev));
-        }
-        if (!ok) break;
-        ptx::mma_commit(b.q_empty());
+        const bool ok = C::kSeparateP ? m.tile_separate_p(step, n, n0, n1) : m.tile_aliased_p(step, n, n0, n1);
+        if (!ok)
+            break;
+        step += n;
+        if (ptx::elect_one())
+            ptx::mma_commit(b.q_empty());
+        __syncwarp();
     }
-    // Drain: all MMAs this thread issued have completed before TMEM is freed.
-    ptx::mma_commit(b.drain());
-    wait_bounded(b.drain(), 0u, c, kSiteDrain);
+    // Drain: all MMAs this warp issued have completed before TMEM is freed.
+    if (ptx::elect_one())
+        ptx::mma_commit(b.drain());
+    __syncwarp();
+    warp_wait(b.drain(), 0u, c, kSiteDrain);
 }
 
 // ------------------------------------------------------------------ softmax
@@ -456,15 +533,17 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
                     s[i] = (i < lim) ? s[i] : -INFINITY;
             }
 
-            float mx[8];
+            float mx[8];   // eight partial maxima: s[0..15] pairwise, then s[16..127] two at a time
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                mx[i] = s[i];
+            for (int k = 0; k < 8; ++k)
+                mx[k] = fmaxf(s[2 * k], s[2 * k + 1]);
 #pragma unroll
-            for (int i = 8; i < 128; ++i)
-                mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-            const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            for (int i = 16; i < 128; i += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mx[k] = ptx::fmax3(mx[k], s[i + 2 * k], s[i + 2 * k + 1]);
+            const float tile_max = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]), ptx::fmax3(mx[3], mx[4], mx[5]),
+                                              fmaxf(mx[6], mx[7]));
             const float m_new = fmaxf(m, tile_max * p.qk_scale);
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float alpha = ptx::ex2(m - m_use);      // 0 on the first tile (m = -inf)
@@ -641,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;    // 128-byte swizzle atoms need 1024-byte alignment
     uint8_t *base_ptr = smem_raw + (base - raw);
     const uint32_t sQ = base + C::kQOff;
-    const uint32_t sSlot = base + C::kSlotOff;
+    const uint32_t sStage = base + C::kStageOff;
     Bars<D> b{base + C::kBarOff};
     float2 *handoff = reinterpret_cast<float2 *>(base_ptr + C::kHandOff);
     uint32_t *misc = reinterpret_cast<uint32_t *>(base_ptr + C::kMiscOff);
@@ -652,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = warp / 4;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kSlots; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(b.full(s), 1);
             ptx::mbar_init(b.empty(s), 1);
         }
@@ -693,15 +772,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         correction_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff);
     } else {
         ptx::regs_decrease<kRegsProducer>();
-        if (warp == kLoadWarp) {
-            if (lane == 0)
-                load_role<D, CAUSAL>(&tmQ, &tmK, &tmV, p, sQ, sSlot, b, c);
-            __syncwarp();
-        } else if (warp == kMmaWarp) {
-            if (lane == 0)
-                mma_role<D, BF16, CAUSAL>(p, sQ, sSlot, tmem, b, c);
-            __syncwarp();
-        }
+        if (warp == kLoadWarp)
+            load_role<D, CAUSAL>(&tmQ, &tmK, &tmV, p, sQ, sStage, b, c);
+        else if (warp == kMmaWarp)
+            mma_role<D, BF16, CAUSAL>(p, sQ, sStage, tmem, b, c);
     }
 
     ptx::tc_fence_before_sync();
