@@ -99,12 +99,14 @@ struct Cfg {
     static constexpr int kTileBytes = kBM * D * 2;     // one [128, D] 16-bit tile
     static constexpr int kStages = (D == 64) ? 4 : 2;  // K/V ring depth; a stage holds K_j and V_j
     static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kQBufs = (D == 64) ? 2 : 1;   // Q buffers: the next CTA tile's Q loads early
+    static constexpr int kQBufBytes = kQTiles * kTileBytes;
     static constexpr int kQOff = 0;
-    static constexpr int kStageOff = kQTiles * kTileBytes;
+    static constexpr int kStageOff = kQBufs * kQBufBytes;
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-    // full[kStages], empty[kStages], q_full, q_empty, then per Q tile: s_full,
-    // s_free, p_full, a_ready, a_free, o_ready, o_done; then drain
-    static constexpr int kNumBars = 2 * kStages + 2 + kPerTileBars * kQTiles + 1;
+    // full[kStages], empty[kStages], q_full[kQBufs], q_empty[kQBufs], then per
+    // Q tile: s_full, s_free, p_full, a_ready, a_free, o_ready, o_done; then drain
+    static constexpr int kNumBars = 2 * kStages + 2 * kQBufs + kPerTileBars * kQTiles + 1;
     static constexpr int kHandOff = kBarOff + kNumBars * 8;            // float2 [2 tiles][128]
     static constexpr int kMiscOff = kHandOff + kQTiles * kBM * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + slack to align the base to 1024
@@ -206,9 +208,12 @@ struct Bars {
     uint32_t base;
     __device__ uint32_t full(int s) const { return base + 8u * s; }                          // TMA -> MMA: stage s landed
     __device__ uint32_t empty(int s) const { return base + 8u * (Cfg<D>::kStages + s); }     // MMA -> TMA: stage s read
-    __device__ uint32_t q_full() const { return base + 8u * (2 * Cfg<D>::kStages); }
-    __device__ uint32_t q_empty() const { return q_full() + 8u; }
-    __device__ uint32_t per_tile(int w, int k) const { return q_full() + 16u + 8u * (kPerTileBars * w + k); }
+    __device__ uint32_t q_full(int qb) const { return base + 8u * (2 * Cfg<D>::kStages + qb); }
+    __device__ uint32_t q_empty(int qb) const { return base + 8u * (2 * Cfg<D>::kStages + Cfg<D>::kQBufs + qb); }
+    __device__ uint32_t per_tile(int w, int k) const
+    {
+        return base + 8u * (2 * Cfg<D>::kStages + 2 * Cfg<D>::kQBufs + kPerTileBars * w + k);
+    }
     __device__ uint32_t s_full(int w) const { return per_tile(w, 0); }    // MMA -> softmax: S_w ready
     __device__ uint32_t s_free(int w) const { return per_tile(w, 1); }    // softmax -> MMA: S_w loaded
     __device__ uint32_t p_full(int w) const { return per_tile(w, 2); }    // softmax -> MMA: P_w written
@@ -216,7 +221,7 @@ struct Bars {
     __device__ uint32_t a_free(int w) const { return per_tile(w, 4); }    // correction -> softmax: handoff read
     __device__ uint32_t o_ready(int w) const { return per_tile(w, 5); }   // correction -> MMA: O_w rescaled
     __device__ uint32_t o_done(int w) const { return per_tile(w, 6); }    // MMA -> softmax, correction: P.V done
-    __device__ uint32_t drain() const { return q_full() + 16u + 8u * (kPerTileBars * kQTiles); }
+    __device__ uint32_t drain() const { return per_tile(kQTiles, 0); }
 };
 
 // ------------------------------------------------------------------ producer
@@ -236,12 +241,15 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
         int bh, ct;
         decode_tile<CAUSAL>(t, p, bh, ct);
         const int n = max(kv_tiles<CAUSAL>(ct, 0, p.N), kv_tiles<CAUSAL>(ct, 1, p.N));
-        if (!warp_wait(b.q_empty(), (it & 1) ^ 1, c, kSiteLoadQEmpty)) { ok = false; break; }
+        const int qb = it % C::kQBufs;
+        const uint32_t quse = (uint32_t)(it / C::kQBufs);
+        if (!warp_wait(b.q_empty(qb), (quse & 1u) ^ 1u, c, kSiteLoadQEmpty)) { ok = false; break; }
         if (ptx::elect_one()) {
-            ptx::mbar_arrive_expect_tx(b.q_full(), kQTiles * C::kTileBytes);
+            const uint32_t dst = sQ + qb * C::kQBufBytes;
+            ptx::mbar_arrive_expect_tx(b.q_full(qb), kQTiles * C::kTileBytes);
             for (int w = 0; w < kQTiles; ++w)
                 for (int x = 0; x < C::kBoxes; ++x)
-                    ptx::tma_load_3d(sQ + w * C::kTileBytes + x * C::kBoxBytes, tmQ, b.q_full(), x * 64,
+                    ptx::tma_load_3d(dst + w * C::kTileBytes + x * C::kBoxBytes, tmQ, b.q_full(qb), x * 64,
                                      ct * kCtaRows + w * kBM, bh);
         }
         __syncwarp();
@@ -270,10 +278,12 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
         if (!*c.abort_flag)
             warp_wait(b.empty(s), use & 1u, c, kSiteTail);
     }
-    if (it > 0) {
-        warp_wait(b.q_full(), (uint32_t)((it - 1) & 1), c, kSiteTail);
+    for (int qb = 0; qb < C::kQBufs && qb < it; ++qb) {
+        const int last = it - 1 - ((it - 1 - qb) % C::kQBufs);   // last CTA tile that used Q buffer qb
+        const uint32_t use = (uint32_t)(last / C::kQBufs);
+        warp_wait(b.q_full(qb), use & 1u, c, kSiteTail);
         if (!*c.abort_flag)
-            warp_wait(b.q_empty(), (uint32_t)((it - 1) & 1), c, kSiteTail);
+            warp_wait(b.q_empty(qb), use & 1u, c, kSiteTail);
     }
 }
 
@@ -331,6 +341,8 @@ struct MmaIssuer {
 
     // S_w = Q_w K^T over D/16 k-steps: K-major operands advance 32 bytes per
     // step inside a 128-byte swizzle row and 16 KB per 64-column box.
+    uint32_t q_cur;      // descriptor lower word of Q tile 0 in the current Q buffer
+
     template <int W>
     __device__ bool issue_s(int st)
     {
@@ -340,7 +352,7 @@ struct MmaIssuer {
                 return false;
             ptx::tc_fence_after_sync();
         }
-        const uint32_t qa = q_lo + (uint32_t)(W * C::kTileBytes >> 4);
+        const uint32_t qa = q_cur + (uint32_t)(W * C::kTileBytes >> 4);
         const uint32_t ka = k_lo + (uint32_t)(st * (C::kStageBytes >> 4));
         if (ptx::elect_one()) {
 #pragma unroll
@@ -440,22 +452,24 @@ __device__ void mma_role(const FwdParams &p, uint32_t sQ, uint32_t sStage, uint3
 {
     using C = Cfg<D>;
     MmaIssuer<D, BF16> m{desc_lo(sQ, 16), desc_lo(sStage, 16), desc_lo(sStage + C::kTileBytes, C::kBoxBytes),
-                         tmem, b, c, 0u, 0u, 0u, 0u};
+                         tmem, b, c, 0u, 0u, 0u, 0u, 0u};
     int step = 0, it = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
         int bh, ct;
         decode_tile<CAUSAL>(t, p, bh, ct);
         const int n0 = kv_tiles<CAUSAL>(ct, 0, p.N), n1 = kv_tiles<CAUSAL>(ct, 1, p.N);
         const int n = max(n0, n1);
-        if (!warp_wait(b.q_full(), (uint32_t)(it & 1), c, kSiteMmaQFull))
+        const int qb = it % C::kQBufs;
+        if (!warp_wait(b.q_full(qb), (uint32_t)(it / C::kQBufs) & 1u, c, kSiteMmaQFull))
             break;
         ptx::tc_fence_after_sync();
+        m.q_cur = m.q_lo + (uint32_t)(qb * (C::kQBufBytes >> 4));
         const bool ok = C::kSeparateP ? m.tile_separate_p(step, n, n0, n1) : m.tile_aliased_p(step, n, n0, n1);
         if (!ok)
             break;
         step += n;
         if (ptx::elect_one())
-            ptx::mma_commit(b.q_empty());
+            ptx::mma_commit(b.q_empty(qb));
         __syncwarp();
     }
     // Drain: all MMAs this warp issued have completed before TMEM is freed.
@@ -735,8 +749,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(b.full(s), 1);
             ptx::mbar_init(b.empty(s), 1);
         }
-        ptx::mbar_init(b.q_full(), 1);
-        ptx::mbar_init(b.q_empty(), 1);
+        for (int qb = 0; qb < C::kQBufs; ++qb) {
+            ptx::mbar_init(b.q_full(qb), 1);
+            ptx::mbar_init(b.q_empty(qb), 1);
+        }
         for (int w = 0; w < kQTiles; ++w) {
             ptx::mbar_init(b.s_full(w), 1);
             ptx::mbar_init(b.s_free(w), kBM);
