@@ -15,14 +15,16 @@
 // interleaved ("How to profile and optimise kernels", causal launch order).
 //
 // Warp roles (512 threads, four warpgroups):
-//   warpgroup 0  softmax of Q tile 0: S -> P, running max m and sum l (a row per thread)
+//   warpgroup 0  softmax of Q tile 0: S -> P, running max m and sum l (a row per thread),
+//                and the (rare) O rescale
 //   warpgroup 1  the same for Q tile 1
-//   warpgroup 2  correction (O_w *= exp2(m_old - m_new) before each P.V) and the
-//                epilogue (O = acc / l, LSE) for both Q tiles
-//   warpgroup 3  warp 12: TMA producer (Q tiles, then K_j, V_j into a smem ring)
-//                warp 13: tcgen05 MMA issuer (one thread) and TMEM owner
+//   warpgroup 2  epilogue for both Q tiles: O = acc / l and LSE, written once per tile
+//   warpgroup 3  warp 12: TMA producer (Q tiles, then K_j and V_j into a stage ring)
+//                warp 13: tcgen05 MMA issuer and TMEM owner
 // Registers are rebalanced with setmaxnreg: the softmax warpgroups hold a
-// 128-score row per thread, the other two need little.
+// 128-score row per thread, the other two need little.  The producer warps
+// run as whole warps with one elected lane issuing, so their control state is
+// warp-uniform.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D)
@@ -44,6 +46,12 @@
 // and then scaled (valid because scale > 0), m is kept in log2 units, and
 // LSE = (m + log2 l) * ln 2.  P is rounded to the input type for the P.V MMA;
 // l is summed from the fp32 P (the P cast section of the same page).
+// l and O are rescaled by exp2(m_old - m_new) only for rows whose max moved
+// (alpha = 1 otherwise, "A09 - Advanced Triton & FlashAttention", 3. Deep
+// Dive: the rescaling update); a warp whose 32 rows all kept their max skips
+// the O rescale.  As more keys are seen a new maximum becomes ever rarer, so
+// the softmax warps do the rescale themselves before releasing P instead of
+// handing it to other warps every step.
 // Masking happens only on the diagonal tile (causal) and the ragged last key
 // tile; tiles above the diagonal are never loaded ("A09 - Advanced Triton &
 // FlashAttention", causal masking: skipping beats masking).  Masked scores
@@ -73,11 +81,11 @@ constexpr int kBN = 128;        // keys per K/V tile
 constexpr int kQTiles = 2;      // Q tiles per CTA tile
 constexpr int kCtaRows = kBM * kQTiles;
 constexpr int kThreads = 512;
-constexpr int kCorrWarpgroup = 2;
+constexpr int kEpilogueWarpgroup = 2;
 constexpr int kLoadWarp = 12;
 constexpr int kMmaWarp = 13;
-constexpr uint32_t kRegsSoftmax = 184;   // 2 x 128 x 184 + 128 x 56 + 128 x 88 = 65536
-constexpr uint32_t kRegsCorrection = 56;
+constexpr uint32_t kRegsSoftmax = 184;   // 2 x 128 x 184 + 128 x 56 + 128 x 88 = 65536 (launch: 512 x 128)
+constexpr uint32_t kRegsEpilogue = 56;
 constexpr uint32_t kRegsProducer = 88;
 constexpr int kPerTileBars = 7;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -85,8 +93,8 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 // Wait sites recorded in the status word.
 enum : uint32_t {
-    kSiteLoadQEmpty = 1, kSiteLoadSlotEmpty, kSiteMmaQFull, kSiteMmaSlotFull, kSiteMmaPFull, kSiteMmaOReady,
-    kSiteMmaSFree, kSiteSoftSFull, kSiteSoftODone, kSiteSoftAFree, kSiteCorrAReady, kSiteCorrODone, kSiteDrain,
+    kSiteLoadQEmpty = 1, kSiteLoadSlotEmpty, kSiteMmaQFull, kSiteMmaSlotFull, kSiteMmaPFull, kSiteMmaOFree,
+    kSiteMmaSFree, kSiteSoftSFull, kSiteSoftODone, kSiteSoftStFree, kSiteEpiStReady, kSiteEpiODone, kSiteDrain,
     kSiteTail
 };
 
@@ -105,7 +113,7 @@ struct Cfg {
     static constexpr int kStageOff = kQBufs * kQBufBytes;
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
     // full[kStages], empty[kStages], q_full[kQBufs], q_empty[kQBufs], then per
-    // Q tile: s_full, s_free, p_full, a_ready, a_free, o_ready, o_done; then drain
+    // Q tile: s_full, s_free, p_full, o_done, st_ready, st_free, o_free; then drain
     static constexpr int kNumBars = 2 * kStages + 2 * kQBufs + kPerTileBars * kQTiles + 1;
     static constexpr int kHandOff = kBarOff + kNumBars * 8;            // float2 [2 tiles][128]
     static constexpr int kMiscOff = kHandOff + kQTiles * kBM * 8;
@@ -214,13 +222,13 @@ struct Bars {
     {
         return base + 8u * (2 * Cfg<D>::kStages + 2 * Cfg<D>::kQBufs + kPerTileBars * w + k);
     }
-    __device__ uint32_t s_full(int w) const { return per_tile(w, 0); }    // MMA -> softmax: S_w ready
-    __device__ uint32_t s_free(int w) const { return per_tile(w, 1); }    // softmax -> MMA: S_w loaded
-    __device__ uint32_t p_full(int w) const { return per_tile(w, 2); }    // softmax -> MMA: P_w written
-    __device__ uint32_t a_ready(int w) const { return per_tile(w, 3); }   // softmax -> correction: handoff written
-    __device__ uint32_t a_free(int w) const { return per_tile(w, 4); }    // correction -> softmax: handoff read
-    __device__ uint32_t o_ready(int w) const { return per_tile(w, 5); }   // correction -> MMA: O_w rescaled
-    __device__ uint32_t o_done(int w) const { return per_tile(w, 6); }    // MMA -> softmax, correction: P.V done
+    __device__ uint32_t s_full(int w) const { return per_tile(w, 0); }     // MMA -> softmax: S_w ready
+    __device__ uint32_t s_free(int w) const { return per_tile(w, 1); }     // softmax -> MMA: S_w loaded (D = 64)
+    __device__ uint32_t p_full(int w) const { return per_tile(w, 2); }     // softmax -> MMA: P_w written, O_w rescaled
+    __device__ uint32_t o_done(int w) const { return per_tile(w, 3); }     // MMA -> softmax, epilogue: P.V done
+    __device__ uint32_t st_ready(int w) const { return per_tile(w, 4); }   // softmax -> epilogue: final (m, l) written
+    __device__ uint32_t st_free(int w) const { return per_tile(w, 5); }    // epilogue -> softmax: (m, l) read
+    __device__ uint32_t o_free(int w) const { return per_tile(w, 6); }     // epilogue -> MMA: O_w read out
     __device__ uint32_t drain() const { return per_tile(kQTiles, 0); }
 };
 
@@ -322,6 +330,7 @@ struct MmaIssuer {
     Bars<D> b;
     Ctl c;
     uint32_t n_s0, n_s1, n_pv0, n_pv1;   // S and P.V MMAs issued per Q tile
+    uint32_t n_t0, n_t1;                 // Q tiles whose first P.V has been issued, per Q tile slot
 
     __device__ bool stage_wait(int step, int &st) const
     {
@@ -374,8 +383,13 @@ struct MmaIssuer {
     __device__ bool issue_pv(int st, bool accumulate)
     {
         uint32_t &n = W ? n_pv1 : n_pv0;
-        if (!warp_wait(b.p_full(W), n & 1u, c, kSiteMmaPFull) ||
-            !warp_wait(b.o_ready(W), n & 1u, c, kSiteMmaOReady))
+        uint32_t &nt = W ? n_t1 : n_t0;
+        if (!accumulate) {   // first P.V of a CTA tile overwrites O_w: the epilogue must have read it
+            if (nt > 0 && !warp_wait(b.o_free(W), (nt - 1) & 1u, c, kSiteMmaOFree))
+                return false;
+            ++nt;
+        }
+        if (!warp_wait(b.p_full(W), n & 1u, c, kSiteMmaPFull))
             return false;
         ptx::tc_fence_after_sync();
         const uint32_t va = v_lo + (uint32_t)(st * (C::kStageBytes >> 4));
@@ -452,7 +466,7 @@ __device__ void mma_role(const FwdParams &p, uint32_t sQ, uint32_t sStage, uint3
 {
     using C = Cfg<D>;
     MmaIssuer<D, BF16> m{desc_lo(sQ, 16), desc_lo(sStage, 16), desc_lo(sStage + C::kTileBytes, C::kBoxBytes),
-                         tmem, b, c, 0u, 0u, 0u, 0u, 0u};
+                         tmem, b, c, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     int step = 0, it = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
         int bh, ct;
@@ -490,22 +504,9 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
     const uint32_t lane_off = (uint32_t)(t & ~31) << 16;
     const uint32_t tS = tmem + C::col_s(w) + lane_off;
     const uint32_t tP = tmem + C::col_p(w) + lane_off;
+    const uint32_t tO = tmem + C::col_o(w) + lane_off;
     const uint64_t qk2 = ptx::f2_pack(p.qk_scale, p.qk_scale);
-    uint32_t s_phase = 0, o_phase = 0;
-    uint32_t n_hand = 0;   // handoffs to the correction warps so far
-    // Publish one value pair to this row's correction thread.  The handoff
-    // slot is reused only after the correction thread has read it (a_free),
-    // so a_ready is never more than one phase ahead of its waiter.
-    auto hand_over = [&](float x, float y) -> bool {
-        if (n_hand > 0) {
-            if (!warp_wait(b.a_free(w), (n_hand - 1) & 1u, c, kSiteSoftAFree))
-                return false;
-        }
-        handoff[w * kBM + t] = make_float2(x, y);
-        ++n_hand;
-        ptx::mbar_arrive(b.a_ready(w));
-        return true;
-    };
+    uint32_t s_phase = 0, o_phase = 0, n_st = 0;
 
     for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
         int bh, ct;
@@ -515,7 +516,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             continue;
         const int row = ct * kCtaRows + w * kBM + t;                // query index (may be >= N: padding)
         const int row_limit = CAUSAL ? min(p.N, row + 1) : p.N;     // keys < row_limit are visible
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY, l = 0.f;                               // running max (log2 units), row sum
 
         for (int j = 0; j < nw; ++j) {
             if (!warp_wait(b.s_full(w), s_phase & 1u, c, kSiteSoftSFull))
@@ -557,20 +558,22 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
                 for (int k = 0; k < 8; ++k)
                     mx[k] = ptx::fmax3(mx[k], s[i + 2 * k], s[i + 2 * k + 1]);
             const float tile_max = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]), ptx::fmax3(mx[3], mx[4], mx[5]),
-                                              fmaxf(mx[6], mx[7]));
-            const float m_new = fmaxf(m, tile_max * p.qk_scale);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ptx::ex2(m - m_use);      // 0 on the first tile (m = -inf)
-            if (!hand_over(alpha, 0.f))                   // the correction warps may rescale O_w now
-                return;
+                                              fmaxf(mx[6], mx[7])) * p.qk_scale;
+            // The running max changes only when this tile holds a larger score
+            // (always on the first visible tile, where m = -inf); otherwise
+            // alpha = 1 and nothing is rescaled.
+            const bool move = tile_max > m;
+            const float m_new = move ? tile_max : m;
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;   // no visible key yet: shift 0
+            const float alpha = move ? ptx::ex2(m - m_use) : 1.f;     // 0 on the first tile (m = -inf)
             const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
 
-            if (C::kSeparateP && j > 0) {   // P_w of the previous step has been consumed
+            if (C::kSeparateP && j > 0) {   // P.V of step j-1 done: P_w may be overwritten, O_w is final
                 if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
                     return;
                 ++o_phase;
                 ptx::tc_fence_after_sync();
-            }
+            }   // (D = 128: S_w(j) is issued after P.V_w(j-1), so s_full already implies it)
 
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
@@ -592,101 +595,76 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             ptx::f2_unpack(a2, a_lo, a_hi);
             l = l * alpha + (a_lo + a_hi);
             m = m_new;
+
+            // O_w *= alpha for the rows of this warp, skipped when no row's max
+            // moved (ever less likely as more keys have been seen).
+            if (j > 0 && __any_sync(0xffffffffu, move)) {
+                const uint64_t al2 = ptx::f2_pack(alpha, alpha);
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tO + q * 32, o);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float lo, hi;
+                        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                                                   al2),
+                                       lo, hi);
+                        o[2 * i] = __float_as_uint(lo);
+                        o[2 * i + 1] = __float_as_uint(hi);
+                    }
+                    ptx::tmem_st32(tO + q * 32, o);
+                }
+            }
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(b.p_full(w));
         }
-        // Final row statistics for the epilogue.
-        if (!hand_over(m, l))
-            return;
         if (C::kSeparateP) {   // account for the last P.V of this tile
             if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
                 return;
             ++o_phase;
         }
+        // Final row statistics for the epilogue warps (slot reused only once read).
+        if (n_st > 0 && !warp_wait(b.st_free(w), (n_st - 1) & 1u, c, kSiteSoftStFree))
+            return;
+        handoff[w * kBM + t] = make_float2(m, l);
+        ++n_st;
+        ptx::mbar_arrive(b.st_ready(w));
     }
 }
 
-// ------------------------------------------------------------------ correction + epilogue
+// ------------------------------------------------------------------ epilogue
 
+// Per finished Q tile: O = acc / l in the input type and LSE = (m + log2 l) ln 2,
+// then release O_w to the next tile's first P.V.
 template <int D, bool BF16, bool CAUSAL>
-__device__ void correction_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, const float2 *handoff)
+__device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, const float2 *handoff)
 {
     using C = Cfg<D>;
     const int t = threadIdx.x % 128;              // row within a Q tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(t & ~31) << 16;
-    uint32_t a_phase[2] = {0u, 0u}, o_phase[2] = {0u, 0u};
-    // Take one value pair from this row's softmax thread and release the slot.
-    auto take = [&](int w, float2 &v) -> bool {
-        if (!warp_wait(b.a_ready(w), a_phase[w] & 1u, c, kSiteCorrAReady))
-            return false;
-        ++a_phase[w];
-        v = handoff[w * kBM + t];
-        ptx::mbar_arrive(b.a_free(w));
-        return true;
-    };
+    uint32_t n_st[2] = {0u, 0u}, n_pv[2] = {0u, 0u};
 
     for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
         int bh, ct;
         decode_tile<CAUSAL>(tile, p, bh, ct);
-        const int nw[2] = {kv_tiles<CAUSAL>(ct, 0, p.N), kv_tiles<CAUSAL>(ct, 1, p.N)};
-        const int n = max(nw[0], nw[1]);
-        // Step j of Q tile w: O_w *= alpha before O_w += P_w(j) V_j.  Step 0
-        // needs no rescale (that MMA overwrites O_w) but still signals that the
-        // previous tile's epilogue has finished reading O_w.
-        for (int j = 0; j < n; ++j) {
-            for (int w = 0; w < kQTiles; ++w) {
-                if (j >= nw[w])
-                    continue;
-                float2 hv;
-                if (!take(w, hv))
-                    return;
-                if (j > 0) {
-                    const float alpha = hv.x;
-                    if (!warp_wait(b.o_done(w), o_phase[w] & 1u, c, kSiteCorrODone))
-                        return;
-                    ++o_phase[w];
-                    ptx::tc_fence_after_sync();
-                    if (!__all_sync(0xffffffffu, alpha == 1.f)) {
-                        const uint64_t a2 = ptx::f2_pack(alpha, alpha);
-                        const uint32_t tO = tmem + C::col_o(w) + lane_off;
 #pragma unroll
-                        for (int q = 0; q < D / 32; ++q) {
-                            uint32_t o[32];
-                            ptx::tmem_ld32(tO + q * 32, o);
-                            ptx::tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                uint64_t v = ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]),
-                                                                      __uint_as_float(o[2 * i + 1])), a2);
-                                float lo, hi;
-                                ptx::f2_unpack(v, lo, hi);
-                                o[2 * i] = __float_as_uint(lo);
-                                o[2 * i + 1] = __float_as_uint(hi);
-                            }
-                            ptx::tmem_st32(tO + q * 32, o);
-                        }
-                        ptx::tmem_wait_st();
-                    }
-                }
-                ptx::tc_fence_before_sync();
-                ptx::mbar_arrive(b.o_ready(w));
-            }
-        }
-        // Epilogue: O = acc / l in the input type, LSE = (m + log2 l) ln 2.
         for (int w = 0; w < kQTiles; ++w) {
-            if (nw[w] == 0)
+            const int nw = kv_tiles<CAUSAL>(ct, w, p.N);
+            if (nw == 0)
                 continue;
-            float2 st;
-            if (!take(w, st))
+            if (!warp_wait(b.st_ready(w), n_st[w] & 1u, c, kSiteEpiStReady))
                 return;
-            const float m = st.x;
-            const float l = st.y;
-            if (!warp_wait(b.o_done(w), o_phase[w] & 1u, c, kSiteCorrODone))
+            ++n_st[w];
+            const float2 st = handoff[w * kBM + t];
+            ptx::mbar_arrive(b.st_free(w));
+            n_pv[w] += (uint32_t)nw;   // the last P.V of this tile is completion n_pv - 1 of o_done(w)
+            if (!warp_wait(b.o_done(w), (n_pv[w] - 1) & 1u, c, kSiteEpiODone))
                 return;
-            ++o_phase[w];
             ptx::tc_fence_after_sync();
-            const float inv_l = 1.f / l;
+            const float inv_l = 1.f / st.y;
             const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
             const int row = ct * kCtaRows + w * kBM + t;
             const bool valid = row < p.N;
@@ -715,8 +693,9 @@ __device__ void correction_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ct
                 }
             }
             if (valid)
-                p.LSE[(size_t)bh * p.N + row] = (m + log2f(l)) * kLn2;
+                p.LSE[(size_t)bh * p.N + row] = (st.x + log2f(st.y)) * kLn2;
             ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(b.o_free(w));
         }
     }
 }
@@ -757,10 +736,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(b.s_full(w), 1);
             ptx::mbar_init(b.s_free(w), kBM);
             ptx::mbar_init(b.p_full(w), kBM);
-            ptx::mbar_init(b.a_ready(w), kBM);
-            ptx::mbar_init(b.a_free(w), kBM);
-            ptx::mbar_init(b.o_ready(w), kBM);
             ptx::mbar_init(b.o_done(w), 1);
+            ptx::mbar_init(b.st_ready(w), kBM);
+            ptx::mbar_init(b.st_free(w), kBM);
+            ptx::mbar_init(b.o_free(w), kBM);
         }
         ptx::mbar_init(b.drain(), 1);
         *c.abort_flag = 0;
@@ -780,12 +759,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc);
 
-    if (wg < kCorrWarpgroup) {
+    if (wg < kEpilogueWarpgroup) {
         ptx::regs_increase<kRegsSoftmax>();
         softmax_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff);
-    } else if (wg == kCorrWarpgroup) {
-        ptx::regs_decrease<kRegsCorrection>();
-        correction_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff);
+    } else if (wg == kEpilogueWarpgroup) {
+        ptx::regs_decrease<kRegsEpilogue>();
+        epilogue_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff);
     } else {
         ptx::regs_decrease<kRegsProducer>();
         if (warp == kLoadWarp)
