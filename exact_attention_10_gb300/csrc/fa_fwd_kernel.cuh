@@ -20,7 +20,7 @@
 //   warpgroup 1  the same for Q tile 1
 //   warpgroup 2  epilogue for both Q tiles: O = acc / l and LSE, written once per tile
 //   warpgroup 3  warp 12: TMA producer (Q tiles, then K_j and V_j into a stage ring)
-//                warp 13: tcgen05 MMA issuer and TMEM owner
+//                warps 13, 14: tcgen05 MMA issuers for Q tiles 0 and 1 (warp 13 owns TMEM)
 // Registers are rebalanced with setmaxnreg: the softmax warpgroups hold a
 // 128-score row per thread, the other two need little.  The producer warps
 // run as whole warps with one elected lane issuing, so their control state is
@@ -36,9 +36,10 @@
 //            (tcgen05 MMAs from one thread execute in issue order).
 // P feeds the P.V MMA as its TMEM A operand.
 //
-// MMA issue order per K/V step j:
-//   D = 64:  S0_{j+1}, S1_{j+1}, O0 += P0_j V_j, O1 += P1_j V_j
-//   D = 128: S0_j, O1 += P1_{j-1} V_{j-1}, S1_j, O0 += P0_j V_j
+// MMA issue order per K/V step j, per Q tile w (each tile has its own issuing
+// warp, so the two streams interleave on the tensor core by themselves):
+//   D = 64:  S_w(j+1) as soon as the softmax has loaded S_w(j), then O_w += P_w(j) V_j
+//   D = 128: S_w(j), then O_w += P_w(j) V_j once P_w(j) has overwritten S_w(j)
 // so each softmax warpgroup's work overlaps the other tile's MMAs.
 //
 // Softmax follows the exp2 form ("How to profile and optimise kernels", exp2):
@@ -83,7 +84,7 @@ constexpr int kCtaRows = kBM * kQTiles;
 constexpr int kThreads = 512;
 constexpr int kEpilogueWarpgroup = 2;
 constexpr int kLoadWarp = 12;
-constexpr int kMmaWarp = 13;
+constexpr int kMmaWarp = 13;          // MMA issuer(s): warp 13 (and 14 at D = 64)
 constexpr uint32_t kRegsSoftmax = 184;   // 2 x 128 x 184 + 128 x 56 + 128 x 88 = 65536 (launch: 512 x 128)
 constexpr uint32_t kRegsEpilogue = 56;
 constexpr uint32_t kRegsProducer = 88;
@@ -102,6 +103,10 @@ template <int D>
 struct Cfg {
     static_assert(D == 64 || D == 128, "head dimension 64 or 128");
     static constexpr bool kSeparateP = (D == 64);
+    // One MMA-issuing warp per Q tile at D = 64, where the many small MMAs of a
+    // step would outrun one issuer; one warp for both tiles at D = 128, where
+    // its interleaved order keeps the two softmax warpgroups out of phase.
+    static constexpr int kMmaWarps = (D == 64) ? 2 : 1;
     static constexpr int kBoxes = D / 64;              // 128-byte-wide TMA boxes per tile row
     static constexpr int kBoxBytes = kBM * 128;        // one [128 rows, 64 cols] 16-bit box
     static constexpr int kTileBytes = kBM * D * 2;     // one [128, D] 16-bit tile
@@ -312,25 +317,29 @@ __device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo)
     return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
 
-// The MMA-issuing warp.  The whole warp runs the control flow and the waits,
-// so loop state and descriptors stay warp-uniform; one elected lane (the
-// same lane every time, as tcgen05.commit tracks the MMAs of the lane that
-// issued them) issues the tcgen05.mma and tcgen05.commit instructions.
-// Everything per step is kept in scalar registers (tile indices are
-// compile-time): this warp's issue rate bounds the tensor pipe.
+// The MMA-issuing warps, one per Q tile.  A single thread issues a tcgen05.mma
+// only every ~60-80 cycles whatever its shape, so one issuer cannot keep the
+// tensor core busy with the small per-step MMAs of attention (N = 64 P.V at
+// D = 64); two issuers on different schedulers reach the full rate.  Each
+// warp runs its control flow and waits as a whole warp, so loop state and
+// descriptors stay warp-uniform; one elected lane (the same lane every time,
+// as tcgen05.commit tracks the MMAs of the lane that issued them) issues the
+// tcgen05.mma and tcgen05.commit instructions.  Tile-level ping-pong between
+// the two softmax warpgroups falls out of the two independent MMA streams.
 template <int D, bool BF16>
 struct MmaIssuer {
     using C = Cfg<D>;
     static constexpr uint32_t kIdescQK = instr_desc_f16(BF16, kBM, kBN, false);   // S = Q K^T, both K-major
     static constexpr uint32_t kIdescPV = instr_desc_f16(BF16, kBM, D, true);      // O += P V, V is MN-major
-    uint32_t q_lo;       // descriptor lower word of Q tile 0 (tile 1 is kTileBytes further)
+    int w;               // Q tile served by this warp
+    uint32_t q_lo;       // descriptor lower word of Q tile w in Q buffer 0
     uint32_t k_lo;       // descriptor lower word of K in stage 0, K-major (leading byte offset unused)
     uint32_t v_lo;       // same for V in stage 0 (MN-major: leading byte offset = box stride)
-    uint32_t tmem;
+    uint32_t tS, tO, tP; // TMEM columns of S_w, O_w, P_w
     Bars<D> b;
     Ctl c;
-    uint32_t n_s0, n_s1, n_pv0, n_pv1;   // S and P.V MMAs issued per Q tile
-    uint32_t n_t0, n_t1;                 // Q tiles whose first P.V has been issued, per Q tile slot
+    uint32_t n_s, n_pv, n_t;   // S and P.V MMAs issued, CTA tiles whose first P.V was issued
+    uint32_t q_cur;            // descriptor lower word of Q tile w in the current Q buffer
 
     __device__ bool stage_wait(int step, int &st) const
     {
@@ -341,6 +350,8 @@ struct MmaIssuer {
         return true;
     }
 
+    // Release a stage once this warp's MMAs reading it have completed (the
+    // empty barrier expects one such arrival from each MMA warp).
     __device__ void release(int st) const
     {
         if (ptx::elect_one())
@@ -350,123 +361,139 @@ struct MmaIssuer {
 
     // S_w = Q_w K^T over D/16 k-steps: K-major operands advance 32 bytes per
     // step inside a 128-byte swizzle row and 16 KB per 64-column box.
-    uint32_t q_cur;      // descriptor lower word of Q tile 0 in the current Q buffer
-
-    template <int W>
     __device__ bool issue_s(int st)
     {
-        uint32_t &n = W ? n_s1 : n_s0;
-        if (C::kSeparateP && n > 0) {   // the softmax has loaded the previous S_w
-            if (!warp_wait(b.s_free(W), (n - 1) & 1u, c, kSiteMmaSFree))
+        if (C::kSeparateP && n_s > 0) {   // the softmax has loaded the previous S_w
+            if (!warp_wait(b.s_free(w), (n_s - 1) & 1u, c, kSiteMmaSFree))
                 return false;
             ptx::tc_fence_after_sync();
         }
-        const uint32_t qa = q_cur + (uint32_t)(W * C::kTileBytes >> 4);
         const uint32_t ka = k_lo + (uint32_t)(st * (C::kStageBytes >> 4));
         if (ptx::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (uint32_t)((kk / 4) * (C::kBoxBytes >> 4) + (kk % 4) * 2);
-                ptx::mma_ss(tmem + C::col_s(W), desc_from_lo(qa + off), desc_from_lo(ka + off), kIdescQK,
-                            kk > 0 ? 1u : 0u);
+                ptx::mma_ss(tS, desc_from_lo(q_cur + off), desc_from_lo(ka + off), kIdescQK, kk > 0 ? 1u : 0u);
             }
-            ptx::mma_commit(b.s_full(W));
+            ptx::mma_commit(b.s_full(w));
         }
         __syncwarp();
-        ++n;
+        ++n_s;
         return true;
     }
 
     // O_w (+)= P_w V over 128/16 k-steps: P from TMEM (8 columns per step),
     // V MN-major: 16 key rows = 2 KB per step.
-    template <int W>
     __device__ bool issue_pv(int st, bool accumulate)
     {
-        uint32_t &n = W ? n_pv1 : n_pv0;
-        uint32_t &nt = W ? n_t1 : n_t0;
         if (!accumulate) {   // first P.V of a CTA tile overwrites O_w: the epilogue must have read it
-            if (nt > 0 && !warp_wait(b.o_free(W), (nt - 1) & 1u, c, kSiteMmaOFree))
+            if (n_t > 0 && !warp_wait(b.o_free(w), (n_t - 1) & 1u, c, kSiteMmaOFree))
                 return false;
-            ++nt;
+            ++n_t;
         }
-        if (!warp_wait(b.p_full(W), n & 1u, c, kSiteMmaPFull))
+        if (!warp_wait(b.p_full(w), n_pv & 1u, c, kSiteMmaPFull))
             return false;
         ptx::tc_fence_after_sync();
         const uint32_t va = v_lo + (uint32_t)(st * (C::kStageBytes >> 4));
         if (ptx::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-                ptx::mma_ts(tmem + C::col_o(W), tmem + C::col_p(W) + kk * 8, desc_from_lo(va + kk * (2048 >> 4)),
-                            kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-            ptx::mma_commit(b.o_done(W));
+                ptx::mma_ts(tO, tP + kk * 8, desc_from_lo(va + kk * (2048 >> 4)), kIdescPV,
+                            (accumulate || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(b.o_done(w));
         }
         __syncwarp();
-        ++n;
+        ++n_pv;
         return true;
     }
 
-    // D = 64 order: S of step j+1 for both tiles, then P.V of step j.
-    __device__ bool tile_separate_p(int step0, int n, int n0, int n1)
+    // One CTA tile: steps 0..n-1 of the K/V stream, of which Q tile w uses the
+    // first nw.  Every stage is released by this warp, used or not.
+    __device__ bool tile(int step0, int n, int nw)
     {
-        int st, st_next;
-        if (!stage_wait(step0, st))
-            return false;
-        if (n0 > 0 && !issue_s<0>(st))
-            return false;
-        if (n1 > 0 && !issue_s<1>(st))
-            return false;
-        for (int j = 0; j < n; ++j) {
-            if (j + 1 < n) {
-                if (!stage_wait(step0 + j + 1, st_next))
+        int st;
+        if (C::kSeparateP) {
+            // D = 64 order: S_w of step j+1 as soon as the softmax has loaded S_w(j),
+            // then P.V of step j.
+            if (!stage_wait(step0, st))
+                return false;
+            if (nw > 0 && !issue_s(st))
+                return false;
+            for (int j = 0; j < n; ++j) {
+                int st_next = st;
+                if (j + 1 < n) {
+                    if (!stage_wait(step0 + j + 1, st_next))
+                        return false;
+                    if (j + 1 < nw && !issue_s(st_next))
+                        return false;
+                }
+                if (j < nw && !issue_pv(st, j > 0))
                     return false;
-                if (j + 1 < n0 && !issue_s<0>(st_next))
-                    return false;
-                if (j + 1 < n1 && !issue_s<1>(st_next))
-                    return false;
+                release(st);
+                st = st_next;
             }
-            if (j < n0 && !issue_pv<0>(st, j > 0))
-                return false;
-            if (j < n1 && !issue_pv<1>(st, j > 0))
-                return false;
-            release(st);   // K_j and V_j both read
-            st = st_next;
-        }
-        return true;
-    }
-
-    // D = 128 order: S0_j, P.V1_{j-1}, S1_j, P.V0_j (P overwrites S in TMEM).
-    __device__ bool tile_aliased_p(int step0, int n, int n0, int n1)
-    {
-        int st, prev = -1;
-        for (int j = 0; j < n; ++j) {
-            if (!stage_wait(step0 + j, st))
-                return false;
-            if (j < n0 && !issue_s<0>(st))
-                return false;
-            if (j >= 1) {
-                if (j - 1 < n1 && !issue_pv<1>(prev, j - 1 > 0))
+        } else {
+            // D = 128 order: S_w(j), then P.V_w(j) once P_w(j) overwrote S_w(j) in TMEM;
+            // S_w(j+1) follows in issue order.
+            for (int j = 0; j < n; ++j) {
+                if (!stage_wait(step0 + j, st))
                     return false;
-                release(prev);   // K_{j-1} and V_{j-1} both read
+                if (j < nw && (!issue_s(st) || !issue_pv(st, j > 0)))
+                    return false;
+                release(st);
             }
-            if (j < n1 && !issue_s<1>(st))
-                return false;
-            if (j < n0 && !issue_pv<0>(st, j > 0))
-                return false;
-            prev = st;
         }
-        if (n - 1 < n1 && !issue_pv<1>(prev, n - 1 > 0))
-            return false;
-        release(prev);
         return true;
     }
 };
 
+// One warp for both Q tiles (D = 128): per step S0_j, P.V1_{j-1}, S1_j, P.V0_j,
+// so each softmax warpgroup works while the tensor core runs the other
+// tile's MMAs, and P_w(j) overwrites S_w(j) in TMEM before S_w(j+1) is issued.
+template <int D, bool BF16>
+__device__ bool tile_interleaved(MmaIssuer<D, BF16> &m0, MmaIssuer<D, BF16> &m1, int step0, int n, int n0, int n1)
+{
+    int st, prev = -1;
+    for (int j = 0; j < n; ++j) {
+        if (!m0.stage_wait(step0 + j, st))
+            return false;
+        if (j < n0 && !m0.issue_s(st))
+            return false;
+        if (j >= 1) {
+            if (j - 1 < n1 && !m1.issue_pv(prev, j - 1 > 0))
+                return false;
+            m0.release(prev);   // K_{j-1} and V_{j-1} both read
+        }
+        if (j < n1 && !m1.issue_s(st))
+            return false;
+        if (j < n0 && !m0.issue_pv(st, j > 0))
+            return false;
+        prev = st;
+    }
+    if (n - 1 < n1 && !m1.issue_pv(prev, n - 1 > 0))
+        return false;
+    m0.release(prev);
+    return true;
+}
+
 template <int D, bool BF16, bool CAUSAL>
-__device__ void mma_role(const FwdParams &p, uint32_t sQ, uint32_t sStage, uint32_t tmem, Bars<D> b, Ctl c)
+__device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage, uint32_t tmem, Bars<D> b, Ctl c)
 {
     using C = Cfg<D>;
-    MmaIssuer<D, BF16> m{desc_lo(sQ, 16), desc_lo(sStage, 16), desc_lo(sStage + C::kTileBytes, C::kBoxBytes),
-                         tmem, b, c, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    auto make = [&](int q) {
+        return MmaIssuer<D, BF16>{q,
+                                  desc_lo(sQ + q * C::kTileBytes, 16),
+                                  desc_lo(sStage, 16),
+                                  desc_lo(sStage + C::kTileBytes, C::kBoxBytes),
+                                  tmem + C::col_s(q),
+                                  tmem + C::col_o(q),
+                                  tmem + C::col_p(q),
+                                  b,
+                                  c,
+                                  0u, 0u, 0u, 0u};
+    };
+    MmaIssuer<D, BF16> m = make(w);                 // this warp's tile (D = 64) or tile 0 (D = 128)
+    MmaIssuer<D, BF16> m1 = make(1);                // tile 1 when one warp serves both
     int step = 0, it = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
         int bh, ct;
@@ -478,11 +505,12 @@ __device__ void mma_role(const FwdParams &p, uint32_t sQ, uint32_t sStage, uint3
             break;
         ptx::tc_fence_after_sync();
         m.q_cur = m.q_lo + (uint32_t)(qb * (C::kQBufBytes >> 4));
-        const bool ok = C::kSeparateP ? m.tile_separate_p(step, n, n0, n1) : m.tile_aliased_p(step, n, n0, n1);
+        m1.q_cur = m1.q_lo + (uint32_t)(qb * (C::kQBufBytes >> 4));
+        const bool ok = (C::kMmaWarps == 2) ? m.tile(step, n, w ? n1 : n0) : tile_interleaved(m, m1, step, n, n0, n1);
         if (!ok)
             break;
         step += n;
-        if (ptx::elect_one())
+        if (ptx::elect_one())   // Q buffer free once this warp's S MMAs of the tile completed
             ptx::mma_commit(b.q_empty(qb));
         __syncwarp();
     }
@@ -568,17 +596,12 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             const float alpha = move ? ptx::ex2(m - m_use) : 1.f;     // 0 on the first tile (m = -inf)
             const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
 
-            if (C::kSeparateP && j > 0) {   // P.V of step j-1 done: P_w may be overwritten, O_w is final
-                if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
-                    return;
-                ++o_phase;
-                ptx::tc_fence_after_sync();
-            }   // (D = 128: S_w(j) is issued after P.V_w(j-1), so s_full already implies it)
-
+            // Exponentials into packed 16-bit pairs first (registers only), so
+            // they overlap the previous step's P.V, which still reads P_w.
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+            uint32_t pk[2][32];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const uint64_t x = ptx::f2_fma(ptx::f2_pack(s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1]), qk2, negm2);
@@ -586,10 +609,17 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
                     ptx::f2_unpack(x, x0, x1);
                     const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
                     acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
-                    pk[i] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
+                    pk[h][i] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
                 }
-                ptx::tmem_st32(tP + h * 32, pk);
             }
+            if (C::kSeparateP && j > 0) {   // P.V of step j-1 done: P_w may be overwritten, O_w is final
+                if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
+                    return;
+                ++o_phase;
+                ptx::tc_fence_after_sync();
+            }   // (D = 128: S_w(j) is issued after P.V_w(j-1), so s_full already implies it)
+            ptx::tmem_st32(tP, pk[0]);
+            ptx::tmem_st32(tP + 32, pk[1]);
             const uint64_t a2 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
             float a_lo, a_hi;
             ptx::f2_unpack(a2, a_lo, a_hi);
@@ -726,11 +756,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(b.full(s), 1);
-            ptx::mbar_init(b.empty(s), 1);
+            ptx::mbar_init(b.empty(s), C::kMmaWarps);
         }
         for (int qb = 0; qb < C::kQBufs; ++qb) {
             ptx::mbar_init(b.q_full(qb), 1);
-            ptx::mbar_init(b.q_empty(qb), 1);
+            ptx::mbar_init(b.q_empty(qb), C::kMmaWarps);
         }
         for (int w = 0; w < kQTiles; ++w) {
             ptx::mbar_init(b.s_full(w), 1);
@@ -741,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(b.st_free(w), kBM);
             ptx::mbar_init(b.o_free(w), kBM);
         }
-        ptx::mbar_init(b.drain(), 1);
+        ptx::mbar_init(b.drain(), C::kMmaWarps);
         *c.abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -769,8 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::regs_decrease<kRegsProducer>();
         if (warp == kLoadWarp)
             load_role<D, CAUSAL>(&tmQ, &tmK, &tmV, p, sQ, sStage, b, c);
-        else if (warp == kMmaWarp)
-            mma_role<D, BF16, CAUSAL>(p, sQ, sStage, tmem, b, c);
+        else if (warp < kMmaWarp + C::kMmaWarps)
+            mma_role<D, BF16, CAUSAL>(warp - kMmaWarp, p, sQ, sStage, tmem, b, c);
     }
 
     ptx::tc_fence_before_sync();
