@@ -119,7 +119,8 @@ def _traffic_record(kernel_name: str):
     except (OSError, ValueError):
         return None
     h = hashlib.sha256()
-    for rel in ("exact_attention_10_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_10_gb300/csrc/sm103_ptx.cuh"):
+    for rel in ("exact_attention_10_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_10_gb300/csrc/sm103_ptx.cuh",
+                "exact_attention_10_gb300/csrc/fa_schedule.h"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     entry = rec.get(kernel_name)

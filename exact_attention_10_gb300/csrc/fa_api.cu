@@ -150,13 +150,85 @@ fa_status dispatch_dtype(bool bf16, bool causal, const CUtensorMap &q, const CUt
                   : launch_variant<D, false, false>(q, k, v, p, grid, s, dev);
 }
 
+// Per-(device, stream) workspace for split tiles: partial O and (m, l) for
+// two slots per CTA, and one counter per (tile, Q tile) that must be zero
+// when a launch starts (each launch leaves it zero).  Allocated on the first
+// call that needs it on that stream and grown when a later call needs more;
+// calls on different streams never share one, so they cannot race.
+struct Workspace {
+    int dev;
+    cudaStream_t stream;
+    void *ptr;
+    size_t bytes;
+    size_t counter_bytes;
+};
+constexpr int kMaxWorkspaces = 64;
+Workspace g_ws[kMaxWorkspaces];
+int g_ws_count = 0;
+
+fa_status workspace_for(int dev, cudaStream_t stream, const fa::Schedule &sc, int D, fa::FwdParams *p)
+{
+    const size_t slots = (size_t)2 * sc.G;
+    const size_t o_bytes = slots * fa::kCtaRows * D * sizeof(float);
+    const size_t ml_bytes = slots * fa::kCtaRows * sizeof(float2);
+    const size_t cnt_bytes = (size_t)2 * sc.T * sizeof(int);
+    const size_t need = o_bytes + ml_bytes + cnt_bytes;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace *w = nullptr;
+    for (int i = 0; i < g_ws_count; ++i)
+        if (g_ws[i].dev == dev && g_ws[i].stream == stream)
+            w = &g_ws[i];
+    if (!w) {
+        if (g_ws_count == kMaxWorkspaces)
+            return FA_ERR_CUDA;
+        w = &g_ws[g_ws_count++];
+        *w = Workspace{dev, stream, nullptr, 0, 0};
+    }
+    if (w->bytes < need) {
+        if (w->ptr) {
+            // work already queued on this stream may still use the old buffer
+            if (cudaStreamSynchronize(stream) != cudaSuccess || cudaFree(w->ptr) != cudaSuccess) {
+                cudaGetLastError();
+                return FA_ERR_CUDA;
+            }
+            w->ptr = nullptr;
+            w->bytes = 0;
+        }
+        if (cudaMalloc(&w->ptr, need) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_CUDA;
+        }
+        w->bytes = need;
+        w->counter_bytes = 0;
+    }
+    // Counters sit at the end of the buffer and must be zero when a launch
+    // starts.  Launches leave them zero, so they are cleared only when the
+    // buffer is new or has grown (and after an expired in-kernel wait, by
+    // fa_sync_status).
+    const size_t cnt_off = w->bytes - cnt_bytes;
+    if (w->counter_bytes != cnt_bytes) {
+        if (cudaMemsetAsync(static_cast<char *>(w->ptr) + cnt_off, 0, cnt_bytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_CUDA;
+        }
+        w->counter_bytes = cnt_bytes;
+    }
+    p->part_o = static_cast<float *>(w->ptr);
+    p->part_ml = reinterpret_cast<float2 *>(static_cast<char *>(w->ptr) + o_bytes);
+    p->counters = reinterpret_cast<int *>(static_cast<char *>(w->ptr) + cnt_off);
+    return FA_OK;
+}
+
 }  // namespace
 
-extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
-                            int D, int causal, float scale, fa_dtype dtype, fa_stream_t stream)
+extern "C" fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                               int N, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
+                               fa_stream_t stream)
 {
     // Arguments first: nothing below touches the device until they are sound.
     if (dtype != FA_BF16 && dtype != FA_FP16)
+        return FA_ERR_INVALID_VALUE;
+    if (schedule != FA_SCHEDULE_AUTO && schedule != FA_SCHEDULE_WHOLE_TILES && schedule != FA_SCHEDULE_BALANCED)
         return FA_ERR_INVALID_VALUE;
     if (D != 64 && D != 128)
         return FA_ERR_INVALID_VALUE;
@@ -199,19 +271,27 @@ extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O
         !encode_map(&tv, V, (int)BH, N, D, bf16))
         return FA_ERR_CUDA;
 
-    fa::FwdParams p;
+    fa::FwdParams p{};
     p.O = O;
     p.LSE = LSE;
     p.N = N;
-    p.BH = (int)BH;
-    p.ctiles_per_bh = (N + fa::kCtaRows - 1) / fa::kCtaRows;
-    p.total_tiles = p.BH * p.ctiles_per_bh;
     p.qk_scale = scale * 1.4426950408889634f;   // scale * log2(e)
-    const int grid = p.total_tiles < di->sms ? p.total_tiles : di->sms;
+    p.sch = fa::sched_plan(N, (int)BH, causal != 0, di->sms, (int)schedule);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (p.sch.split) {
+        const fa_status ws = workspace_for(dev, s, p.sch, D, &p);
+        if (ws != FA_OK)
+            return ws;
+    }
     if (D == 64)
-        return dispatch_dtype<64>(bf16, causal != 0, tq, tk, tv, p, grid, s, dev);
-    return dispatch_dtype<128>(bf16, causal != 0, tq, tk, tv, p, grid, s, dev);
+        return dispatch_dtype<64>(bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
+    return dispatch_dtype<128>(bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
+}
+
+extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
+                            int D, int causal, float scale, fa_dtype dtype, fa_stream_t stream)
+{
+    return fa_fwd_ex(Q, K, V, O, LSE, B, H, N, D, causal, scale, dtype, FA_SCHEDULE_AUTO, stream);
 }
 
 extern "C" fa_status fa_sync_status(fa_stream_t stream)
@@ -226,6 +306,15 @@ extern "C" fa_status fa_sync_status(fa_stream_t stream)
         return FA_ERR_CUDA;
     }
     if (word != 0) {
+        // an aborted launch may have left split-tile counters non-zero
+        int dev = -1;
+        cudaGetDevice(&dev);
+        {
+            std::lock_guard<std::mutex> lock(g_mu);
+            for (int i = 0; i < g_ws_count; ++i)
+                if (g_ws[i].dev == dev && g_ws[i].ptr)
+                    g_ws[i].counter_bytes = 0;   // cleared again by the next call that uses it
+        }
         const unsigned int zero = 0;
         if (cudaMemcpyToSymbol(fa::g_status_word, &zero, sizeof zero) != cudaSuccess) {
             cudaGetLastError();

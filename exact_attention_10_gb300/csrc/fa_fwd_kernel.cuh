@@ -69,6 +69,7 @@
 #include <cuda.h>
 #include <cstdint>
 
+#include "fa_schedule.h"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -85,10 +86,13 @@ constexpr int kThreads = 512;
 constexpr int kEpilogueWarpgroup = 2;
 constexpr int kLoadWarp = 12;
 constexpr int kMmaWarp = 13;          // MMA issuer(s): warp 13 (and 14 at D = 64)
-constexpr uint32_t kRegsSoftmax = 184;   // 2 x 128 x 184 + 128 x 56 + 128 x 88 = 65536 (launch: 512 x 128)
-constexpr uint32_t kRegsEpilogue = 56;
-constexpr uint32_t kRegsProducer = 88;
+constexpr uint32_t kRegsSoftmax = 184;   // 2 x 128 x 184 + 128 x 64 + 128 x 80 = 65536 (launch: 512 x 128)
+constexpr uint32_t kRegsEpilogue = 64;
+constexpr uint32_t kRegsProducer = 80;
 constexpr int kPerTileBars = 7;
+constexpr int kMergeBufs = 3;            // merge staging buffers in flight
+constexpr int kMergeOBytes = 8192;       // partial O bytes per staging buffer
+constexpr int kMaxMergeParts = kSchedMaxParts;   // parts of one split tile, at most (the planner keeps to it)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -96,7 +100,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 enum : uint32_t {
     kSiteLoadQEmpty = 1, kSiteLoadSlotEmpty, kSiteMmaQFull, kSiteMmaSlotFull, kSiteMmaPFull, kSiteMmaOFree,
     kSiteMmaSFree, kSiteSoftSFull, kSiteSoftODone, kSiteSoftStFree, kSiteEpiStReady, kSiteEpiODone, kSiteDrain,
-    kSiteTail
+    kSiteTail, kSiteMerge, kSiteMergeTail
 };
 
 template <int D>
@@ -119,10 +123,18 @@ struct Cfg {
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
     // full[kStages], empty[kStages], q_full[kQBufs], q_empty[kQBufs], then per
     // Q tile: s_full, s_free, p_full, o_done, st_ready, st_free, o_free; then drain
-    static constexpr int kNumBars = 2 * kStages + 2 * kQBufs + kPerTileBars * kQTiles + 1;
+    static constexpr int kNumBars = 2 * kStages + 2 * kQBufs + kPerTileBars * kQTiles + 1 + kMergeBufs;
     static constexpr int kHandOff = kBarOff + kNumBars * 8;            // float2 [2 tiles][128]
     static constexpr int kMiscOff = kHandOff + kQTiles * kBM * 8;
-    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + slack to align the base to 1024
+    // Merge staging: kMergeBufs buffers, each the partial O of kMergeRows rows
+    // of one part; the merge weights, fp32 [kMaxMergeParts][128 rows]; the
+    // global address of each part's partial O for the Q tile, u64 [kMaxMergeParts].
+    static constexpr int kMergeRows = kMergeOBytes / (D * 4);
+    static constexpr int kMergeOff = (kMiscOff + 16 + 127) & ~127;
+    static constexpr int kWeightOff = kMergeOff + kMergeBufs * kMergeOBytes;
+    static constexpr int kSlotOff = kWeightOff + kMaxMergeParts * kBM * 4;   // u64: each part's partial O of the Q tile
+    static constexpr int kSmemBytes = kSlotOff + kMaxMergeParts * 8 + 1024;   // + slack to align the base to 1024
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t col_s(int w) { return w ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t col_o(int w) { return w ? 256u + D : 256u; }
@@ -133,10 +145,11 @@ struct FwdParams {
     void *O;
     float *LSE;
     int N;
-    int BH;
-    int ctiles_per_bh;   // ceil(N / 256)
-    int total_tiles;     // BH * ctiles_per_bh
     float qk_scale;      // scale * log2(e)
+    Schedule sch;        // work decomposition (fa_schedule.h)
+    float *part_o;       // balanced schedule: partial O, [2 * grid slots][256 rows][D] fp32
+    float2 *part_ml;     // balanced schedule: partial (m, l) per row, [2 * grid slots][256]
+    int *counters;       // balanced schedule: finished parts per (tile, Q tile), zero between launches
 };
 
 // Shared-memory matrix descriptor (tcgen05), 128-byte swizzle, 8-row groups
@@ -154,29 +167,12 @@ __host__ __device__ constexpr uint32_t instr_desc_f16(bool bf16, int M, int N, b
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-template <bool CAUSAL>
-__device__ __forceinline__ void decode_tile(int t, const FwdParams &p, int &bh, int &ct)
+// Q-tile step count within a part: Q tile w of the part's tile visits steps
+// [0, nw); the part covers [kb, ke); its share is [kb, min(ke, nw)).
+__device__ __forceinline__ int part_steps(const Part &pt, int nw)
 {
-    if (CAUSAL) {   // longest first, heads interleaved
-        ct = p.ctiles_per_bh - 1 - t / p.BH;
-        bh = t % p.BH;
-    } else {        // head-major: neighbouring CTAs share a head's K/V in L2
-        bh = t / p.ctiles_per_bh;
-        ct = t % p.ctiles_per_bh;
-    }
-}
-
-// K/V tiles visited by Q tile w of CTA tile ct; 0 if it holds no valid row.
-template <bool CAUSAL>
-__device__ __forceinline__ int kv_tiles(int ct, int w, int N)
-{
-    const int r0 = ct * kCtaRows + w * kBM;
-    if (r0 >= N)
-        return 0;
-    if (!CAUSAL)
-        return (N + kBN - 1) / kBN;
-    const int last = min(r0 + kBM - 1, N - 1);
-    return last / kBN + 1;
+    const int e = (pt.ke < nw) ? pt.ke : nw;
+    return (e > pt.kb) ? e - pt.kb : 0;
 }
 
 struct Ctl {
@@ -189,16 +185,20 @@ __device__ __noinline__ void record_timeout(Ctl c, uint32_t site)
     atomicCAS(&g_status_word, 0u, 1u | (site << 8));
 }
 
-// Bounded wait by one thread; false if it gave up (timeout or abort).
+// Bounded wait by one thread; false if it gave up (timeout or abort).  After a
+// first test, each poll lets the thread sleep until the phase completes (up to
+// kSuspendNs), so waiting warps leave the issue slots to the warps computing.
+constexpr uint32_t kSuspendNs = 20000;
+
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Ctl c, uint32_t site)
 {
     if (ptx::mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = ptx::global_timer_ns();
     for (uint32_t spin = 1;; ++spin) {
-        if (ptx::mbar_try_wait(bar, parity))
+        if (ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs))
             return true;
-        if ((spin & 63u) == 0) {
+        if ((spin & 7u) == 0) {
             if (*c.abort_flag)
                 return false;
             if (ptx::global_timer_ns() - t0 > kWaitLimitNs) {
@@ -235,6 +235,7 @@ struct Bars {
     __device__ uint32_t st_free(int w) const { return per_tile(w, 5); }    // epilogue -> softmax: (m, l) read
     __device__ uint32_t o_free(int w) const { return per_tile(w, 6); }     // epilogue -> MMA: O_w read out
     __device__ uint32_t drain() const { return per_tile(kQTiles, 0); }
+    __device__ uint32_t merge_full(int i) const { return per_tile(kQTiles, 1 + i); }   // bulk copy -> merge: buffer i landed
 };
 
 // ------------------------------------------------------------------ producer
@@ -248,12 +249,14 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
 {
     using C = Cfg<D>;
     int step = 0;   // K/V stages filled so far
-    int it = 0;     // CTA tiles started by this CTA
+    int it = 0;     // parts started by this CTA (one Q load each)
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
+    PartIter parts;
+    parts.init(p.sch, blockIdx.x);
+    Part pt;
+    while (ok && parts.next(p.sch, pt)) {
         int bh, ct;
-        decode_tile<CAUSAL>(t, p, bh, ct);
-        const int n = max(kv_tiles<CAUSAL>(ct, 0, p.N), kv_tiles<CAUSAL>(ct, 1, p.N));
+        sched_decode(p.sch, pt.tile, bh, ct);
         const int qb = it % C::kQBufs;
         const uint32_t quse = (uint32_t)(it / C::kQBufs);
         if (!warp_wait(b.q_empty(qb), (quse & 1u) ^ 1u, c, kSiteLoadQEmpty)) { ok = false; break; }
@@ -266,7 +269,8 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
                                      ct * kCtaRows + w * kBM, bh);
         }
         __syncwarp();
-        for (int j = 0; j < n; ++j, ++step) {
+        ++it;
+        for (int j = pt.kb; j < pt.ke; ++j, ++step) {
             const int st = step % C::kStages;
             const uint32_t use = (uint32_t)(step / C::kStages);
             if (!warp_wait(b.empty(st), (use & 1u) ^ 1u, c, kSiteLoadSlotEmpty)) { ok = false; break; }
@@ -495,11 +499,14 @@ __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage
     MmaIssuer<D, BF16> m = make(w);                 // this warp's tile (D = 64) or tile 0 (D = 128)
     MmaIssuer<D, BF16> m1 = make(1);                // tile 1 when one warp serves both
     int step = 0, it = 0;
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+    PartIter parts;
+    parts.init(p.sch, blockIdx.x);
+    Part pt;
+    while (parts.next(p.sch, pt)) {
         int bh, ct;
-        decode_tile<CAUSAL>(t, p, bh, ct);
-        const int n0 = kv_tiles<CAUSAL>(ct, 0, p.N), n1 = kv_tiles<CAUSAL>(ct, 1, p.N);
-        const int n = max(n0, n1);
+        sched_decode(p.sch, pt.tile, bh, ct);
+        const int n0 = part_steps(pt, sched_kv_tiles(p.sch, ct, 0)), n1 = part_steps(pt, sched_kv_tiles(p.sch, ct, 1));
+        const int n = pt.ke - pt.kb;
         const int qb = it % C::kQBufs;
         if (!warp_wait(b.q_full(qb), (uint32_t)(it / C::kQBufs) & 1u, c, kSiteMmaQFull))
             break;
@@ -510,9 +517,10 @@ __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage
         if (!ok)
             break;
         step += n;
-        if (ptx::elect_one())   // Q buffer free once this warp's S MMAs of the tile completed
+        if (ptx::elect_one())   // Q buffer free once this warp's S MMAs of the part completed
             ptx::mma_commit(b.q_empty(qb));
         __syncwarp();
+        ++it;
     }
     // Drain: all MMAs this warp issued have completed before TMEM is freed.
     if (ptx::elect_one())
@@ -536,17 +544,22 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
     const uint64_t qk2 = ptx::f2_pack(p.qk_scale, p.qk_scale);
     uint32_t s_phase = 0, o_phase = 0, n_st = 0;
 
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    PartIter parts;
+    parts.init(p.sch, blockIdx.x);
+    Part pt;
+    while (parts.next(p.sch, pt)) {
         int bh, ct;
-        decode_tile<CAUSAL>(tile, p, bh, ct);
-        const int nw = kv_tiles<CAUSAL>(ct, w, p.N);
-        if (nw == 0)
+        sched_decode(p.sch, pt.tile, bh, ct);
+        const int nw = sched_kv_tiles(p.sch, ct, w);    // steps of this Q tile in the whole tile
+        const int np = part_steps(pt, nw);              // ... of which this part holds steps kb .. kb + np - 1
+        if (np == 0)
             continue;
         const int row = ct * kCtaRows + w * kBM + t;                // query index (may be >= N: padding)
         const int row_limit = CAUSAL ? min(p.N, row + 1) : p.N;     // keys < row_limit are visible
         float m = -INFINITY, l = 0.f;                               // running max (log2 units), row sum
 
-        for (int j = 0; j < nw; ++j) {
+        for (int jr = 0; jr < np; ++jr) {
+            const int j = pt.kb + jr;   // K/V step within the tile
             if (!warp_wait(b.s_full(w), s_phase & 1u, c, kSiteSoftSFull))
                 return;
             ++s_phase;
@@ -612,7 +625,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
                     pk[h][i] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
                 }
             }
-            if (C::kSeparateP && j > 0) {   // P.V of step j-1 done: P_w may be overwritten, O_w is final
+            if (C::kSeparateP && jr > 0) {   // P.V of the previous step done: P_w may be overwritten, O_w is final
                 if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
                     return;
                 ++o_phase;
@@ -628,7 +641,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
 
             // O_w *= alpha for the rows of this warp, skipped when no row's max
             // moved (ever less likely as more keys have been seen).
-            if (j > 0 && __any_sync(0xffffffffu, move)) {
+            if (jr > 0 && __any_sync(0xffffffffu, move)) {
                 const uint64_t al2 = ptx::f2_pack(alpha, alpha);
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
@@ -667,65 +680,337 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
 
 // ------------------------------------------------------------------ epilogue
 
-// Per finished Q tile: O = acc / l in the input type and LSE = (m + log2 l) ln 2,
-// then release O_w to the next tile's first P.V.
+// Epilogue warps sync among themselves (named barrier 1, 128 threads).
+__device__ __forceinline__ void epilogue_sync()
+{
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Epilogue warps sync and agree (named barrier 2): true iff `ok` held in every
+// thread.  Keeps the warpgroup's decisions to leave uniform, so that no warp
+// is left waiting at a barrier that the others have left.
+__device__ __forceinline__ bool epilogue_all(bool ok)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
+}
+
+// Wait bounded by time alone (not by the abort flag): for copies in flight
+// that must land before the CTA may exit.
+__device__ __forceinline__ void wait_landed(uint32_t bar, uint32_t parity, Ctl c, uint32_t site)
+{
+    const uint64_t t0 = ptx::global_timer_ns();
+    while (!ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs)) {
+        if (ptx::global_timer_ns() - t0 > kWaitLimitNs) {
+            record_timeout(c, site);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ float4 ld_cg_f4(const float *p)
+{
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float2 ld_cg_f2(const float2 *p)
+{
+    float2 v;
+    asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
+
+// Merge the partial results of one Q tile of a split tile: with per-part row
+// max m_k and sum l_k (log2 units) and O_k normalised by l_k,
+//   M = max_k m_k,  L = sum_k l_k 2^(m_k - M),  O = sum_k (l_k 2^(m_k - M) / L) O_k,
+//   LSE = (M + log2 L) ln 2
+// -- the same rescaling identity the recurrence uses between K/V tiles
+// ("A09 - Advanced Triton & FlashAttention", 3. Deep Dive).  Every row of a Q
+// tile sees at least one key in each of the tile's steps (the diagonal step
+// starts at the Q tile's first row), so each part's m_k is finite.
+//
+// The epilogue warps share their schedulers with the busy softmax warps, so
+// the merge keeps its instruction count low: first each thread takes one row,
+// computes the weights l_k 2^(m_k - M) / L of all parts into shared memory and
+// writes LSE; then the partial O streams through kMergeBufs shared-memory
+// buffers by bulk copies (a chunk: kMergeRows rows of one part, in the order
+// row block, part), each thread adding weight x O for 4 columns of 4 rows of
+// a chunk.  `issued` counts the chunks this CTA has streamed (buffer g %
+// kMergeBufs, phase g / kMergeBufs of chunk g).  False if a wait gave up; the
+// copies in flight have landed by then.
+template <int D, bool BF16>
+__device__ __noinline__ bool merge_parts(const FwdParams &p, int tile, int nw, int w, int bh, int ct, uint32_t sbuf,
+                                         uint32_t sweights, uint32_t saddr, Bars<D> b, uint32_t &issued, Ctl c)
+{
+    using C = Cfg<D>;
+    constexpr int R = C::kMergeRows;              // 32 or 16 rows per chunk
+    constexpr int kTpr = D / 4;                   // threads per row of a chunk
+    constexpr int kPos = R * kTpr / kBM;          // positions (4 columns of a row) per thread: 4
+    constexpr int kRowStep = kBM / kTpr;          // rows between a thread's positions: 8 or 4
+    const int t = threadIdx.x % kBM;
+    int pt, n, clo, chi, slot;
+    sched_tile_ctas(p.sch, tile, pt, n, clo, chi);
+    int nparts = 0;
+    for (int cc = clo; cc <= chi; ++cc)
+        if (sched_part_slot(p.sch, pt, n, nw, cc, slot)) {
+            if (t == nparts && nparts < kMaxMergeParts)   // thread k notes part k's partial O
+                ptx::st_shared_u64(saddr + 8 * t,
+                                   reinterpret_cast<uint64_t>(p.part_o + ((size_t)slot * kCtaRows + w * kBM) * D));
+            ++nparts;
+        }
+    nparts = (nparts < kMaxMergeParts) ? nparts : kMaxMergeParts;
+    const int r_base = ct * kCtaRows + w * kBM;   // first row of the Q tile in the head
+    const int nrows = (p.N - r_base < kBM) ? p.N - r_base : kBM;
+    const int nchunks = ((nrows + R - 1) / R) * nparts;
+    const uint32_t first = issued;
+
+    // Chunk k = (row block rb, part pi) goes to buffer (first + k) % kMergeBufs.
+    int i_rb = 0, i_pi = 0;   // the next chunk to stream (thread 0)
+    uint32_t i_buf = first % kMergeBufs;
+    auto issue_next = [&]() {
+        const uint32_t bar = b.merge_full((int)i_buf);
+        const float *src = reinterpret_cast<const float *>(ptx::ld_shared_u64(saddr + 8 * i_pi)) + i_rb * R * D;
+        ptx::mbar_arrive_expect_tx(bar, kMergeOBytes);
+        ptx::bulk_load(sbuf + i_buf * kMergeOBytes, src, kMergeOBytes, bar);
+        if (++i_pi == nparts) {
+            i_pi = 0;
+            ++i_rb;
+        }
+        i_buf = (i_buf + 1 == kMergeBufs) ? 0 : i_buf + 1;
+    };
+
+    // Weights, one row per thread (rows past N are computed and never used).
+    {
+        const size_t mrow = (size_t)w * kBM + t;
+        float2 ml[kMaxMergeParts];
+        int k = 0;
+        for (int cc = clo; cc <= chi && k < kMaxMergeParts; ++cc)
+            if (sched_part_slot(p.sch, pt, n, nw, cc, slot)) {
+#pragma unroll
+                for (int q = 0; q < kMaxMergeParts; ++q)
+                    if (q == k)
+                        ml[q] = ld_cg_f2(p.part_ml + (size_t)slot * kCtaRows + mrow);
+                ++k;
+            }
+        epilogue_sync();   // the part addresses are in shared memory
+        if (t == 0) {
+            ptx::fence_proxy_async_global();
+            for (int q = 0; q < kMergeBufs && q < nchunks; ++q)
+                issue_next();
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kMaxMergeParts; ++q)
+            if (q < nparts)
+                M = fmaxf(M, ml[q].x);
+        float L = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMaxMergeParts; ++q)
+            if (q < nparts) {
+                ml[q].y *= ptx::ex2(ml[q].x - M);
+                L += ml[q].y;
+            }
+        const float inv_L = 1.f / L;
+#pragma unroll
+        for (int q = 0; q < kMaxMergeParts; ++q)
+            if (q < nparts)
+                ptx::st_shared_f32(sweights + 4 * (q * kBM + t), ml[q].y * inv_L);
+        if (t < nrows)
+            p.LSE[(size_t)bh * p.N + r_base + t] = (M + log2f(L)) * kLn2;
+    }
+
+    // This thread's positions in a chunk: float4 t + 128 j, i.e. row
+    // t / kTpr + j * kRowStep, columns (t % kTpr) * 4 .. + 3.
+    const int row0 = t / kTpr, col = (t % kTpr) * 4;
+    uint64_t acc[kPos][2];
+    bool ok = true;
+    int k = 0, rb = 0, pi = 0;
+    uint32_t buf = first % kMergeBufs;
+#pragma unroll 1
+    for (; k < nchunks; ++k) {
+        // also the barrier after which every thread is done with chunk k - 1
+        // and the weights are all written
+        ok = epilogue_all(wait_bounded(b.merge_full((int)buf), ((first + k) / kMergeBufs) & 1u, c, kSiteMerge));
+        if (!ok)
+            break;
+        if (t == 0 && k >= 1 && k - 1 + kMergeBufs < nchunks)
+            issue_next();   // into the buffer chunk k - 1 has left
+        if (pi == 0) {
+#pragma unroll
+            for (int j = 0; j < kPos; ++j)
+                acc[j][0] = acc[j][1] = 0ull;
+        }
+        const uint32_t so = sbuf + buf * kMergeOBytes + (uint32_t)(row0 * D + col) * 4;
+        const uint32_t sw = sweights + 4 * (pi * kBM + rb * R + row0);
+#pragma unroll
+        for (int j = 0; j < kPos; ++j) {
+            const float wt = ptx::ld_shared_f32(sw + 4 * j * kRowStep);
+            const float4 o = ptx::ld_shared_v4f32(so + j * kRowStep * D * 4);
+            const uint64_t w2 = ptx::f2_pack(wt, wt);
+            acc[j][0] = ptx::f2_fma(ptx::f2_pack(o.x, o.y), w2, acc[j][0]);
+            acc[j][1] = ptx::f2_fma(ptx::f2_pack(o.z, o.w), w2, acc[j][1]);
+        }
+        if (pi == nparts - 1) {
+            const int r0 = rb * R + row0;
+            uint8_t *dst = reinterpret_cast<uint8_t *>(p.O) + (((size_t)bh * p.N + (size_t)(r_base + r0)) * D + col) * 2;
+#pragma unroll
+            for (int j = 0; j < kPos; ++j) {
+                if (r0 + j * kRowStep >= nrows)
+                    continue;
+                float x0, x1, x2, x3;
+                ptx::f2_unpack(acc[j][0], x0, x1);
+                ptx::f2_unpack(acc[j][1], x2, x3);
+                const uint32_t lo = BF16 ? ptx::pack_bf16x2(x0, x1) : ptx::pack_f16x2(x0, x1);
+                const uint32_t hi = BF16 ? ptx::pack_bf16x2(x2, x3) : ptx::pack_f16x2(x2, x3);
+                *reinterpret_cast<uint2 *>(dst + (size_t)j * kRowStep * D * 2) = make_uint2(lo, hi);
+            }
+        }
+        if (++pi == nparts) {
+            pi = 0;
+            ++rb;
+        }
+        buf = (buf + 1 == kMergeBufs) ? 0 : buf + 1;
+    }
+    // Chunks streamed: kMergeBufs in the prologue, then one per chunk after
+    // the first that was waited for successfully, so k - 1 + kMergeBufs when
+    // the wait for chunk k >= 1 failed (all nchunks on success).  Those from
+    // chunk k on may still be in flight and must land before the CTA exits.
+    const int cap = (k == 0) ? kMergeBufs : k - 1 + kMergeBufs;
+    const int streamed = (cap < nchunks) ? cap : nchunks;
+    if (!ok && t == 0)
+        for (int q = k; q < streamed; ++q)
+            wait_landed(b.merge_full((int)((first + q) % kMergeBufs)), ((first + q) / kMergeBufs) & 1u, c,
+                        kSiteMergeTail);
+    issued = first + (uint32_t)streamed;
+    epilogue_sync();   // every thread is done with the buffers and weights before they are reused
+    return ok;
+}
+
+// Per finished part: for each Q tile, read O_w out of TMEM, then release it
+// to the next part's first P.V.  A part that holds all of its Q tile's steps
+// writes O = acc / l in the input type and LSE = (m + log2 l) ln 2; a part of
+// a split tile writes its partial result to its workspace slot, and the part
+// that finishes last merges all of them -- after both Q tiles have been read
+// out, so that a merge never holds back the release of an accumulator.
 template <int D, bool BF16, bool CAUSAL>
-__device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, const float2 *handoff)
+__device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, const float2 *handoff,
+                              volatile int *flag, uint32_t sMerge)
 {
     using C = Cfg<D>;
     const int t = threadIdx.x % 128;              // row within a Q tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(t & ~31) << 16;
     uint32_t n_st[2] = {0u, 0u}, n_pv[2] = {0u, 0u};
+    uint32_t merged = 0;                          // merge chunks streamed by this CTA
 
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    PartIter parts;
+    parts.init(p.sch, blockIdx.x);
+    Part pt;
+    while (parts.next(p.sch, pt)) {
         int bh, ct;
-        decode_tile<CAUSAL>(tile, p, bh, ct);
-#pragma unroll
+        sched_decode(p.sch, pt.tile, bh, ct);
+        uint32_t published = 0;                   // bit w: Q tile w wrote a partial result
+#pragma unroll 1
         for (int w = 0; w < kQTiles; ++w) {
-            const int nw = kv_tiles<CAUSAL>(ct, w, p.N);
-            if (nw == 0)
+            const int nw = sched_kv_tiles(p.sch, ct, w);
+            const int np = part_steps(pt, nw);
+            if (np == 0)
                 continue;
-            if (!warp_wait(b.st_ready(w), n_st[w] & 1u, c, kSiteEpiStReady))
+            if (!epilogue_all(warp_wait(b.st_ready(w), n_st[w] & 1u, c, kSiteEpiStReady)))
                 return;
             ++n_st[w];
             const float2 st = handoff[w * kBM + t];
             ptx::mbar_arrive(b.st_free(w));
-            n_pv[w] += (uint32_t)nw;   // the last P.V of this tile is completion n_pv - 1 of o_done(w)
-            if (!warp_wait(b.o_done(w), (n_pv[w] - 1) & 1u, c, kSiteEpiODone))
+            n_pv[w] += (uint32_t)np;   // the last P.V of this part is completion n_pv - 1 of o_done(w)
+            if (!epilogue_all(warp_wait(b.o_done(w), (n_pv[w] - 1) & 1u, c, kSiteEpiODone)))
                 return;
             ptx::tc_fence_after_sync();
+            const bool whole = pt.kb == 0 && pt.ke >= nw;   // no other part holds steps of this Q tile
             const float inv_l = 1.f / st.y;
             const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
             const int row = ct * kCtaRows + w * kBM + t;
             const bool valid = row < p.N;
             uint8_t *orow =
                 reinterpret_cast<uint8_t *>(p.O) + ((size_t)bh * p.N + (size_t)(valid ? row : 0)) * D * 2;
+            float *prow = whole ? nullptr : p.part_o + ((size_t)pt.slot * kCtaRows + w * kBM + t) * D;
             const uint32_t tO = tmem + C::col_o(w) + lane_off;
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t o[32];
-                ptx::tmem_ld32(tO + q * 32, o);
+#pragma unroll 1
+            for (int q = 0; q < D / 16; ++q) {   // 16 columns at a time keeps this warpgroup's registers low
+                uint32_t o[16];
+                ptx::tmem_ld16(tO + q * 16, o);
                 ptx::tmem_wait_ld();
-                uint32_t pk[16];
+                float v[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float a, z;
-                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
-                                               il2),
-                                   a, z);
-                    pk[i] = BF16 ? ptx::pack_bf16x2(a, z) : ptx::pack_f16x2(a, z);
-                }
-                if (valid) {
+                for (int i = 0; i < 8; ++i)
+                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
+                                   v[2 * i], v[2 * i + 1]);
+                if (whole) {
+                    if (valid) {
+                        uint32_t pk[8];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        ptx::st_global_v4(orow + q * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
-                                          pk[4 * v + 3]);
+                        for (int i = 0; i < 8; ++i)
+                            pk[i] = BF16 ? ptx::pack_bf16x2(v[2 * i], v[2 * i + 1]) : ptx::pack_f16x2(v[2 * i], v[2 * i + 1]);
+                        ptx::st_global_v4(orow + q * 32, pk[0], pk[1], pk[2], pk[3]);
+                        ptx::st_global_v4(orow + q * 32 + 16, pk[4], pk[5], pk[6], pk[7]);
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        ptx::st_global_v4(prow + q * 16 + 4 * u, __float_as_uint(v[4 * u]), __float_as_uint(v[4 * u + 1]),
+                                          __float_as_uint(v[4 * u + 2]), __float_as_uint(v[4 * u + 3]));
                 }
             }
-            if (valid)
-                p.LSE[(size_t)bh * p.N + row] = (st.x + log2f(st.y)) * kLn2;
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(b.o_free(w));
+            if (whole) {
+                if (valid)
+                    p.LSE[(size_t)bh * p.N + row] = (st.x + log2f(st.y)) * kLn2;
+            } else {
+                p.part_ml[(size_t)pt.slot * kCtaRows + w * kBM + t] = st;
+                published |= 1u << w;
+            }
+        }
+        if (published == 0)
+            continue;
+        // Split tile: make this part's partials visible, count it in, and
+        // merge each Q tile for which it is the last part to finish.
+        __threadfence();
+        epilogue_sync();
+        if (t == 0) {
+            int last = 0;
+            for (int w = 0; w < kQTiles; ++w) {
+                if (!(published >> w & 1u))
+                    continue;
+                const int nw = sched_kv_tiles(p.sch, ct, w);
+                const int expected = sched_part_slots(p.sch, pt.tile, nw, nullptr, 0);
+                const int done = atomicAdd(&p.counters[2 * pt.tile + w], 1) + 1;
+                if (done == expected)
+                    last |= 1 << w;
+            }
+            *flag = last;
+        }
+        epilogue_sync();
+        const int last = *flag;
+        epilogue_sync();   // every thread has read the flag before it is reused
+        if (last == 0)
+            continue;
+        __threadfence();
+#pragma unroll 1
+        for (int w = 0; w < kQTiles; ++w) {
+            if (!(last >> w & 1))
+                continue;
+            if (!merge_parts<D, BF16>(p, pt.tile, sched_kv_tiles(p.sch, ct, w), w, bh, ct, sMerge,
+                                      sMerge + (C::kWeightOff - C::kMergeOff), sMerge + (C::kSlotOff - C::kMergeOff), b,
+                                      merged, c))
+                return;
+            if (t == 0)
+                p.counters[2 * pt.tile + w] = 0;   // ready for the next launch
         }
     }
 }
@@ -735,7 +1020,7 @@ __device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl 
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const __grid_constant__ CUtensorMap tmV, const FwdParams p)
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -772,6 +1057,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(b.o_free(w), kBM);
         }
         ptx::mbar_init(b.drain(), C::kMmaWarps);
+        for (int i = 0; i < kMergeBufs; ++i)
+            ptx::mbar_init(b.merge_full(i), 1);
         *c.abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -794,7 +1081,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         softmax_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff);
     } else if (wg == kEpilogueWarpgroup) {
         ptx::regs_decrease<kRegsEpilogue>();
-        epilogue_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff);
+        epilogue_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff, reinterpret_cast<volatile int *>(misc + 2),
+                                       base + C::kMergeOff);
     } else {
         ptx::regs_decrease<kRegsProducer>();
         if (warp == kLoadWarp)

@@ -14,7 +14,8 @@ from .build import LIB_PATH
 FA_BF16, FA_FP16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_MISALIGNED", 3: "FA_ERR_UNSUPPORTED_DEVICE",
           4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
-EXPORTS = ("fa_fwd", "fa_sync_status", "fa_status_string")
+EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_sync_status", "fa_status_string")
+SCHEDULES = {"auto": 0, "whole_tiles": 1, "balanced": 2}
 
 _lib = None
 
@@ -36,6 +37,8 @@ def load(path: str = LIB_PATH):
     vp, c_int = ctypes.c_void_p, ctypes.c_int
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, ctypes.c_float, c_int, vp]
     lib.fa_fwd.restype = c_int
+    lib.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, ctypes.c_float, c_int, c_int, vp]
+    lib.fa_fwd_ex.restype = c_int
     lib.fa_sync_status.argtypes = [vp]
     lib.fa_sync_status.restype = c_int
     lib.fa_status_string.argtypes = [c_int]
@@ -53,9 +56,12 @@ def status_string(status: int) -> str:
 
 
 def fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int, N: int, D: int,
-            causal: int, scale: float, dtype: int, stream: int = 0) -> int:
-    """Call fa_fwd with raw integer pointers; returns the status code unchanged."""
-    return load().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, D, causal, scale, dtype, stream)
+            causal: int, scale: float, dtype: int, stream: int = 0, schedule: int | None = None) -> int:
+    """Call fa_fwd (or fa_fwd_ex with a schedule code) with raw integer
+    pointers; returns the status code unchanged."""
+    if schedule is None:
+        return load().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, D, causal, scale, dtype, stream)
+    return load().fa_fwd_ex(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, D, causal, scale, dtype, schedule, stream)
 
 
 def sync_status(stream: int = 0) -> int:
@@ -71,12 +77,14 @@ def _dtype_code(t) -> int:
     raise TypeError(f"fa_fwd takes bfloat16 or float16 tensors, got {t.dtype}")
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
+            schedule: str = "auto"):
     """Attention forward on CUDA tensors [B, H, N, D]; returns (O, LSE).
 
-    ``out`` / ``lse`` may be given to write into existing buffers.  Raises
-    FAError on any non-OK status.  Asynchronous on ``stream`` (default: the
-    current torch stream).
+    ``out`` / ``lse`` may be given to write into existing buffers.
+    ``schedule`` is "auto", "whole_tiles" or "balanced" (fa_schedule).
+    Raises FAError on any non-OK status.  Asynchronous on ``stream``
+    (default: the current torch stream).
     """
     import torch
     if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
@@ -96,8 +104,10 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     st = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    if schedule not in SCHEDULES:
+        raise ValueError(f"schedule must be one of {sorted(SCHEDULES)}")
     rc = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D,
-                 int(bool(causal)), float(scale), code, st)
+                 int(bool(causal)), float(scale), code, st, SCHEDULES[schedule])
     if rc != 0:
         raise FAError(rc, "fa_fwd")
     return out, lse

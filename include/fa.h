@@ -23,8 +23,18 @@
  *    non-causal, head dimension 64 or 128.
  *
  * Every call is asynchronous on the caller's stream and stream-ordered like a
- * kernel launch.  The library allocates no device memory per call; nothing
- * in this header throws.
+ * kernel launch.  Nothing in this header throws.
+ *
+ * Device memory: calls that use the balanced schedule (below) need a
+ * workspace for partial results -- per CTA two slots of [256, D] fp32 plus
+ * (m, l) per row, and one int counter per (CTA tile, Q tile) -- about
+ * 2 x 152 x 256 x (D + 2) x 4 bytes plus 8 bytes per 256 query rows per head.
+ * It is allocated once per (device, stream) on the first such call, kept for
+ * the life of the process, and reallocated larger (after synchronising that
+ * stream) when a later call needs more; the counters are cleared with an
+ * asynchronous memset when the buffer is new.  Calls on one stream share its
+ * workspace in stream order; calls on different streams never share one.
+ * Calls with the whole-tile schedule allocate nothing.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -42,6 +52,29 @@ typedef enum {
     FA_BF16 = 0,   /* bfloat16 */
     FA_FP16 = 1    /* IEEE binary16 */
 } fa_dtype;
+
+/*
+ * Work decomposition over the persistent CTAs (one per SM).  A CTA tile is
+ * 256 query rows of one head; a step is one 128-key tile of K and V.
+ *  - FA_SCHEDULE_WHOLE_TILES: CTA c computes whole CTA tiles c, c + G, ...
+ *  - FA_SCHEDULE_BALANCED: every CTA gets an equal share of all (tile, step)
+ *    units; a tile cut by a share boundary is computed in parts whose partial
+ *    results (O normalised per part, row max and sum) are merged by the last
+ *    part to finish with the same rescaling rule the recurrence uses between
+ *    key tiles ("A09 - Advanced Triton & FlashAttention", 3. Deep Dive).  This
+ *    removes the idle SMs of a last partial wave of tiles.
+ *  - FA_SCHEDULE_AUTO: the balanced schedule where it is expected to pay
+ *    (non-causal calls whose shares span at least two tiles and whose last
+ *    wave would leave SMs idle), whole tiles otherwise.
+ * All three compute the same function; results agree to rounding.  The
+ * pages describe one CTA per (Q tile, head) on a grid; these schedules are
+ * this library's own.
+ */
+typedef enum {
+    FA_SCHEDULE_AUTO = 0,
+    FA_SCHEDULE_WHOLE_TILES = 1,
+    FA_SCHEDULE_BALANCED = 2
+} fa_schedule;
 
 typedef enum {
     FA_OK = 0,
@@ -75,13 +108,26 @@ typedef enum {
  * `stream` completes.  The device is the caller's current CUDA device.
  *
  * Returns FA_OK once the kernel is enqueued.  Argument errors are detected
- * before anything is enqueued and leave O and LSE untouched.  Errors raised
- * inside the kernel (a bounded wait that expired) are recorded in a
- * per-device status word and returned by fa_sync_status().
+ * before anything is enqueued and leave O and LSE untouched; FA_ERR_CUDA is
+ * returned if a needed workspace cannot be allocated.  Errors raised inside
+ * the kernel (a bounded wait that expired) are recorded in a per-device
+ * status word and returned by fa_sync_status().
+ *
+ * fa_fwd uses FA_SCHEDULE_AUTO.
  */
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
                  int B, int H, int N, int D, int causal, float scale,
                  fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * fa_fwd_ex -- fa_fwd with an explicit work decomposition `schedule` (see
+ * fa_schedule); any other value returns FA_ERR_INVALID_VALUE.  A balanced
+ * request the shape cannot take (more than 2^30 units of work) runs whole
+ * tiles.
+ */
+fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                    int B, int H, int N, int D, int causal, float scale,
+                    fa_dtype dtype, fa_schedule schedule, fa_stream_t stream);
 
 /*
  * fa_sync_status -- synchronise `stream`, then return and clear the device
