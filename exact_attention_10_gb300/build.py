@@ -1,7 +1,9 @@
 """Build the CUDA library (libfa_gb300.so) in-tree with nvcc for sm_103a.
 
-One translation unit (csrc/fa_api.cu, which includes the kernel header) so the
-build stays quick on both the x86_64 build machine and the aarch64 GPU host.
+Two translation units, compiled in parallel and linked into one shared
+library: csrc/fa_api.cu (the C ABI and the whole-tile kernel variants) and
+csrc/fa_split.cu (the balanced-schedule variants), so the build stays quick on
+both the x86_64 build machine and the aarch64 GPU host.
 The runtime is linked statically and the driver's tensor-map encoder is
 resolved at run time, so the library loads on a machine without a GPU driver
 (its compute calls then return FA_ERR_UNSUPPORTED_DEVICE).
@@ -14,7 +16,7 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "fa_api.cu")
+SRCS = [os.path.join(PKG, "csrc", "fa_api.cu"), os.path.join(PKG, "csrc", "fa_split.cu")]
 LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -25,14 +27,31 @@ def nvcc() -> str:
 
 
 def build(out: str = LIB_PATH, verbose: bool = False, extra=None) -> str:
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I", os.path.join(ROOT, "include"), "-I", os.path.join(PKG, "csrc"),
-           *(["-Xptxas", "-v"] if verbose else []), *(extra or []), SRC, "-o", out]
+    common = [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+              "-I", os.path.join(ROOT, "include"), "-I", os.path.join(PKG, "csrc"),
+              *(["-Xptxas", "-v"] if verbose else []), *(extra or [])]
+    objs = [out + "." + os.path.splitext(os.path.basename(src))[0] + ".o" for src in SRCS]
+    procs = [(src, subprocess.Popen([nvcc(), *common, "-c", src, "-o", obj], stdout=subprocess.PIPE,
+                                    stderr=subprocess.PIPE, text=True))
+             for src, obj in zip(SRCS, objs)]
+    errors = []
+    for src, proc in procs:
+        _, err = proc.communicate()
+        if proc.returncode != 0:
+            errors.append(f"{src}:\n{err}")
+        elif verbose:
+            sys.stderr.write(err)
+    if errors:
+        raise RuntimeError("CUDA library build failed:\n" + "\n".join(errors))
+    cmd = [nvcc(), *ARCH, "-shared", *objs, "-o", out]
     res = subprocess.run(cmd, capture_output=True, text=True)
+    for obj in objs:
+        try:
+            os.remove(obj)
+        except OSError:
+            pass
     if res.returncode != 0:
-        raise RuntimeError(f"CUDA library build failed:\n{' '.join(cmd)}\n{res.stderr}")
-    if verbose:
-        sys.stderr.write(res.stderr)
+        raise RuntimeError(f"CUDA library link failed:\n{' '.join(cmd)}\n{res.stderr}")
     return out
 
 

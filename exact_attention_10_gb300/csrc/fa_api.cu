@@ -15,7 +15,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "fa_fwd_kernel.cuh"
+#include "fa_launch.cuh"
 
 namespace {
 
@@ -41,14 +41,12 @@ EncodeTiledFn encode_tiled()
     return fn;
 }
 
-constexpr int kMaxDevices = 64;
-constexpr int kVariants = 8;   // D x dtype x causal
+constexpr int kMaxDevices = fa_launch::kMaxDevices;
 
 struct DeviceInfo {
     bool probed = false;
     bool supported = false;
     int sms = 0;
-    bool smem_attr_set[kVariants] = {};
 };
 
 std::mutex g_mu;
@@ -113,41 +111,6 @@ bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D, bool bf16
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
-}
-
-template <int D, bool BF16, bool CAUSAL>
-fa_status launch_variant(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const fa::FwdParams &p,
-                         int grid, cudaStream_t stream, int dev)
-{
-    auto kern = fa::fa_fwd_sm103<D, BF16, CAUSAL>;
-    const int variant = (D == 128 ? 4 : 0) + (BF16 ? 0 : 2) + (CAUSAL ? 1 : 0);
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        bool &set = g_devices[dev].smem_attr_set[variant];
-        if (!set) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fa::Cfg<D>::kSmemBytes) !=
-                cudaSuccess) {
-                cudaGetLastError();
-                return FA_ERR_CUDA;
-            }
-            set = true;
-        }
-    }
-    kern<<<grid, fa::kThreads, fa::Cfg<D>::kSmemBytes, stream>>>(q, k, v, p);
-    if (cudaGetLastError() != cudaSuccess)
-        return FA_ERR_CUDA;
-    return FA_OK;
-}
-
-template <int D>
-fa_status dispatch_dtype(bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                         const fa::FwdParams &p, int grid, cudaStream_t s, int dev)
-{
-    if (bf16)
-        return causal ? launch_variant<D, true, true>(q, k, v, p, grid, s, dev)
-                      : launch_variant<D, true, false>(q, k, v, p, grid, s, dev);
-    return causal ? launch_variant<D, false, true>(q, k, v, p, grid, s, dev)
-                  : launch_variant<D, false, false>(q, k, v, p, grid, s, dev);
 }
 
 // Per-(device, stream) workspace for split tiles: partial O and (m, l) for
@@ -221,6 +184,21 @@ fa_status workspace_for(int dev, cudaStream_t stream, const fa::Schedule &sc, in
 
 }  // namespace
 
+namespace fa_launch {
+
+fa_status launch_whole(int D, bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k,
+                       const CUtensorMap &v, const fa::FwdParams &p, int grid, cudaStream_t s, int dev)
+{
+    return launch_any<false>(D, bf16, causal, q, k, v, p, grid, s, dev);
+}
+
+bool take_status_word_whole(unsigned int *word)
+{
+    return take_status_word_here(word);
+}
+
+}  // namespace fa_launch
+
 extern "C" fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                                int N, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
                                fa_stream_t stream)
@@ -283,9 +261,9 @@ extern "C" fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void
         if (ws != FA_OK)
             return ws;
     }
-    if (D == 64)
-        return dispatch_dtype<64>(bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
-    return dispatch_dtype<128>(bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
+    if (p.sch.split)
+        return fa_launch::launch_split(D, bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
+    return fa_launch::launch_whole(D, bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
 }
 
 extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
@@ -300,12 +278,10 @@ extern "C" fa_status fa_sync_status(fa_stream_t stream)
         cudaGetLastError();
         return FA_ERR_CUDA;
     }
-    unsigned int word = 0;
-    if (cudaMemcpyFromSymbol(&word, fa::g_status_word, sizeof word) != cudaSuccess) {
-        cudaGetLastError();
+    unsigned int w_whole = 0, w_split = 0;
+    if (!fa_launch::take_status_word_whole(&w_whole) || !fa_launch::take_status_word_split(&w_split))
         return FA_ERR_CUDA;
-    }
-    if (word != 0) {
+    if ((w_whole | w_split) != 0) {
         // an aborted launch may have left split-tile counters non-zero
         int dev = -1;
         cudaGetDevice(&dev);
@@ -314,11 +290,6 @@ extern "C" fa_status fa_sync_status(fa_stream_t stream)
             for (int i = 0; i < g_ws_count; ++i)
                 if (g_ws[i].dev == dev && g_ws[i].ptr)
                     g_ws[i].counter_bytes = 0;   // cleared again by the next call that uses it
-        }
-        const unsigned int zero = 0;
-        if (cudaMemcpyToSymbol(fa::g_status_word, &zero, sizeof zero) != cudaSuccess) {
-            cudaGetLastError();
-            return FA_ERR_CUDA;
         }
         return FA_ERR_DEVICE_TIMEOUT;
     }

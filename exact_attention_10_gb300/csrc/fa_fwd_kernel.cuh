@@ -67,6 +67,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cstddef>
 #include <cstdint>
 
 #include "fa_schedule.h"
@@ -75,8 +76,10 @@
 namespace fa {
 
 // Device status word: 0 = fine; otherwise 1 | (site << 8) of the first wait
-// that expired.  Read and cleared by fa_sync_status().
-__device__ unsigned int g_status_word;
+// that expired.  Each translation unit that includes this header has its own
+// (device code is not linked across units); fa_sync_status() reads and clears
+// every unit's word (take_status_word).
+static __device__ unsigned int g_status_word;
 
 constexpr int kBM = 128;        // query rows per Q tile (one TMEM lane each)
 constexpr int kBN = 128;        // keys per K/V tile
@@ -86,13 +89,29 @@ constexpr int kThreads = 512;
 constexpr int kEpilogueWarpgroup = 2;
 constexpr int kLoadWarp = 12;
 constexpr int kMmaWarp = 13;          // MMA issuer(s): warp 13 (and 14 at D = 64)
+constexpr int kMergeWarp = 15;        // merges split tiles (balanced schedule)
 constexpr uint32_t kRegsSoftmax = 184;   // 2 x 128 x 184 + 128 x 64 + 128 x 80 = 65536 (launch: 512 x 128)
 constexpr uint32_t kRegsEpilogue = 64;
 constexpr uint32_t kRegsProducer = 80;
 constexpr int kPerTileBars = 7;
-constexpr int kMergeBufs = 3;            // merge staging buffers in flight
-constexpr int kMergeOBytes = 8192;       // partial O bytes per staging buffer
+constexpr int kMergeBufs = 4;            // merge staging buffers in flight
+constexpr int kMergeOBytes = 4096;       // partial O bytes per staging buffer
 constexpr int kMaxMergeParts = kSchedMaxParts;   // parts of one split tile, at most (the planner keeps to it)
+constexpr int kJobSlots = 2;             // merge jobs queued from the epilogue to the merge warp
+
+// A merge job, posted by the epilogue in shared memory: the Q tile's rows
+// [orow0, orow0 + nrows) of the [B*H*N] output rows, the workspace counter to
+// reset, and each part's partial O and (m, l) (row 0 of the Q tile in its
+// slot).  nparts = 0 tells the merge warp to stop.
+struct MergeJob {
+    long long orow0;
+    int nrows;
+    int nparts;
+    int counter;
+    int pad;
+    unsigned long long o_addr[kMaxMergeParts];
+    unsigned long long ml_addr[kMaxMergeParts];
+};
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -100,7 +119,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 enum : uint32_t {
     kSiteLoadQEmpty = 1, kSiteLoadSlotEmpty, kSiteMmaQFull, kSiteMmaSlotFull, kSiteMmaPFull, kSiteMmaOFree,
     kSiteMmaSFree, kSiteSoftSFull, kSiteSoftODone, kSiteSoftStFree, kSiteEpiStReady, kSiteEpiODone, kSiteDrain,
-    kSiteTail, kSiteMerge, kSiteMergeTail
+    kSiteTail, kSiteMerge, kSiteMergeTail, kSiteMergeJob, kSiteEpiJobFree
 };
 
 template <int D>
@@ -123,18 +142,22 @@ struct Cfg {
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
     // full[kStages], empty[kStages], q_full[kQBufs], q_empty[kQBufs], then per
     // Q tile: s_full, s_free, p_full, o_done, st_ready, st_free, o_free; then drain
-    static constexpr int kNumBars = 2 * kStages + 2 * kQBufs + kPerTileBars * kQTiles + 1 + kMergeBufs;
+    static constexpr int kNumBars = 2 * kStages + 2 * kQBufs + kPerTileBars * kQTiles + 1 + kMergeBufs + 1 + 2 * kJobSlots;
     static constexpr int kHandOff = kBarOff + kNumBars * 8;            // float2 [2 tiles][128]
     static constexpr int kMiscOff = kHandOff + kQTiles * kBM * 8;
     // Merge staging: kMergeBufs buffers, each the partial O of kMergeRows rows
-    // of one part; the merge weights, fp32 [kMaxMergeParts][128 rows]; the
-    // global address of each part's partial O for the Q tile, u64 [kMaxMergeParts].
+    // of one part; the parts' (m, l) of the Q tile, float2 [kMaxMergeParts][128]
+    // (turned into merge weights in place); the job queue, kJobSlots MergeJobs.
     static constexpr int kMergeRows = kMergeOBytes / (D * 4);
     static constexpr int kMergeOff = (kMiscOff + 16 + 127) & ~127;
-    static constexpr int kWeightOff = kMergeOff + kMergeBufs * kMergeOBytes;
-    static constexpr int kSlotOff = kWeightOff + kMaxMergeParts * kBM * 4;   // u64: each part's partial O of the Q tile
-    static constexpr int kSmemBytes = kSlotOff + kMaxMergeParts * 8 + 1024;   // + slack to align the base to 1024
-    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static constexpr int kMlOff = kMergeOff + kMergeBufs * kMergeOBytes;
+    static constexpr int kJobOff = kMlOff + kMaxMergeParts * kBM * 8;
+    // Shared memory of a launch (+ slack to align the base to 1024): the
+    // whole-tile variant has no merge area.
+    static constexpr int kSmemSplit = kJobOff + kJobSlots * (int)sizeof(MergeJob) + 1024;
+    static constexpr int kSmemWhole = kMiscOff + 16 + 1024;
+    __host__ __device__ static constexpr int smem_bytes(bool split) { return split ? kSmemSplit : kSmemWhole; }
+    static_assert(kSmemSplit <= 232448 && kSmemWhole <= kSmemSplit, "shared memory per CTA");
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t col_s(int w) { return w ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t col_o(int w) { return w ? 256u + D : 256u; }
@@ -179,7 +202,7 @@ struct Ctl {
     volatile int *abort_flag;
 };
 
-__device__ __noinline__ void record_timeout(Ctl c, uint32_t site)
+static __device__ __noinline__ void record_timeout(Ctl c, uint32_t site)
 {
     *c.abort_flag = 1;
     atomicCAS(&g_status_word, 0u, 1u | (site << 8));
@@ -235,7 +258,10 @@ struct Bars {
     __device__ uint32_t st_free(int w) const { return per_tile(w, 5); }    // epilogue -> softmax: (m, l) read
     __device__ uint32_t o_free(int w) const { return per_tile(w, 6); }     // epilogue -> MMA: O_w read out
     __device__ uint32_t drain() const { return per_tile(kQTiles, 0); }
-    __device__ uint32_t merge_full(int i) const { return per_tile(kQTiles, 1 + i); }   // bulk copy -> merge: buffer i landed
+    __device__ uint32_t merge_full(int i) const { return per_tile(kQTiles, 1 + i); }   // bulk copy -> merge warp: buffer i landed
+    __device__ uint32_t ml_full() const { return per_tile(kQTiles, 1 + kMergeBufs); }    // bulk copy -> merge warp: (m, l) landed
+    __device__ uint32_t job_full(int j) const { return per_tile(kQTiles, 2 + kMergeBufs + j); }               // epilogue -> merge warp
+    __device__ uint32_t job_empty(int j) const { return per_tile(kQTiles, 2 + kMergeBufs + kJobSlots + j); }  // merge warp -> epilogue
 };
 
 // ------------------------------------------------------------------ producer
@@ -243,7 +269,7 @@ struct Bars {
 // TMA producer, run by a whole warp; one elected lane issues the copies.
 // Per CTA tile: both Q tiles into the Q buffer, then for each step j the
 // pair K_j, V_j into the next stage of the ring.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
                           const FwdParams &p, uint32_t sQ, uint32_t sStage, Bars<D> b, Ctl c)
 {
@@ -252,11 +278,11 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
     int it = 0;     // parts started by this CTA (one Q load each)
     bool ok = true;
     PartIter parts;
-    parts.init(p.sch, blockIdx.x);
+    parts.init_t<SPLIT>(p.sch, blockIdx.x);
     Part pt;
-    while (ok && parts.next(p.sch, pt)) {
+    while (ok && parts.next_t<SPLIT>(p.sch, pt)) {
         int bh, ct;
-        sched_decode(p.sch, pt.tile, bh, ct);
+        sched_decode_t<SPLIT>(p.sch, pt.tile, bh, ct);
         const int qb = it % C::kQBufs;
         const uint32_t quse = (uint32_t)(it / C::kQBufs);
         if (!warp_wait(b.q_empty(qb), (quse & 1u) ^ 1u, c, kSiteLoadQEmpty)) { ok = false; break; }
@@ -480,7 +506,7 @@ __device__ bool tile_interleaved(MmaIssuer<D, BF16> &m0, MmaIssuer<D, BF16> &m1,
     return true;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage, uint32_t tmem, Bars<D> b, Ctl c)
 {
     using C = Cfg<D>;
@@ -500,11 +526,11 @@ __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage
     MmaIssuer<D, BF16> m1 = make(1);                // tile 1 when one warp serves both
     int step = 0, it = 0;
     PartIter parts;
-    parts.init(p.sch, blockIdx.x);
+    parts.init_t<SPLIT>(p.sch, blockIdx.x);
     Part pt;
-    while (parts.next(p.sch, pt)) {
+    while (parts.next_t<SPLIT>(p.sch, pt)) {
         int bh, ct;
-        sched_decode(p.sch, pt.tile, bh, ct);
+        sched_decode_t<SPLIT>(p.sch, pt.tile, bh, ct);
         const int n0 = part_steps(pt, sched_kv_tiles(p.sch, ct, 0)), n1 = part_steps(pt, sched_kv_tiles(p.sch, ct, 1));
         const int n = pt.ke - pt.kb;
         const int qb = it % C::kQBufs;
@@ -531,7 +557,7 @@ __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage
 
 // ------------------------------------------------------------------ softmax
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, float2 *handoff)
 {
     using C = Cfg<D>;
@@ -545,11 +571,11 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
     uint32_t s_phase = 0, o_phase = 0, n_st = 0;
 
     PartIter parts;
-    parts.init(p.sch, blockIdx.x);
+    parts.init_t<SPLIT>(p.sch, blockIdx.x);
     Part pt;
-    while (parts.next(p.sch, pt)) {
+    while (parts.next_t<SPLIT>(p.sch, pt)) {
         int bh, ct;
-        sched_decode(p.sch, pt.tile, bh, ct);
+        sched_decode_t<SPLIT>(p.sch, pt.tile, bh, ct);
         const int nw = sched_kv_tiles(p.sch, ct, w);    // steps of this Q tile in the whole tile
         const int np = part_steps(pt, nw);              // ... of which this part holds steps kb .. kb + np - 1
         if (np == 0)
@@ -736,250 +762,285 @@ __device__ __forceinline__ float2 ld_cg_f2(const float2 *p)
 // tile sees at least one key in each of the tile's steps (the diagonal step
 // starts at the Q tile's first row), so each part's m_k is finite.
 //
-// The epilogue warps share their schedulers with the busy softmax warps, so
-// the merge keeps its instruction count low: first each thread takes one row,
-// computes the weights l_k 2^(m_k - M) / L of all parts into shared memory and
-// writes LSE; then the partial O streams through kMergeBufs shared-memory
-// buffers by bulk copies (a chunk: kMergeRows rows of one part, in the order
-// row block, part), each thread adding weight x O for 4 columns of 4 rows of
-// a chunk.  `issued` counts the chunks this CTA has streamed (buffer g %
-// kMergeBufs, phase g / kMergeBufs of chunk g).  False if a wait gave up; the
-// copies in flight have landed by then.
+// One warp does all merges, off the path of the warps that read accumulators
+// out of TMEM: it takes jobs from the epilogue's queue, brings each part's
+// (m, l) into shared memory with one bulk copy, turns them into the weights
+// l_k 2^(m_k - M) / L in place (a lane per row) and writes LSE, then streams
+// the partial O through kMergeBufs buffers (a chunk: kMergeRows rows of one
+// part, in the order row block, part), each lane adding weight x O for 4
+// columns of 8 rows of a chunk, and writes O.  Every wait is bounded; on a
+// failed wait the copies in flight are let land and the warp stops.
 template <int D, bool BF16>
-__device__ __noinline__ bool merge_parts(const FwdParams &p, int tile, int nw, int w, int bh, int ct, uint32_t sbuf,
-                                         uint32_t sweights, uint32_t saddr, Bars<D> b, uint32_t &issued, Ctl c)
+__device__ void merge_role(const FwdParams &p, uint32_t sbuf, uint32_t sml, const MergeJob *jobs, Bars<D> b, Ctl c)
 {
     using C = Cfg<D>;
-    constexpr int R = C::kMergeRows;              // 32 or 16 rows per chunk
-    constexpr int kTpr = D / 4;                   // threads per row of a chunk
-    constexpr int kPos = R * kTpr / kBM;          // positions (4 columns of a row) per thread: 4
-    constexpr int kRowStep = kBM / kTpr;          // rows between a thread's positions: 8 or 4
-    const int t = threadIdx.x % kBM;
-    int pt, n, clo, chi, slot;
-    sched_tile_ctas(p.sch, tile, pt, n, clo, chi);
-    int nparts = 0;
-    for (int cc = clo; cc <= chi; ++cc)
-        if (sched_part_slot(p.sch, pt, n, nw, cc, slot)) {
-            if (t == nparts && nparts < kMaxMergeParts)   // thread k notes part k's partial O
-                ptx::st_shared_u64(saddr + 8 * t,
-                                   reinterpret_cast<uint64_t>(p.part_o + ((size_t)slot * kCtaRows + w * kBM) * D));
-            ++nparts;
-        }
-    nparts = (nparts < kMaxMergeParts) ? nparts : kMaxMergeParts;
-    const int r_base = ct * kCtaRows + w * kBM;   // first row of the Q tile in the head
-    const int nrows = (p.N - r_base < kBM) ? p.N - r_base : kBM;
-    const int nchunks = ((nrows + R - 1) / R) * nparts;
-    const uint32_t first = issued;
+    constexpr int R = C::kMergeRows;              // 16 or 8 rows per chunk
+    constexpr int kTpr = D / 4;                   // lanes per row of a chunk
+    constexpr int kPos = R * kTpr / 32;           // positions (4 columns of a row) per lane: 8
+    constexpr int kRowStep = 32 / kTpr;           // rows between a lane's positions: 2 or 1
+    const int lane = threadIdx.x % 32;
+    const int row0 = lane / kTpr, col = (lane % kTpr) * 4;
+    uint32_t n_jobs = 0, streamed = 0, ml_uses = 0;   // jobs taken; O chunks and (m, l) copies so far
 
-    // Chunk k = (row block rb, part pi) goes to buffer (first + k) % kMergeBufs.
-    int i_rb = 0, i_pi = 0;   // the next chunk to stream (thread 0)
-    uint32_t i_buf = first % kMergeBufs;
-    auto issue_next = [&]() {
-        const uint32_t bar = b.merge_full((int)i_buf);
-        const float *src = reinterpret_cast<const float *>(ptx::ld_shared_u64(saddr + 8 * i_pi)) + i_rb * R * D;
-        ptx::mbar_arrive_expect_tx(bar, kMergeOBytes);
-        ptx::bulk_load(sbuf + i_buf * kMergeOBytes, src, kMergeOBytes, bar);
-        if (++i_pi == nparts) {
-            i_pi = 0;
-            ++i_rb;
-        }
-        i_buf = (i_buf + 1 == kMergeBufs) ? 0 : i_buf + 1;
-    };
-
-    // Weights, one row per thread (rows past N are computed and never used).
-    {
-        const size_t mrow = (size_t)w * kBM + t;
-        float2 ml[kMaxMergeParts];
-        int k = 0;
-        for (int cc = clo; cc <= chi && k < kMaxMergeParts; ++cc)
-            if (sched_part_slot(p.sch, pt, n, nw, cc, slot)) {
-#pragma unroll
-                for (int q = 0; q < kMaxMergeParts; ++q)
-                    if (q == k)
-                        ml[q] = ld_cg_f2(p.part_ml + (size_t)slot * kCtaRows + mrow);
-                ++k;
+    for (;;) {
+        const int j = (int)(n_jobs % kJobSlots);
+        if (!warp_wait(b.job_full(j), (n_jobs / kJobSlots) & 1u, c, kSiteMergeJob))
+            return;
+        const MergeJob &job = jobs[j];
+        const int nparts = job.nparts, nrows = job.nrows;
+        if (nparts == 0)
+            return;   // stop
+        const int nchunks = ((nrows + R - 1) / R) * nparts;
+        const uint32_t first = streamed;
+        int i_rb = 0, i_pi = 0, issued = 0;   // next chunk to stream (lane 0)
+        auto issue_next = [&]() {
+            const uint32_t g = first + (uint32_t)issued, buf = g % kMergeBufs;
+            const float *src = reinterpret_cast<const float *>(job.o_addr[i_pi]) + i_rb * R * D;
+            ptx::mbar_arrive_expect_tx(b.merge_full((int)buf), kMergeOBytes);
+            ptx::bulk_load(sbuf + buf * kMergeOBytes, src, kMergeOBytes, b.merge_full((int)buf));
+            if (++i_pi == nparts) {
+                i_pi = 0;
+                ++i_rb;
             }
-        epilogue_sync();   // the part addresses are in shared memory
-        if (t == 0) {
-            ptx::fence_proxy_async_global();
-            for (int q = 0; q < kMergeBufs && q < nchunks; ++q)
+            ++issued;
+        };
+        if (lane == 0) {
+            ptx::fence_proxy_async_global();   // the parts' partials, made visible by the counter's acquire
+            ptx::mbar_arrive_expect_tx(b.ml_full(), (uint32_t)nparts * kBM * 8);
+            for (int k = 0; k < nparts; ++k)
+                ptx::bulk_load(sml + k * kBM * 8, reinterpret_cast<const void *>(job.ml_addr[k]), kBM * 8, b.ml_full());
+            while (issued < kMergeBufs && issued < nchunks)
                 issue_next();
         }
-        float M = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kMaxMergeParts; ++q)
-            if (q < nparts)
-                M = fmaxf(M, ml[q].x);
-        float L = 0.f;
-#pragma unroll
-        for (int q = 0; q < kMaxMergeParts; ++q)
-            if (q < nparts) {
-                ml[q].y *= ptx::ex2(ml[q].x - M);
-                L += ml[q].y;
+        issued = __shfl_sync(0xffffffffu, issued, 0);
+        bool ok = warp_wait(b.ml_full(), ml_uses & 1u, c, kSiteMerge);
+        const bool ml_landed = ok;
+        ++ml_uses;
+        if (ok) {
+            // weights in place of m; a lane per row
+            for (int r = lane; r < kBM; r += 32) {
+                float M = -INFINITY;
+                for (int k = 0; k < nparts; ++k)
+                    M = fmaxf(M, ptx::ld_shared_f32(sml + (k * kBM + r) * 8));
+                float L = 0.f;
+                for (int k = 0; k < nparts; ++k) {
+                    const uint32_t a = sml + (k * kBM + r) * 8;
+                    const float e = ptx::ld_shared_f32(a + 4) * ptx::ex2(ptx::ld_shared_f32(a) - M);
+                    ptx::st_shared_f32(a, e);
+                    L += e;
+                }
+                const float inv_L = 1.f / L;
+                for (int k = 0; k < nparts; ++k) {
+                    const uint32_t a = sml + (k * kBM + r) * 8;
+                    ptx::st_shared_f32(a, ptx::ld_shared_f32(a) * inv_L);
+                }
+                if (r < nrows)
+                    p.LSE[job.orow0 + r] = (M + log2f(L)) * kLn2;
             }
-        const float inv_L = 1.f / L;
-#pragma unroll
-        for (int q = 0; q < kMaxMergeParts; ++q)
-            if (q < nparts)
-                ptx::st_shared_f32(sweights + 4 * (q * kBM + t), ml[q].y * inv_L);
-        if (t < nrows)
-            p.LSE[(size_t)bh * p.N + r_base + t] = (M + log2f(L)) * kLn2;
-    }
-
-    // This thread's positions in a chunk: float4 t + 128 j, i.e. row
-    // t / kTpr + j * kRowStep, columns (t % kTpr) * 4 .. + 3.
-    const int row0 = t / kTpr, col = (t % kTpr) * 4;
-    uint64_t acc[kPos][2];
-    bool ok = true;
-    int k = 0, rb = 0, pi = 0;
-    uint32_t buf = first % kMergeBufs;
-#pragma unroll 1
-    for (; k < nchunks; ++k) {
-        // also the barrier after which every thread is done with chunk k - 1
-        // and the weights are all written
-        ok = epilogue_all(wait_bounded(b.merge_full((int)buf), ((first + k) / kMergeBufs) & 1u, c, kSiteMerge));
-        if (!ok)
-            break;
-        if (t == 0 && k >= 1 && k - 1 + kMergeBufs < nchunks)
-            issue_next();   // into the buffer chunk k - 1 has left
-        if (pi == 0) {
-#pragma unroll
-            for (int j = 0; j < kPos; ++j)
-                acc[j][0] = acc[j][1] = 0ull;
+            __syncwarp();
         }
-        const uint32_t so = sbuf + buf * kMergeOBytes + (uint32_t)(row0 * D + col) * 4;
-        const uint32_t sw = sweights + 4 * (pi * kBM + rb * R + row0);
+        uint64_t acc[kPos][2];
+        int k = 0, rb = 0, pi = 0;
+        for (; ok && k < nchunks; ++k) {
+            const uint32_t g = first + (uint32_t)k, buf = g % kMergeBufs;
+            ok = warp_wait(b.merge_full((int)buf), (g / kMergeBufs) & 1u, c, kSiteMerge);
+            if (!ok)
+                break;
+            if (pi == 0) {
 #pragma unroll
-        for (int j = 0; j < kPos; ++j) {
-            const float wt = ptx::ld_shared_f32(sw + 4 * j * kRowStep);
-            const float4 o = ptx::ld_shared_v4f32(so + j * kRowStep * D * 4);
-            const uint64_t w2 = ptx::f2_pack(wt, wt);
-            acc[j][0] = ptx::f2_fma(ptx::f2_pack(o.x, o.y), w2, acc[j][0]);
-            acc[j][1] = ptx::f2_fma(ptx::f2_pack(o.z, o.w), w2, acc[j][1]);
-        }
-        if (pi == nparts - 1) {
-            const int r0 = rb * R + row0;
-            uint8_t *dst = reinterpret_cast<uint8_t *>(p.O) + (((size_t)bh * p.N + (size_t)(r_base + r0)) * D + col) * 2;
+                for (int q = 0; q < kPos; ++q)
+                    acc[q][0] = acc[q][1] = 0ull;
+            }
+            const uint32_t so = sbuf + buf * kMergeOBytes + (uint32_t)(row0 * D + col) * 4;
+            const uint32_t sw = sml + (uint32_t)(pi * kBM + rb * R + row0) * 8;
 #pragma unroll
-            for (int j = 0; j < kPos; ++j) {
-                if (r0 + j * kRowStep >= nrows)
-                    continue;
-                float x0, x1, x2, x3;
-                ptx::f2_unpack(acc[j][0], x0, x1);
-                ptx::f2_unpack(acc[j][1], x2, x3);
-                const uint32_t lo = BF16 ? ptx::pack_bf16x2(x0, x1) : ptx::pack_f16x2(x0, x1);
-                const uint32_t hi = BF16 ? ptx::pack_bf16x2(x2, x3) : ptx::pack_f16x2(x2, x3);
-                *reinterpret_cast<uint2 *>(dst + (size_t)j * kRowStep * D * 2) = make_uint2(lo, hi);
+            for (int q = 0; q < kPos; ++q) {
+                const float wt = ptx::ld_shared_f32(sw + q * kRowStep * 8);
+                const float4 o = ptx::ld_shared_v4f32(so + q * kRowStep * D * 4);
+                const uint64_t w2 = ptx::f2_pack(wt, wt);
+                acc[q][0] = ptx::f2_fma(ptx::f2_pack(o.x, o.y), w2, acc[q][0]);
+                acc[q][1] = ptx::f2_fma(ptx::f2_pack(o.z, o.w), w2, acc[q][1]);
+            }
+            __syncwarp();   // every lane is done with this buffer
+            if (lane == 0 && issued < nchunks)
+                issue_next();   // into the buffer just read
+            issued = __shfl_sync(0xffffffffu, issued, 0);
+            if (pi == nparts - 1) {
+                const int r0 = rb * R + row0;
+                uint8_t *dst = reinterpret_cast<uint8_t *>(p.O) + ((size_t)(job.orow0 + r0) * D + col) * 2;
+#pragma unroll
+                for (int q = 0; q < kPos; ++q) {
+                    if (r0 + q * kRowStep >= nrows)
+                        continue;
+                    float x0, x1, x2, x3;
+                    ptx::f2_unpack(acc[q][0], x0, x1);
+                    ptx::f2_unpack(acc[q][1], x2, x3);
+                    const uint32_t lo = BF16 ? ptx::pack_bf16x2(x0, x1) : ptx::pack_f16x2(x0, x1);
+                    const uint32_t hi = BF16 ? ptx::pack_bf16x2(x2, x3) : ptx::pack_f16x2(x2, x3);
+                    *reinterpret_cast<uint2 *>(dst + (size_t)q * kRowStep * D * 2) = make_uint2(lo, hi);
+                }
+            }
+            if (++pi == nparts) {
+                pi = 0;
+                ++rb;
             }
         }
-        if (++pi == nparts) {
-            pi = 0;
-            ++rb;
+        streamed = first + (uint32_t)issued;
+        if (!ok) {   // let every copy in flight land before the CTA may exit
+            if (lane == 0) {
+                if (!ml_landed)
+                    wait_landed(b.ml_full(), (ml_uses - 1) & 1u, c, kSiteMergeTail);
+                for (int q = k; q < issued; ++q)
+                    wait_landed(b.merge_full((int)((first + q) % kMergeBufs)), ((first + q) / kMergeBufs) & 1u, c,
+                                kSiteMergeTail);
+            }
+            __syncwarp();
+            return;
         }
-        buf = (buf + 1 == kMergeBufs) ? 0 : buf + 1;
+        if (lane == 0) {
+            p.counters[job.counter] = 0;   // ready for the next launch
+            ptx::mbar_arrive(b.job_empty(j));
+        }
+        __syncwarp();
+        ++n_jobs;
     }
-    // Chunks streamed: kMergeBufs in the prologue, then one per chunk after
-    // the first that was waited for successfully, so k - 1 + kMergeBufs when
-    // the wait for chunk k >= 1 failed (all nchunks on success).  Those from
-    // chunk k on may still be in flight and must land before the CTA exits.
-    const int cap = (k == 0) ? kMergeBufs : k - 1 + kMergeBufs;
-    const int streamed = (cap < nchunks) ? cap : nchunks;
-    if (!ok && t == 0)
-        for (int q = k; q < streamed; ++q)
-            wait_landed(b.merge_full((int)((first + q) % kMergeBufs)), ((first + q) / kMergeBufs) & 1u, c,
-                        kSiteMergeTail);
-    issued = first + (uint32_t)streamed;
-    epilogue_sync();   // every thread is done with the buffers and weights before they are reused
-    return ok;
 }
 
 // Per finished part: for each Q tile, read O_w out of TMEM, then release it
 // to the next part's first P.V.  A part that holds all of its Q tile's steps
 // writes O = acc / l in the input type and LSE = (m + log2 l) ln 2; a part of
 // a split tile writes its partial result to its workspace slot, and the part
-// that finishes last merges all of them -- after both Q tiles have been read
-// out, so that a merge never holds back the release of an accumulator.
-template <int D, bool BF16, bool CAUSAL>
-__device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, const float2 *handoff,
-                              volatile int *flag, uint32_t sMerge)
+// that finishes last hands the merge of that Q tile to the merge warp.
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+__device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, uint32_t s_handoff, uint32_t s_flag,
+                              uint32_t s_jobs)
 {
     using C = Cfg<D>;
     const int t = threadIdx.x % 128;              // row within a Q tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(t & ~31) << 16;
-    uint32_t n_st[2] = {0u, 0u}, n_pv[2] = {0u, 0u};
-    uint32_t merged = 0;                          // merge chunks streamed by this CTA
+    // Phase bits: bit w = parity of the st_ready(w) completions taken, bit
+    // 2 + w = parity of the P.V products of Q tile w done (o_done(w)).
+    uint32_t ph = 0;
+    uint32_t n_jobs = 0;                          // merge jobs posted
+
+    // Post a job in the next queue slot: nparts = 0 stops the merge warp.
+    // Thread k fills part k; false if the wait for a free slot gave up.
+    auto post = [&](int nparts, long long orow0, int nrows, int counter, int tile_ts, int n, int nw, int w, int clo,
+                    int chi) -> bool {
+        const int j = (int)(n_jobs % kJobSlots);
+        if (!epilogue_all(warp_wait(b.job_empty(j), ((n_jobs / kJobSlots) & 1u) ^ 1u, c, kSiteEpiJobFree)))
+            return false;
+        const uint32_t job = s_jobs + j * (uint32_t)sizeof(MergeJob);
+        if (t == 0) {
+            ptx::st_shared_u64(job + offsetof(MergeJob, orow0), (uint64_t)orow0);
+            ptx::st_shared_u32(job + offsetof(MergeJob, nrows), (uint32_t)nrows);
+            ptx::st_shared_u32(job + offsetof(MergeJob, nparts), (uint32_t)nparts);
+            ptx::st_shared_u32(job + offsetof(MergeJob, counter), (uint32_t)counter);
+        }
+        int k = 0, slot;
+        for (int cc = clo; cc <= chi && nparts > 0; ++cc)
+            if (sched_part_slot(p.sch, tile_ts, n, nw, cc, slot)) {
+                if (t == k && k < kMaxMergeParts) {
+                    const size_t srow = (size_t)slot * kCtaRows + w * kBM;
+                    ptx::st_shared_u64(job + offsetof(MergeJob, o_addr) + 8 * k, reinterpret_cast<uint64_t>(p.part_o + srow * D));
+                    ptx::st_shared_u64(job + offsetof(MergeJob, ml_addr) + 8 * k, reinterpret_cast<uint64_t>(p.part_ml + srow));
+                }
+                ++k;
+            }
+        epilogue_sync();   // the job is complete before it is handed over
+        if (t == 0)
+            ptx::mbar_arrive(b.job_full(j));
+        ++n_jobs;
+        return true;
+    };
 
     PartIter parts;
-    parts.init(p.sch, blockIdx.x);
+    parts.init_t<SPLIT>(p.sch, blockIdx.x);
     Part pt;
-    while (parts.next(p.sch, pt)) {
+    while (parts.next_t<SPLIT>(p.sch, pt)) {
         int bh, ct;
-        sched_decode(p.sch, pt.tile, bh, ct);
+        sched_decode_t<SPLIT>(p.sch, pt.tile, bh, ct);
         uint32_t published = 0;                   // bit w: Q tile w wrote a partial result
-#pragma unroll 1
+#pragma unroll
         for (int w = 0; w < kQTiles; ++w) {
             const int nw = sched_kv_tiles(p.sch, ct, w);
             const int np = part_steps(pt, nw);
             if (np == 0)
                 continue;
-            if (!epilogue_all(warp_wait(b.st_ready(w), n_st[w] & 1u, c, kSiteEpiStReady)))
+            // (the whole-tile variant has no warpgroup barrier to keep in step,
+            // so each warp may leave on its own)
+            bool ok = warp_wait(b.st_ready(w), (ph >> w) & 1u, c, kSiteEpiStReady);
+            if (!(SPLIT ? epilogue_all(ok) : ok))
                 return;
-            ++n_st[w];
-            const float2 st = handoff[w * kBM + t];
+            ph ^= 1u << w;
+            const float2 st = ptx::ld_shared_v2f32(s_handoff + (w * kBM + t) * 8);
             ptx::mbar_arrive(b.st_free(w));
-            n_pv[w] += (uint32_t)np;   // the last P.V of this part is completion n_pv - 1 of o_done(w)
-            if (!epilogue_all(warp_wait(b.o_done(w), (n_pv[w] - 1) & 1u, c, kSiteEpiODone)))
+            ph ^= ((uint32_t)np & 1u) << (2 + w);   // the part's last P.V completes phase (done so far - 1) of o_done(w)
+            ok = warp_wait(b.o_done(w), ((ph >> (2 + w)) & 1u) ^ 1u, c, kSiteEpiODone);
+            if (!(SPLIT ? epilogue_all(ok) : ok))
                 return;
             ptx::tc_fence_after_sync();
-            const bool whole = pt.kb == 0 && pt.ke >= nw;   // no other part holds steps of this Q tile
+            const bool whole = !SPLIT || (pt.kb == 0 && pt.ke >= nw);   // no other part holds steps of this Q tile
             const float inv_l = 1.f / st.y;
             const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
             const int row = ct * kCtaRows + w * kBM + t;
             const bool valid = row < p.N;
-            uint8_t *orow =
-                reinterpret_cast<uint8_t *>(p.O) + ((size_t)bh * p.N + (size_t)(valid ? row : 0)) * D * 2;
-            float *prow = whole ? nullptr : p.part_o + ((size_t)pt.slot * kCtaRows + w * kBM + t) * D;
             const uint32_t tO = tmem + C::col_o(w) + lane_off;
-#pragma unroll 1
-            for (int q = 0; q < D / 16; ++q) {   // 16 columns at a time keeps this warpgroup's registers low
-                uint32_t o[16];
-                ptx::tmem_ld16(tO + q * 16, o);
-                ptx::tmem_wait_ld();
-                float v[16];
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
-                                   v[2 * i], v[2 * i + 1]);
-                if (whole) {
-                    if (valid) {
-                        uint32_t pk[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            pk[i] = BF16 ? ptx::pack_bf16x2(v[2 * i], v[2 * i + 1]) : ptx::pack_f16x2(v[2 * i], v[2 * i + 1]);
-                        ptx::st_global_v4(orow + q * 32, pk[0], pk[1], pk[2], pk[3]);
-                        ptx::st_global_v4(orow + q * 32 + 16, pk[4], pk[5], pk[6], pk[7]);
-                    }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        ptx::st_global_v4(prow + q * 16 + 4 * u, __float_as_uint(v[4 * u]), __float_as_uint(v[4 * u + 1]),
-                                          __float_as_uint(v[4 * u + 2]), __float_as_uint(v[4 * u + 3]));
-                }
-            }
-            ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(b.o_free(w));
             if (whole) {
+                uint8_t *orow =
+                    reinterpret_cast<uint8_t *>(p.O) + ((size_t)bh * p.N + (size_t)(valid ? row : 0)) * D * 2;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tO + q * 32, o);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {   // packed in place: o[i] = columns 2i, 2i + 1
+                        float x, y;
+                        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2),
+                                       x, y);
+                        o[i] = BF16 ? ptx::pack_bf16x2(x, y) : ptx::pack_f16x2(x, y);
+                    }
+                    if (valid) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            ptx::st_global_v4(orow + q * 64 + v * 16, o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+                    }
+                }
                 if (valid)
                     p.LSE[(size_t)bh * p.N + row] = (st.x + log2f(st.y)) * kLn2;
             } else {
+                float *prow = p.part_o + ((size_t)pt.slot * kCtaRows + w * kBM + t) * D;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tO + q * 32, o);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        float x0, x1, x2, x3;
+                        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1])), il2),
+                                       x0, x1);
+                        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3])), il2),
+                                       x2, x3);
+                        ptx::st_global_v4(prow + q * 32 + 4 * u, __float_as_uint(x0), __float_as_uint(x1),
+                                          __float_as_uint(x2), __float_as_uint(x3));
+                    }
+                }
                 p.part_ml[(size_t)pt.slot * kCtaRows + w * kBM + t] = st;
                 published |= 1u << w;
             }
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(b.o_free(w));
         }
-        if (published == 0)
+        if (!SPLIT || published == 0)
             continue;
         // Split tile: make this part's partials visible, count it in, and
-        // merge each Q tile for which it is the last part to finish.
+        // hand over the merge of each Q tile for which it is the last part to
+        // finish.  The tile's parts are held by this CTA and its neighbours.
+        const int n = sched_steps(p.sch, pt.tile);
+        int clo, chi;
+        sched_tile_ctas_near(p.sch, pt.ts, n, blockIdx.x, clo, chi);
         __threadfence();
         epilogue_sync();
         if (t == 0) {
@@ -988,36 +1049,41 @@ __device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl 
                 if (!(published >> w & 1u))
                     continue;
                 const int nw = sched_kv_tiles(p.sch, ct, w);
-                const int expected = sched_part_slots(p.sch, pt.tile, nw, nullptr, 0);
+                int expected = 0, slot;
+                for (int cc = clo; cc <= chi; ++cc)
+                    expected += sched_part_slot(p.sch, pt.ts, n, nw, cc, slot) ? 1 : 0;
                 const int done = atomicAdd(&p.counters[2 * pt.tile + w], 1) + 1;
                 if (done == expected)
                     last |= 1 << w;
             }
-            *flag = last;
+            if (last)
+                __threadfence();   // acquire: the other parts' partials are visible to this CTA
+            ptx::st_shared_u32(s_flag, (uint32_t)last);
         }
         epilogue_sync();
-        const int last = *flag;
+        const int last = (int)ptx::ld_shared_u32(s_flag);
         epilogue_sync();   // every thread has read the flag before it is reused
-        if (last == 0)
-            continue;
-        __threadfence();
 #pragma unroll 1
         for (int w = 0; w < kQTiles; ++w) {
             if (!(last >> w & 1))
                 continue;
-            if (!merge_parts<D, BF16>(p, pt.tile, sched_kv_tiles(p.sch, ct, w), w, bh, ct, sMerge,
-                                      sMerge + (C::kWeightOff - C::kMergeOff), sMerge + (C::kSlotOff - C::kMergeOff), b,
-                                      merged, c))
+            const int nw = sched_kv_tiles(p.sch, ct, w);
+            int nparts = 0, slot;
+            for (int cc = clo; cc <= chi; ++cc)
+                nparts += sched_part_slot(p.sch, pt.ts, n, nw, cc, slot) ? 1 : 0;
+            const int r_base = ct * kCtaRows + w * kBM;
+            if (!post(nparts < kMaxMergeParts ? nparts : kMaxMergeParts, (long long)bh * p.N + r_base,
+                      (p.N - r_base < kBM) ? p.N - r_base : kBM, 2 * pt.tile + w, pt.ts, n, nw, w, clo, chi))
                 return;
-            if (t == 0)
-                p.counters[2 * pt.tile + w] = 0;   // ready for the next launch
         }
     }
+    if (SPLIT)
+        post(0, 0, 0, 0, 0, 0, 0, 0, 0, -1);   // stop the merge warp
 }
 
 // ------------------------------------------------------------------ kernel
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p)
@@ -1057,8 +1123,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(b.o_free(w), kBM);
         }
         ptx::mbar_init(b.drain(), C::kMmaWarps);
-        for (int i = 0; i < kMergeBufs; ++i)
+        for (int i = 0; SPLIT && i < kMergeBufs; ++i)
             ptx::mbar_init(b.merge_full(i), 1);
+        if (SPLIT)
+            ptx::mbar_init(b.ml_full(), 1);
+        for (int j = 0; SPLIT && j < kJobSlots; ++j) {
+            ptx::mbar_init(b.job_full(j), 1);
+            ptx::mbar_init(b.job_empty(j), 1);
+        }
         *c.abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -1078,17 +1150,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (wg < kEpilogueWarpgroup) {
         ptx::regs_increase<kRegsSoftmax>();
-        softmax_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff);
+        softmax_role<D, BF16, CAUSAL, SPLIT>(p, tmem, b, c, handoff);
     } else if (wg == kEpilogueWarpgroup) {
         ptx::regs_decrease<kRegsEpilogue>();
-        epilogue_role<D, BF16, CAUSAL>(p, tmem, b, c, handoff, reinterpret_cast<volatile int *>(misc + 2),
-                                       base + C::kMergeOff);
+        epilogue_role<D, BF16, CAUSAL, SPLIT>(p, tmem, b, c, base + C::kHandOff, base + C::kMiscOff + 8, base + C::kJobOff);
     } else {
         ptx::regs_decrease<kRegsProducer>();
         if (warp == kLoadWarp)
-            load_role<D, CAUSAL>(&tmQ, &tmK, &tmV, p, sQ, sStage, b, c);
+            load_role<D, CAUSAL, SPLIT>(&tmQ, &tmK, &tmV, p, sQ, sStage, b, c);
         else if (warp < kMmaWarp + C::kMmaWarps)
-            mma_role<D, BF16, CAUSAL>(warp - kMmaWarp, p, sQ, sStage, tmem, b, c);
+            mma_role<D, BF16, CAUSAL, SPLIT>(warp - kMmaWarp, p, sQ, sStage, tmem, b, c);
+        else if (SPLIT && warp == kMergeWarp)
+            merge_role<D, BF16>(p, base + C::kMergeOff, base + C::kMlOff,
+                                reinterpret_cast<const MergeJob *>(base_ptr + C::kJobOff), b, c);
     }
 
     ptx::tc_fence_before_sync();

@@ -1,0 +1,100 @@
+// fa_launch.cuh -- kernel selection and launch, shared by the two translation
+// units that instantiate the kernels: fa_api.cu (whole-tile variants, with the
+// C ABI) and fa_split.cu (balanced-schedule variants).  Two units keep each
+// nvcc run to eight kernels and let the build compile them in parallel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace fa_launch {
+
+constexpr int kMaxDevices = 64;
+
+// Internal linkage: each translation unit launches its own kernels, and the
+// once-per-device flags must stay private to this library (a template's
+// static locals would otherwise be one object per process, shared with any
+// other copy of the library loaded beside it).
+namespace {
+
+// Launch one variant on `grid` CTAs.  The dynamic shared-memory limit is
+// raised once per device and variant.
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+fa_status launch_variant(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const fa::FwdParams &p,
+                         int grid, cudaStream_t stream, int dev)
+{
+    static std::mutex mu;
+    static bool attr_set[kMaxDevices] = {};
+    auto kern = fa::fa_fwd_sm103<D, BF16, CAUSAL, SPLIT>;
+    constexpr int smem = fa::Cfg<D>::smem_bytes(SPLIT);
+    if (dev < 0 || dev >= kMaxDevices)
+        return FA_ERR_UNSUPPORTED_DEVICE;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+                cudaGetLastError();
+                return FA_ERR_CUDA;
+            }
+            attr_set[dev] = true;
+        }
+    }
+    kern<<<grid, fa::kThreads, smem, stream>>>(q, k, v, p);
+    if (cudaGetLastError() != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+template <bool SPLIT>
+fa_status launch_any(int D, bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                     const fa::FwdParams &p, int grid, cudaStream_t s, int dev)
+{
+    if (D == 64) {
+        if (bf16)
+            return causal ? launch_variant<64, true, true, SPLIT>(q, k, v, p, grid, s, dev)
+                          : launch_variant<64, true, false, SPLIT>(q, k, v, p, grid, s, dev);
+        return causal ? launch_variant<64, false, true, SPLIT>(q, k, v, p, grid, s, dev)
+                      : launch_variant<64, false, false, SPLIT>(q, k, v, p, grid, s, dev);
+    }
+    if (bf16)
+        return causal ? launch_variant<128, true, true, SPLIT>(q, k, v, p, grid, s, dev)
+                      : launch_variant<128, true, false, SPLIT>(q, k, v, p, grid, s, dev);
+    return causal ? launch_variant<128, false, true, SPLIT>(q, k, v, p, grid, s, dev)
+                  : launch_variant<128, false, false, SPLIT>(q, k, v, p, grid, s, dev);
+}
+
+// Read and clear this translation unit's device status word (current
+// device) into *word; false if the copy failed.
+inline bool take_status_word_here(unsigned int *word)
+{
+    *word = 0;
+    if (cudaMemcpyFromSymbol(word, fa::g_status_word, sizeof *word) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (*word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(fa::g_status_word, &zero, sizeof zero) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+    }
+    return true;
+}
+
+}  // namespace
+
+// Defined in fa_api.cu and fa_split.cu respectively.
+fa_status launch_whole(int D, bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k,
+                       const CUtensorMap &v, const fa::FwdParams &p, int grid, cudaStream_t s, int dev);
+fa_status launch_split(int D, bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k,
+                       const CUtensorMap &v, const fa::FwdParams &p, int grid, cudaStream_t s, int dev);
+bool take_status_word_whole(unsigned int *word);
+bool take_status_word_split(unsigned int *word);
+
+}  // namespace fa_launch

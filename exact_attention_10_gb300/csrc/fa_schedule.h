@@ -96,6 +96,34 @@ FA_HD void sched_decode(const Schedule &s, int t, int &bh, int &ct)
     }
 }
 
+// The round-robin order alone (the kernel's whole-tile variant).
+FA_HD void sched_decode_rr(const Schedule &s, int t, int &bh, int &ct)
+{
+    if (s.causal) {
+        ct = s.C - 1 - t / s.BH;
+        bh = t % s.BH;
+    } else {
+        bh = t / s.C;
+        ct = t % s.C;
+    }
+}
+
+FA_HD int sched_steps_rr(const Schedule &s, int t)
+{
+    if (!s.causal)
+        return s.nkv;
+    return sched_steps_ct(s, s.C - 1 - t / s.BH);
+}
+
+template <bool SPLIT>
+FA_HD void sched_decode_t(const Schedule &s, int t, int &bh, int &ct)
+{
+    if (SPLIT)
+        sched_decode(s, t, bh, ct);
+    else
+        sched_decode_rr(s, t, bh, ct);
+}
+
 FA_HD int sched_steps(const Schedule &s, int t)
 {
     int bh, ct;
@@ -189,6 +217,7 @@ struct Part {
     int kb;
     int ke;
     int slot;
+    int ts;     // balanced: the tile's first unit in the ordered sequence (0 for round-robin)
 };
 
 // The parts of CTA c.  Every role of the CTA walks the same sequence.  In the
@@ -203,14 +232,18 @@ struct PartIter {
     int c;
     int u, ue, tstart;   // balanced: next unit, end of the in-order units, first unit of tile t
     int t, tsteps;
-    int lt, lke;         // balanced: the range's last part, tile lt steps [0, lke), still to come (lt >= 0)
+    int lt, lke, lts;    // balanced: the range's last part, tile lt (first unit lts) steps [0, lke), still to come (lt >= 0)
 
-    FA_HD void init(const Schedule &s, int c_)
+    // The kernel knows its schedule at compile time (SPLIT = s.split) and
+    // takes only that path; init / next decide at run time (host code).
+    template <bool SPLIT>
+    FA_HD void init_t(const Schedule &s, int c_)
     {
         c = c_;
         lt = -1;
         lke = 0;
-        if (s.split) {
+        lts = 0;
+        if (SPLIT) {
             u = s.range[c];
             ue = s.range[c + 1];
             if (u < ue) {
@@ -219,6 +252,7 @@ struct PartIter {
                 if (ls > u) {   // the range ends in a later tile than it starts in
                     lt = tl;
                     lke = ue - ls;
+                    lts = ls;
                     ue = ls;
                 }
                 t = sched_tile_of_unit(s, u, tstart);
@@ -233,14 +267,16 @@ struct PartIter {
         }
     }
 
-    FA_HD bool next(const Schedule &s, Part &p)
+    template <bool SPLIT>
+    FA_HD bool next_t(const Schedule &s, Part &p)
     {
-        if (s.split) {
+        if (SPLIT) {
             if (lt >= 0) {
                 p.tile = lt;
                 p.kb = 0;
                 p.ke = lke;
                 p.slot = 2 * c + 1;
+                p.ts = lts;
                 lt = -1;
                 return true;
             }
@@ -250,6 +286,7 @@ struct PartIter {
             p.kb = u - tstart;
             p.ke = (ue - tstart < tsteps) ? ue - tstart : tsteps;
             p.slot = 2 * c + ((u == s.range[c]) ? 0 : 1);
+            p.ts = tstart;
             u = tstart + p.ke;
             if (p.ke == tsteps) {
                 tstart += tsteps;
@@ -262,10 +299,24 @@ struct PartIter {
             return false;
         p.tile = t;
         p.kb = 0;
-        p.ke = sched_steps(s, t);
+        p.ke = sched_steps_rr(s, t);
         p.slot = -1;
+        p.ts = 0;
         t += s.G;
         return true;
+    }
+
+    FA_HD void init(const Schedule &s, int c_)
+    {
+        if (s.split)
+            init_t<true>(s, c_);
+        else
+            init_t<false>(s, c_);
+    }
+
+    FA_HD bool next(const Schedule &s, Part &p)
+    {
+        return s.split ? next_t<true>(s, p) : next_t<false>(s, p);
     }
 };
 
@@ -276,6 +327,18 @@ FA_HD void sched_tile_ctas(const Schedule &s, int t, int &pt, int &n, int &clo, 
     n = sched_steps(s, t);
     clo = sched_cta_of_unit(s, pt);
     chi = sched_cta_of_unit(s, pt + n - 1);
+}
+
+// The CTAs that hold parts of the tile with first unit pt and n units, found
+// by walking out from c0, a CTA known to hold one of them: clo .. chi.
+FA_HD void sched_tile_ctas_near(const Schedule &s, int pt, int n, int c0, int &clo, int &chi)
+{
+    clo = c0;
+    while (clo > 0 && s.range[clo] > pt)
+        --clo;
+    chi = c0;
+    while (chi + 1 < s.G && s.range[chi + 1] < pt + n)
+        ++chi;
 }
 
 // Whether CTA c holds a part of tile t (first unit pt, n units) in which a Q

@@ -39,6 +39,14 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+/* The library is built with hidden symbol visibility; only these entry
+ * points are exported. */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -115,7 +123,7 @@ typedef enum {
  *
  * fa_fwd uses FA_SCHEDULE_AUTO.
  */
-fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+FA_API fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
                  int B, int H, int N, int D, int causal, float scale,
                  fa_dtype dtype, fa_stream_t stream);
 
@@ -125,7 +133,7 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
  * request the shape cannot take (more than 2^30 units of work) runs whole
  * tiles.
  */
-fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
+FA_API fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
                     int B, int H, int N, int D, int causal, float scale,
                     fa_dtype dtype, fa_schedule schedule, fa_stream_t stream);
 
@@ -135,10 +143,10 @@ fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float 
  * gave up on a wait since the last call, or FA_ERR_CUDA if the synchronise
  * itself failed.
  */
-fa_status fa_sync_status(fa_stream_t stream);
+FA_API fa_status fa_sync_status(fa_stream_t stream);
 
 /* Static, NUL-terminated description of a status code. */
-const char *fa_status_string(fa_status s);
+FA_API const char *fa_status_string(fa_status s);
 
 #ifdef __cplusplus
 }

@@ -66,6 +66,19 @@ static int check_schedule(const Schedule &s, bool planned)
                 std::printf("bad part c=%d tile=%d kb=%d ke=%d\n", c, p.tile, p.kb, p.ke);
                 return 1;
             }
+            if (split && p.ts != (int)sched_prefix(s, p.tile)) {
+                std::printf("part of tile %d carries first unit %d, expected %lld\n", p.tile, p.ts, sched_prefix(s, p.tile));
+                return 1;
+            }
+            if (split) {   // the neighbour walk from this CTA finds the same CTAs as the searches
+                int pt, n, clo, chi, lo2, hi2;
+                sched_tile_ctas(s, p.tile, pt, n, clo, chi);
+                sched_tile_ctas_near(s, p.ts, n, c, lo2, hi2);
+                if (lo2 != clo || hi2 != chi) {
+                    std::printf("tile %d: CTAs %d..%d by search, %d..%d by walk from %d\n", p.tile, clo, chi, lo2, hi2, c);
+                    return 1;
+                }
+            }
             for (int j = p.kb; j < p.ke; ++j)
                 ++cover[p.tile][j];
             units += p.ke - p.kb;

@@ -42,6 +42,21 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_library_exports_nothing_else(lib):
+    """Built with hidden visibility: the dynamic symbol table holds the ABI
+    functions only, so no internal symbol (a launcher's once-per-device flags,
+    say) can be unified with another copy of the library in the process."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", fa_build.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    names = sorted(line.split()[-1] for line in out.splitlines() if line.strip())
+    assert names == _declared_functions(), names
+
+
 def test_status_strings(lib):
     for code in range(6):
         s = fa.status_string(code)

@@ -170,6 +170,30 @@ def test_schedules_agree(causal):
     assert dl <= 1e-4
 
 
+def test_two_library_copies_in_one_process(tmp_path):
+    """A second, separately loaded copy of the library launches its own
+    kernels correctly (its launch set-up is private to it)."""
+    import ctypes
+    import shutil
+    from exact_attention_10_gb300 import build as fa_build
+    copy = str(tmp_path / "libfa_copy.so")
+    shutil.copy(fa_build.LIB_PATH, copy)
+    lib2 = fa.load(copy)
+    w = WORKLOADS["b2h16_n4096"]
+    q, k, v = (x.cuda() for x in make_qkv(w, seed=0))
+    o1, l1 = fa.forward(q, k, v, causal=False, scale=w.scale, schedule="balanced")
+    o2 = torch.empty_like(q)
+    l2 = torch.empty_like(l1)
+    st = torch.cuda.current_stream().cuda_stream
+    for sched in (1, 2):   # whole tiles, balanced
+        rc = lib2.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(), l2.data_ptr(), w.B, w.H, w.N,
+                            w.D, 0, ctypes.c_float(w.scale), 0, sched, ctypes.c_void_p(st))
+        assert rc == 0, rc
+        assert lib2.fa_sync_status(ctypes.c_void_p(st)) == 0
+        if sched == 2:
+            assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_rejects_unknown_schedule():
     w = WORKLOADS["tiny_n256"]
     q, k, v = (x.cuda() for x in make_qkv(w, seed=0))
