@@ -199,9 +199,12 @@ bool take_status_word_whole(unsigned int *word)
 
 }  // namespace fa_launch
 
-extern "C" fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
-                               int N, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
-                               fa_stream_t stream)
+namespace {
+
+// fa_fwd_ex and fa_fwd_noalloc: identical but for where a balanced schedule's
+// workspace comes from (no_alloc: the library's static array).
+fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N, int D,
+                   int causal, float scale, fa_dtype dtype, fa_schedule schedule, fa_stream_t stream, bool no_alloc)
 {
     // Arguments first: nothing below touches the device until they are sound.
     if (dtype != FA_BF16 && dtype != FA_FP16)
@@ -257,13 +260,30 @@ extern "C" fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void
     p.sch = fa::sched_plan(N, (int)BH, causal != 0, di->sms, (int)schedule);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (p.sch.split) {
-        const fa_status ws = workspace_for(dev, s, p.sch, D, &p);
+        const fa_status ws =
+            no_alloc ? fa_launch::noalloc_workspace(dev, s, p.sch, D, &p) : workspace_for(dev, s, p.sch, D, &p);
         if (ws != FA_OK)
             return ws;
     }
     if (p.sch.split)
         return fa_launch::launch_split(D, bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
     return fa_launch::launch_whole(D, bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                               int N, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
+                               fa_stream_t stream)
+{
+    return fwd_impl(Q, K, V, O, LSE, B, H, N, D, causal, scale, dtype, schedule, stream, false);
+}
+
+extern "C" fa_status fa_fwd_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                                    int N, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
+                                    fa_stream_t stream)
+{
+    return fwd_impl(Q, K, V, O, LSE, B, H, N, D, causal, scale, dtype, schedule, stream, true);
 }
 
 extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
@@ -305,6 +325,7 @@ extern "C" const char *fa_status_string(fa_status s)
     case FA_ERR_UNSUPPORTED_DEVICE: return "no compute capability 10.3 device";
     case FA_ERR_CUDA: return "CUDA runtime or launch error";
     case FA_ERR_DEVICE_TIMEOUT: return "a bounded wait inside the kernel expired";
+    case FA_ERR_NO_ALLOC_LIMIT: return "the call needs more than the no-allocation entry point's static workspace";
     }
     return "unknown status";
 }

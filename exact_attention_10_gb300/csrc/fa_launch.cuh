@@ -97,4 +97,20 @@ fa_status launch_split(int D, bool bf16, bool causal, const CUtensorMap &q, cons
 bool take_status_word_whole(unsigned int *word);
 bool take_status_word_split(unsigned int *word);
 
+// The static workspace of fa_fwd_noalloc (fa_split.cu): points p's partial
+// buffers into it for schedule `sc` and head size D, and clears the counters
+// on `stream`.  FA_ERR_NO_ALLOC_LIMIT if the schedule needs more.
+fa_status noalloc_workspace(int dev, cudaStream_t stream, const fa::Schedule &sc, int D, fa::FwdParams *p);
+
+// Bytes of workspace a balanced schedule needs: partial O and (m, l) for two
+// slots per CTA, then one counter per (tile, Q tile).
+inline size_t workspace_bytes(const fa::Schedule &sc, int D, size_t *o_bytes, size_t *ml_bytes, size_t *cnt_bytes)
+{
+    const size_t slots = (size_t)2 * sc.G;
+    *o_bytes = slots * fa::kCtaRows * D * sizeof(float);
+    *ml_bytes = slots * fa::kCtaRows * sizeof(float2);
+    *cnt_bytes = (size_t)2 * sc.T * sizeof(int);
+    return *o_bytes + *ml_bytes + *cnt_bytes;
+}
+
 }  // namespace fa_launch

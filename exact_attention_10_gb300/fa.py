@@ -13,8 +13,8 @@ from .build import LIB_PATH
 
 FA_BF16, FA_FP16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_MISALIGNED", 3: "FA_ERR_UNSUPPORTED_DEVICE",
-          4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
-EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_sync_status", "fa_status_string")
+          4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT", 6: "FA_ERR_NO_ALLOC_LIMIT"}
+EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_noalloc", "fa_sync_status", "fa_status_string")
 SCHEDULES = {"auto": 0, "whole_tiles": 1, "balanced": 2}
 
 _lib = None
@@ -39,6 +39,8 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd.restype = c_int
     lib.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, ctypes.c_float, c_int, c_int, vp]
     lib.fa_fwd_ex.restype = c_int
+    lib.fa_fwd_noalloc.argtypes = lib.fa_fwd_ex.argtypes
+    lib.fa_fwd_noalloc.restype = c_int
     lib.fa_sync_status.argtypes = [vp]
     lib.fa_sync_status.restype = c_int
     lib.fa_status_string.argtypes = [c_int]

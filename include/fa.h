@@ -90,7 +90,8 @@ typedef enum {
     FA_ERR_MISALIGNED = 2,         /* a pointer is not 16-byte aligned (the tensor-copy engine needs it) */
     FA_ERR_UNSUPPORTED_DEVICE = 3, /* no device, or the current device is not compute capability 10.3 */
     FA_ERR_CUDA = 4,               /* a CUDA runtime call or the launch failed */
-    FA_ERR_DEVICE_TIMEOUT = 5      /* a bounded in-kernel wait expired (reported by fa_sync_status) */
+    FA_ERR_DEVICE_TIMEOUT = 5,     /* a bounded in-kernel wait expired (reported by fa_sync_status) */
+    FA_ERR_NO_ALLOC_LIMIT = 6      /* fa_fwd_noalloc: the call needs more than its static workspace */
 } fa_status;
 
 /*
@@ -136,6 +137,45 @@ FA_API fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, fl
 FA_API fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
                     int B, int H, int N, int D, int causal, float scale,
                     fa_dtype dtype, fa_schedule schedule, fa_stream_t stream);
+
+/*
+ * fa_fwd_noalloc -- fa_fwd_ex that allocates no memory, device or host, at
+ * any call.  The pages describe nothing like it: the method itself needs no
+ * scratch, and this entry point only concerns where this library's balanced
+ * schedule keeps its partial results.
+ *
+ * Who needs it: callers that cannot let a library allocate device memory on
+ * their behalf -- a serving loop whose latency budget has no room for the
+ * implicit device-wide synchronisation cudaMalloc / cudaFree may perform, or
+ * a framework that owns every byte of device memory through its own pool and
+ * forbids allocations behind its back.  fa_fwd_ex would allocate its
+ * per-stream workspace on the first balanced call; this entry point instead
+ * uses a workspace compiled into the library: a static device array of
+ * FA_NOALLOC_WORKSPACE_BYTES per device.
+ *
+ * Set-up: the first call on a device looks up that array's address
+ * (cudaGetSymbolAddress, which may load the library's code onto the device)
+ * and keeps it; make that first call before any stream capture.  Every call
+ * clears the partial-result counters (which must start at zero) with an
+ * asynchronous memset on `stream`.
+ *
+ * Limit: a call whose schedule (as fa_fwd_ex would choose it) needs more
+ * workspace than the array holds returns FA_ERR_NO_ALLOC_LIMIT before
+ * anything is enqueued.  The partial-result slots always fit; the counters
+ * take 8 bytes per 256 query rows per head, so B*H*ceil(N/256) may reach
+ * 966,656 -- e.g. B*H = 256 at N = 965,000.  Whole-tile calls need no
+ * workspace and have no limit.
+ *
+ * Overlapping calls race: there is one workspace per device, so two calls
+ * whose work can overlap (on different streams, without ordering between
+ * them) must not both run the balanced schedule; calls on one stream are
+ * ordered and safe.  Arguments, results and other errors are as for
+ * fa_fwd_ex.
+ */
+#define FA_NOALLOC_WORKSPACE_BYTES (48u << 20)
+FA_API fa_status fa_fwd_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                int B, int H, int N, int D, int causal, float scale,
+                                fa_dtype dtype, fa_schedule schedule, fa_stream_t stream);
 
 /*
  * fa_sync_status -- synchronise `stream`, then return and clear the device

@@ -58,7 +58,7 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         s = fa.status_string(code)
         assert s and s != "unknown status"
     assert fa.status_string(99) == "unknown status"
