@@ -628,7 +628,11 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
                                               fmaxf(mx[6], mx[7])) * p.qk_scale;
             // The running max changes only when this tile holds a larger score
             // (always on the first visible tile, where m = -inf); otherwise
-            // alpha = 1 and nothing is rescaled.
+            // alpha = 1 and nothing is rescaled.  (A stale max within a
+            // threshold would save rescales but is not used: with it a row's
+            // dominant probability is no longer exactly 1, and its 16-bit
+            // rounding lands on outputs dominated by one key -- measured
+            // 1.7e-2 in bf16 with Q and K amplified 4x.)
             const bool move = tile_max > m;
             const float m_new = move ? tile_max : m;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;   // no visible key yet: shift 0
@@ -669,21 +673,23 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             // moved (ever less likely as more keys have been seen).
             if (jr > 0 && __any_sync(0xffffffffu, move)) {
                 const uint64_t al2 = ptx::f2_pack(alpha, alpha);
+                uint32_t o[D / 32][32];   // all of O_w's row in flight, one wait
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q)
+                    ptx::tmem_ld32(tO + q * 32, o[q]);
+                ptx::tmem_wait_ld();
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(tO + q * 32, o);
-                    ptx::tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         float lo, hi;
-                        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[q][2 * i]), __uint_as_float(o[q][2 * i + 1])),
                                                    al2),
                                        lo, hi);
-                        o[2 * i] = __float_as_uint(lo);
-                        o[2 * i + 1] = __float_as_uint(hi);
+                        o[q][2 * i] = __float_as_uint(lo);
+                        o[q][2 * i + 1] = __float_as_uint(hi);
                     }
-                    ptx::tmem_st32(tO + q * 32, o);
+                    ptx::tmem_st32(tO + q * 32, o[q]);
                 }
             }
             ptx::tmem_wait_st();
