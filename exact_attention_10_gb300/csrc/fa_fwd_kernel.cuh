@@ -591,10 +591,9 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             ++s_phase;
             ptx::tc_fence_after_sync();
 
-            uint32_t r[4][32];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                ptx::tmem_ld32(tS + q * 32, r[q]);
+            uint32_t r[2][64];
+            ptx::tmem_ld64(tS, r[0]);   // the whole row of S_w in two instructions
+            ptx::tmem_ld64(tS + 64, r[1]);
             ptx::tmem_wait_ld();
             if (C::kSeparateP) {   // S_w may now be overwritten by the next step's MMA
                 ptx::tc_fence_before_sync();
@@ -603,10 +602,8 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
 
             float s[128];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    s[q * 32 + i] = __uint_as_float(r[q][i]);
+            for (int i = 0; i < 128; ++i)
+                s[i] = __uint_as_float(r[i / 64][i % 64]);
 
             if ((CAUSAL && j == nw - 1) || (j + 1) * kBN > p.N) {
                 const int lim = row_limit - j * kBN;
@@ -642,18 +639,15 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             // Exponentials into packed 16-bit pairs first (registers only), so
             // they overlap the previous step's P.V, which still reads P_w.
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-            uint32_t pk[2][32];
+            uint32_t pk[64];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const uint64_t x = ptx::f2_fma(ptx::f2_pack(s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1]), qk2, negm2);
-                    float x0, x1;
-                    ptx::f2_unpack(x, x0, x1);
-                    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-                    acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
-                    pk[h][i] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
-                }
+            for (int i = 0; i < 64; ++i) {
+                const uint64_t x = ptx::f2_fma(ptx::f2_pack(s[2 * i], s[2 * i + 1]), qk2, negm2);
+                float x0, x1;
+                ptx::f2_unpack(x, x0, x1);
+                const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
+                pk[i] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
             }
             if (C::kSeparateP && jr > 0) {   // P.V of the previous step done: P_w may be overwritten, O_w is final
                 if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
@@ -661,8 +655,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
                 ++o_phase;
                 ptx::tc_fence_after_sync();
             }   // (D = 128: S_w(j) is issued after P.V_w(j-1), so s_full already implies it)
-            ptx::tmem_st32(tP, pk[0]);
-            ptx::tmem_st32(tP + 32, pk[1]);
+            ptx::tmem_st64(tP, pk);
             const uint64_t a2 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
             float a_lo, a_hi;
             ptx::f2_unpack(a2, a_lo, a_hi);
@@ -673,15 +666,15 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             // moved (ever less likely as more keys have been seen).
             if (jr > 0 && __any_sync(0xffffffffu, move)) {
                 const uint64_t al2 = ptx::f2_pack(alpha, alpha);
-                uint32_t o[D / 32][32];   // all of O_w's row in flight, one wait
+                uint32_t o[D / 64][64];   // all of O_w's row, 64 columns per instruction, one wait
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q)
-                    ptx::tmem_ld32(tO + q * 32, o[q]);
+                for (int q = 0; q < D / 64; ++q)
+                    ptx::tmem_ld64(tO + q * 64, o[q]);
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
+                for (int q = 0; q < D / 64; ++q) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < 32; ++i) {
                         float lo, hi;
                         ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[q][2 * i]), __uint_as_float(o[q][2 * i + 1])),
                                                    al2),
@@ -689,7 +682,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
                         o[q][2 * i] = __float_as_uint(lo);
                         o[q][2 * i + 1] = __float_as_uint(hi);
                     }
-                    ptx::tmem_st32(tO + q * 32, o[q]);
+                    ptx::tmem_st64(tO + q * 64, o[q]);
                 }
             }
             ptx::tmem_wait_st();
