@@ -55,6 +55,22 @@ def _dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest of every rank's value (this rank's value when single)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, steps: int, flops_per_step: float, slowest_ms: float) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of the same
+    replica, and the job takes as long as its slowest rank."""
+    return world * steps * flops_per_step / (slowest_ms * 1e-3) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples while the timed region runs."""
 
@@ -292,13 +308,9 @@ def main(argv=None):
     if rc != 0:
         raise fa.FAError(rc, "timed region")
     ms = {c: [s.elapsed_time(e) for s, e in zip(starts[c], ends[c])] for c in modes}
-    total_ms = sum(sum(v) for v in ms.values())
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(sum(v) for v in ms.values()), dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * args.steps * (F[False] + F[True]) / (total_ms * 1e-3) / 1e12
+    value = job_tflops(world, args.steps, F[False] + F[True], total_ms)
     clk = clocks.finish()
 
     # end to end through the C ABI: pinned host inputs in, O and LSE back out, every step
@@ -327,12 +339,8 @@ def main(argv=None):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * e2e_steps * (F[False] + F[True]) / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    e2e_value = job_tflops(world, e2e_steps, F[False] + F[True], e2e_ms)
 
     peak, peak_sus, _, peak_src = _peaks()
     mode_info = {}
