@@ -31,6 +31,15 @@
  * IEEE/bfloat16 format definitions) or float64.  Outputs are float64 and are
  * NOT rounded to the input dtype: output rounding counts against tolerance.
  *
+ * attn_ref_forward_qkv() is the same definition for Nq queries against Nkv
+ * keys (cross attention, decode).  Its causal mask is aligned bottom-right:
+ * query i sees keys j <= i + (Nkv - Nq), so the last query sees every key --
+ * the alignment under which decoding the last Nq positions of a sequence
+ * gives the last Nq rows of its square causal attention; it equals the
+ * top-left mask when Nq = Nkv ("How to profile and optimise kernels", causal
+ * alignment).  A query that sees no key (possible when Nq > Nkv) gets O = 0
+ * and LSE = -inf, the empty sum's value.
+ *
  * Besides the explicit definition, attn_ref_tiled() runs the tiled online-
  * softmax recurrence in fp64, step by step in the order the pages give it, so
  * the tests can show that the recurrence equals the definition on small
@@ -106,13 +115,20 @@ void attn_ref_decode(const uint16_t *bits, int dtype, long n, double *out)
 }
 
 /*
- * One query row, straight from the definition above.  q is row i of Q, Kh and
- * Vh the whole [N, D] key and value slices of its head, x a scratch of N.
+ * One query row, straight from the definition above, over the visible keys
+ * 0 .. nvis-1.  q is the query row, Kh and Vh the key and value slices of its
+ * head, x a scratch of at least nvis.  With no visible key, O = 0 and
+ * LSE = -inf.
  */
-static void ref_row(const double *q, const double *Kh, const double *Vh, long N, long D, long i,
-                    int causal, double s, double *x, double *o, double *lse)
+static void ref_row_vis(const double *q, const double *Kh, const double *Vh, long nvis, long D, double s,
+                        double *x, double *o, double *lse)
 {
-    long nvis = causal ? i + 1 : N;     /* |J|: keys 0..i when causal, all N keys otherwise */
+    if (nvis <= 0) {
+        for (long d = 0; d < D; ++d)
+            o[d] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
     double m = -INFINITY;
     for (long j = 0; j < nvis; ++j) {
         double dot = 0.0;
@@ -134,6 +150,13 @@ static void ref_row(const double *q, const double *Kh, const double *Vh, long N,
     for (long d = 0; d < D; ++d)
         o[d] /= l;
     *lse = m + log(l);
+}
+
+/* Row i of square attention: keys 0..i when causal, all N keys otherwise. */
+static void ref_row(const double *q, const double *Kh, const double *Vh, long N, long D, long i,
+                    int causal, double s, double *x, double *o, double *lse)
+{
+    ref_row_vis(q, Kh, Vh, causal ? i + 1 : N, D, s, x, o, lse);
 }
 
 /*
@@ -169,6 +192,54 @@ int attn_ref_forward(const void *Q, const void *K, const void *V, int dtype,
                 for (long i = 0; i < N; ++i)
                     ref_row(Qh + i * D, Kh, Vh, N, D, i, causal, s, x,
                             O + base + (size_t)i * D, LSE + (size_t)bh * N + i);
+            }
+            free(x);
+        }
+    }
+    free(Kh); free(Vh); free(Qh);
+    return failed ? -1 : 0;
+}
+
+/*
+ * Full forward of Nq queries against Nkv keys: Q and O are [BH, Nq, D], K and
+ * V are [BH, Nkv, D], LSE is [BH, Nq]; the causal mask is bottom-right (query
+ * i sees keys j <= i + Nkv - Nq).  Returns 0, or -1 if a scratch allocation
+ * failed.
+ */
+int attn_ref_forward_qkv(const void *Q, const void *K, const void *V, int dtype,
+                         long BH, long Nq, long Nkv, long D, int causal, double s,
+                         double *O, double *LSE)
+{
+    size_t qslice = (size_t)Nq * (size_t)D, kslice = (size_t)Nkv * (size_t)D;
+    double *Kh = (double *)malloc(kslice * sizeof(double));
+    double *Vh = (double *)malloc(kslice * sizeof(double));
+    double *Qh = (double *)malloc(qslice * sizeof(double));
+    if (!Kh || !Vh || !Qh) {
+        free(Kh); free(Vh); free(Qh);
+        return -1;
+    }
+    int failed = 0;
+    for (long bh = 0; bh < BH; ++bh) {
+        load_slice(Q, dtype, (size_t)bh * qslice, Nq, D, Qh);
+        load_slice(K, dtype, (size_t)bh * kslice, Nkv, D, Kh);
+        load_slice(V, dtype, (size_t)bh * kslice, Nkv, D, Vh);
+#pragma omp parallel
+        {
+            double *x = (double *)malloc((size_t)Nkv * sizeof(double));
+            if (!x) {
+#pragma omp atomic write
+                failed = 1;
+            } else {
+#pragma omp for schedule(dynamic, 8)
+                for (long i = 0; i < Nq; ++i) {
+                    long nvis = Nkv;
+                    if (causal) {
+                        long last = i + Nkv - Nq;   /* the last key query i sees */
+                        nvis = last + 1 < Nkv ? last + 1 : Nkv;
+                    }
+                    ref_row_vis(Qh + i * D, Kh, Vh, nvis, D, s, x, O + (size_t)bh * qslice + (size_t)i * D,
+                                LSE + (size_t)bh * Nq + i);
+                }
             }
             free(x);
         }

@@ -19,9 +19,11 @@ from test_oracle_pins import PINS
 
 MUTANTS = {
     "drop_scale": ("        x[j] = s * dot;", "        x[j] = dot;"),
-    "ignore_causal": ("long nvis = causal ? i + 1 : N;     /* |J|", "long nvis = causal ? N : N;     /* |J|"),
-    "causal_off_by_one": ("long nvis = causal ? i + 1 : N;     /* |J|", "long nvis = causal ? i + (i == 0) : N;     /* |J|"),
-    "wrong_key_index": ("dot += q[d] * Kh[j * D + d];", "dot += q[d] * Kh[(N - 1 - j) * D + d];"),
+    "ignore_causal": ("ref_row_vis(q, Kh, Vh, causal ? i + 1 : N,", "ref_row_vis(q, Kh, Vh, causal ? N : N,"),
+    "causal_off_by_one": ("ref_row_vis(q, Kh, Vh, causal ? i + 1 : N,", "ref_row_vis(q, Kh, Vh, causal ? i + (i == 0) : N,"),
+    "wrong_key_index": ("dot += q[d] * Kh[j * D + d];", "dot += q[d] * Kh[(nvis - 1 - j) * D + d];"),
+    "qkv_top_left_causal": ("long last = i + Nkv - Nq;", "long last = i;"),
+    "qkv_empty_row_lse": ("        *lse = -INFINITY;\n        return;", "        *lse = 0.0;\n        return;"),
     "k_instead_of_v": ("o[d] += w * Vh[j * D + d];", "o[d] += w * Kh[j * D + d];"),
     "no_normalisation": ("        o[d] /= l;", "        o[d] /= 1.0;"),
     "lse_log2": ("*lse = m + log(l);", "*lse = m + log2(l);"),

@@ -213,9 +213,61 @@ def pin_first_step_rescale(lib):
         assert abs(L[0, 0] - 0.3125 * float(q[0, 0] @ k[0, 0])) < 1e-15
 
 
+def _masked_sdpa(q, k, v, causal, s):
+    """PyTorch fp64 reference for Nq queries against Nkv keys with an explicit
+    bottom-right causal mask; rows that see no key are defined as O = 0,
+    LSE = -inf (the empty sum)."""
+    Nq, Nkv = q.shape[-2], k.shape[-2]
+    S = s * (q @ k.transpose(-1, -2))
+    if causal:
+        i = torch.arange(Nq).unsqueeze(1)
+        j = torch.arange(Nkv).unsqueeze(0)
+        S = S.masked_fill(j > i + (Nkv - Nq), float("-inf"))
+    lse = torch.logsumexp(S, dim=-1)
+    empty = torch.isinf(lse) & (lse < 0)
+    P = torch.softmax(S.masked_fill(empty.unsqueeze(-1), 0.0), dim=-1)
+    O = (P @ v).masked_fill(empty.unsqueeze(-1), 0.0)
+    return O.numpy(), lse.numpy()
+
+
+def pin_qkv_vs_torch(lib):
+    """Nq queries against Nkv keys (cross attention, decode, Nq > Nkv with
+    empty rows) equal PyTorch's fp64 softmax under an explicit bottom-right
+    mask (an independent route), including O = 0, LSE = -inf for rows that
+    see no key."""
+    for causal in (False, True):
+        for (B, H, Nq, Nkv, D, s) in ((1, 2, 1, 200, 16, 0.25), (2, 1, 37, 130, 8, 0.5), (1, 3, 70, 20, 4, 1.0)):
+            q = torch.from_numpy(_rand((B, H, Nq, D), 31))
+            k = torch.from_numpy(_rand((B, H, Nkv, D), 32))
+            v = torch.from_numpy(_rand((B, H, Nkv, D), 33))
+            O, L = oracle.forward_qkv(q, k, v, causal, s, lib=lib)
+            O_ref, L_ref = _masked_sdpa(q, k, v, causal, s)
+            assert np.array_equal(np.isneginf(L), np.isneginf(L_ref))
+            fin = ~np.isneginf(L_ref)
+            assert np.allclose(L[fin], L_ref[fin], rtol=0, atol=1e-12)
+            assert np.allclose(O, O_ref, rtol=0, atol=1e-13)
+            if causal and Nq > Nkv:
+                assert np.isneginf(L[..., : Nq - Nkv]).all() and (O[..., : Nq - Nkv, :] == 0.0).all()
+
+
+def pin_qkv_is_the_suffix_of_square_causal(lib):
+    """Decoding the last Nq positions of a sequence of Nkv gives the last Nq
+    rows of the square causal attention over the whole sequence (the
+    bottom-right alignment), checked against the square oracle, itself pinned
+    to PyTorch above."""
+    Nkv, D, s = 67, 8, 0.375
+    q_all = _rand((2, Nkv, D), 41)
+    k, v = _rand((2, Nkv, D), 42), _rand((2, Nkv, D), 43)
+    O_sq, L_sq = oracle.forward(q_all, k, v, True, s, lib=lib)
+    for Nq in (1, 5, 64, 67):
+        O, L = oracle.forward_qkv(np.ascontiguousarray(q_all[:, Nkv - Nq:]), k, v, True, s, lib=lib)
+        assert np.allclose(O, O_sq[:, Nkv - Nq:], rtol=0, atol=1e-14)
+        assert np.allclose(L, L_sq[:, Nkv - Nq:], rtol=0, atol=1e-13)
+
+
 PINS = [pin_decode, pin_rows_sum_to_one, pin_probs_vs_scipy, pin_constant_v, pin_identical_keys,
         pin_zero_query, pin_causal_row0, pin_one_hot, pin_vs_torch_sdpa, pin_tiled_equals_explicit,
-        pin_unbalanced_magnitudes, pin_first_step_rescale]
+        pin_unbalanced_magnitudes, pin_first_step_rescale, pin_qkv_vs_torch, pin_qkv_is_the_suffix_of_square_causal]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
