@@ -201,10 +201,12 @@ bool take_status_word_whole(unsigned int *word)
 
 namespace {
 
-// fa_fwd_ex and fa_fwd_noalloc: identical but for where a balanced schedule's
-// workspace comes from (no_alloc: the library's static array).
-fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N, int D,
-                   int causal, float scale, fa_dtype dtype, fa_schedule schedule, fa_stream_t stream, bool no_alloc)
+// fa_fwd_ex, fa_fwd_qkv and fa_fwd_noalloc: N query rows against Nkv keys
+// per head (Nkv = N but for fa_fwd_qkv); no_alloc takes a balanced schedule's
+// workspace from the library's static array.
+fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N, int Nkv,
+                   int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule, fa_stream_t stream,
+                   bool no_alloc)
 {
     // Arguments first: nothing below touches the device until they are sound.
     if (dtype != FA_BF16 && dtype != FA_FP16)
@@ -213,12 +215,12 @@ fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *
         return FA_ERR_INVALID_VALUE;
     if (D != 64 && D != 128)
         return FA_ERR_INVALID_VALUE;
-    if (B < 1 || H < 1 || N < 1 || (causal != 0 && causal != 1))
+    if (B < 1 || H < 1 || N < 1 || Nkv < 1 || (causal != 0 && causal != 1))
         return FA_ERR_INVALID_VALUE;
     if (!std::isfinite(scale) || !(scale > 0.f))
         return FA_ERR_INVALID_VALUE;
     const long long BH = (long long)B * H;
-    if (BH * N >= (1ll << 31))
+    if (BH * N >= (1ll << 31) || BH * Nkv >= (1ll << 31))
         return FA_ERR_INVALID_VALUE;
     if (!Q || !K || !V || !O || !LSE)
         return FA_ERR_INVALID_VALUE;
@@ -227,11 +229,12 @@ fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *
                           reinterpret_cast<uintptr_t>(LSE);
     if (any & 15u)
         return FA_ERR_MISALIGNED;
-    const size_t tbytes = (size_t)BH * N * D * 2, lbytes = (size_t)BH * N * sizeof(float);
-    if (ranges_overlap(O, tbytes, Q, tbytes) || ranges_overlap(O, tbytes, K, tbytes) ||
-        ranges_overlap(O, tbytes, V, tbytes) || ranges_overlap(LSE, lbytes, Q, tbytes) ||
-        ranges_overlap(LSE, lbytes, K, tbytes) || ranges_overlap(LSE, lbytes, V, tbytes) ||
-        ranges_overlap(LSE, lbytes, O, tbytes))
+    const size_t qbytes = (size_t)BH * N * D * 2, kbytes = (size_t)BH * Nkv * D * 2,
+                 lbytes = (size_t)BH * N * sizeof(float);
+    if (ranges_overlap(O, qbytes, Q, qbytes) || ranges_overlap(O, qbytes, K, kbytes) ||
+        ranges_overlap(O, qbytes, V, kbytes) || ranges_overlap(LSE, lbytes, Q, qbytes) ||
+        ranges_overlap(LSE, lbytes, K, kbytes) || ranges_overlap(LSE, lbytes, V, kbytes) ||
+        ranges_overlap(LSE, lbytes, O, qbytes))
         return FA_ERR_INVALID_VALUE;
 
     int dev = -1;
@@ -248,16 +251,18 @@ fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *
 
     const bool bf16 = dtype == FA_BF16;
     alignas(64) CUtensorMap tq, tk, tv;
-    if (!encode_map(&tq, Q, (int)BH, N, D, bf16) || !encode_map(&tk, K, (int)BH, N, D, bf16) ||
-        !encode_map(&tv, V, (int)BH, N, D, bf16))
+    if (!encode_map(&tq, Q, (int)BH, N, D, bf16) || !encode_map(&tk, K, (int)BH, Nkv, D, bf16) ||
+        !encode_map(&tv, V, (int)BH, Nkv, D, bf16))
         return FA_ERR_CUDA;
 
     fa::FwdParams p{};
     p.O = O;
     p.LSE = LSE;
     p.N = N;
+    p.Nkv = Nkv;
+    p.off = causal ? Nkv - N : 0;
     p.qk_scale = scale * 1.4426950408889634f;   // scale * log2(e)
-    p.sch = fa::sched_plan(N, (int)BH, causal != 0, di->sms, (int)schedule);
+    p.sch = fa::sched_plan(N, Nkv, (int)BH, causal != 0, di->sms, (int)schedule);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (p.sch.split) {
         const fa_status ws =
@@ -276,14 +281,21 @@ extern "C" fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void
                                int N, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
                                fa_stream_t stream)
 {
-    return fwd_impl(Q, K, V, O, LSE, B, H, N, D, causal, scale, dtype, schedule, stream, false);
+    return fwd_impl(Q, K, V, O, LSE, B, H, N, N, D, causal, scale, dtype, schedule, stream, false);
+}
+
+extern "C" fa_status fa_fwd_qkv(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                                int Nq, int Nkv, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
+                                fa_stream_t stream)
+{
+    return fwd_impl(Q, K, V, O, LSE, B, H, Nq, Nkv, D, causal, scale, dtype, schedule, stream, false);
 }
 
 extern "C" fa_status fa_fwd_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                                     int N, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
                                     fa_stream_t stream)
 {
-    return fwd_impl(Q, K, V, O, LSE, B, H, N, D, causal, scale, dtype, schedule, stream, true);
+    return fwd_impl(Q, K, V, O, LSE, B, H, N, N, D, causal, scale, dtype, schedule, stream, true);
 }
 
 extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,

@@ -167,7 +167,9 @@ struct Cfg {
 struct FwdParams {
     void *O;
     float *LSE;
-    int N;
+    int N;               // query rows per head
+    int Nkv;             // keys per head
+    int off;             // causal: query i sees keys j <= i + off (Nkv - N, bottom-right alignment)
     float qk_scale;      // scale * log2(e)
     Schedule sch;        // work decomposition (fa_schedule.h)
     float *part_o;       // balanced schedule: partial O, [2 * grid slots][256 rows][D] fp32
@@ -581,7 +583,8 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
         if (np == 0)
             continue;
         const int row = ct * kCtaRows + w * kBM + t;                // query index (may be >= N: padding)
-        const int row_limit = CAUSAL ? min(p.N, row + 1) : p.N;     // keys < row_limit are visible
+        const int row_limit = CAUSAL ? min(p.Nkv, row + 1 + p.off) : p.Nkv;   // keys < row_limit are visible (may be <= 0)
+        const int first_row = ct * kCtaRows + w * kBM;                // the Q tile's first row sees keys <= first_row + off
         float m = -INFINITY, l = 0.f;                               // running max (log2 units), row sum
 
         for (int jr = 0; jr < np; ++jr) {
@@ -605,7 +608,9 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             for (int i = 0; i < 128; ++i)
                 s[i] = __uint_as_float(r[i / 64][i % 64]);
 
-            if ((CAUSAL && j == nw - 1) || (j + 1) * kBN > p.N) {
+            // Steps with keys past what the tile's first row sees (the diagonal,
+            // which crosses one or two steps), and the ragged last step.
+            if ((CAUSAL && (j + 1) * kBN > first_row + p.off + 1) || (j + 1) * kBN > p.Nkv) {
                 const int lim = row_limit - j * kBN;
 #pragma unroll
                 for (int i = 0; i < 128; ++i)
@@ -757,9 +762,9 @@ __device__ __forceinline__ float2 ld_cg_f2(const float2 *p)
 //   M = max_k m_k,  L = sum_k l_k 2^(m_k - M),  O = sum_k (l_k 2^(m_k - M) / L) O_k,
 //   LSE = (M + log2 L) ln 2
 // -- the same rescaling identity the recurrence uses between K/V tiles
-// ("A09 - Advanced Triton & FlashAttention", 3. Deep Dive).  Every row of a Q
-// tile sees at least one key in each of the tile's steps (the diagonal step
-// starts at the Q tile's first row), so each part's m_k is finite.
+// ("A09 - Advanced Triton & FlashAttention", 3. Deep Dive).  A row may see no
+// key in some part (m_k = -inf, l_k = 0: its weight is 0), or in none at all
+// (queries against fewer keys, causal): then M = -inf, O = 0 and LSE = -inf.
 //
 // One warp does all merges, off the path of the warps that read accumulators
 // out of TMEM: it takes jobs from the epilogue's queue, brings each part's
@@ -821,14 +826,15 @@ __device__ void merge_role(const FwdParams &p, uint32_t sbuf, uint32_t sml, cons
                 float M = -INFINITY;
                 for (int k = 0; k < nparts; ++k)
                     M = fmaxf(M, ptx::ld_shared_f32(sml + (k * kBM + r) * 8));
+                const float Mu = (M == -INFINITY) ? 0.f : M;   // no key seen at all: every weight is 0
                 float L = 0.f;
                 for (int k = 0; k < nparts; ++k) {
                     const uint32_t a = sml + (k * kBM + r) * 8;
-                    const float e = ptx::ld_shared_f32(a + 4) * ptx::ex2(ptx::ld_shared_f32(a) - M);
+                    const float e = ptx::ld_shared_f32(a + 4) * ptx::ex2(ptx::ld_shared_f32(a) - Mu);
                     ptx::st_shared_f32(a, e);
                     L += e;
                 }
-                const float inv_L = 1.f / L;
+                const float inv_L = (L > 0.f) ? 1.f / L : 0.f;
                 for (int k = 0; k < nparts; ++k) {
                     const uint32_t a = sml + (k * kBM + r) * 8;
                     ptx::st_shared_f32(a, ptx::ld_shared_f32(a) * inv_L);
@@ -980,7 +986,7 @@ __device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl 
                 return;
             ptx::tc_fence_after_sync();
             const bool whole = !SPLIT || (pt.kb == 0 && pt.ke >= nw);   // no other part holds steps of this Q tile
-            const float inv_l = 1.f / st.y;
+            const float inv_l = (st.y > 0.f) ? 1.f / st.y : 0.f;   // a row that saw no key: O = 0
             const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
             const int row = ct * kCtaRows + w * kBM + t;
             const bool valid = row < p.N;

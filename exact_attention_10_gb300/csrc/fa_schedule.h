@@ -42,17 +42,31 @@ constexpr long long kSchedMaxUnits = 0x3fffffffLL;   // units of a balanced sche
 constexpr int kSchedMaxParts = 8;                    // parts of one tile in a balanced schedule, at most
 
 struct Schedule {
-    int N;          // sequence length
+    int N;          // query rows per head
+    int Nkv;        // keys per head
+    int off;        // causal alignment: query i sees keys j <= i + off (off = Nkv - N, bottom-right)
     int BH;         // batch * heads
     int C;          // CTA tiles per head: ceil(N / 256)
     int T;          // CTA tiles: BH * C
-    int nkv;        // K/V steps of a full row: ceil(N / 128)
+    int nkv;        // K/V steps of a full row: ceil(Nkv / 128)
     int causal;     // 0 or 1
     int G;          // CTAs in the grid
     int split;      // 1: balanced schedule with partial tiles
     long long U;    // total units (the balanced schedule requires U <= kSchedMaxUnits)
     int range[kSchedMaxGrid + 1];   // balanced: range[c] = floor(U c / G), filled by sched_fill_ranges
 };
+
+// Causal steps of rows up to `last`: up to the step holding key last + off.
+// Rows that see no key at all (last + off < 0) still take one step, fully
+// masked, so that their O = 0 and LSE = -inf get written.
+FA_HD int sched_causal_steps(const Schedule &s, int last)
+{
+    const int vis = last + s.off;
+    if (vis < 0)
+        return 1;
+    const int n = vis / kSchedBN + 1;
+    return n < s.nkv ? n : s.nkv;
+}
 
 // K/V steps visited by Q tile w (0 or 1) of CTA tile ct; 0 if it holds no valid row.
 FA_HD int sched_kv_tiles(const Schedule &s, int ct, int w)
@@ -63,7 +77,7 @@ FA_HD int sched_kv_tiles(const Schedule &s, int ct, int w)
     if (!s.causal)
         return s.nkv;
     const int last = (r0 + kSchedBM - 1 < s.N - 1) ? r0 + kSchedBM - 1 : s.N - 1;
-    return last / kSchedBN + 1;
+    return sched_causal_steps(s, last);
 }
 
 // Steps of CTA tile ct: those of its last valid Q tile.
@@ -72,7 +86,7 @@ FA_HD int sched_steps_ct(const Schedule &s, int ct)
     if (!s.causal)
         return s.nkv;
     const int last = (ct * kSchedCtaRows + kSchedCtaRows - 1 < s.N - 1) ? ct * kSchedCtaRows + kSchedCtaRows - 1 : s.N - 1;
-    return last / kSchedBN + 1;
+    return sched_causal_steps(s, last);
 }
 
 FA_HD void sched_decode(const Schedule &s, int t, int &bh, int &ct)
@@ -383,14 +397,17 @@ FA_HD int sched_part_slots(const Schedule &s, int t, int nw, int *slots, int max
 constexpr int kSchedMinGain = 4;
 
 // mode: 0 = as above, 1 = round-robin, 2 = balanced wherever it can be built.
-inline Schedule sched_plan(int N, int BH, bool causal, int sms, int mode = 0)
+// N query rows against Nkv keys per head.
+inline Schedule sched_plan(int N, int Nkv, int BH, bool causal, int sms, int mode = 0)
 {
     Schedule s{};
     s.N = N;
+    s.Nkv = Nkv;
+    s.off = causal ? Nkv - N : 0;
     s.BH = BH;
     s.C = (N + kSchedCtaRows - 1) / kSchedCtaRows;
     s.T = BH * s.C;
-    s.nkv = (N + kSchedBN - 1) / kSchedBN;
+    s.nkv = (Nkv + kSchedBN - 1) / kSchedBN;
     s.causal = causal ? 1 : 0;
     s.split = 0;
     s.G = s.T < sms ? s.T : sms;

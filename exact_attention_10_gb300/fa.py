@@ -14,7 +14,7 @@ from .build import LIB_PATH
 FA_BF16, FA_FP16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_MISALIGNED", 3: "FA_ERR_UNSUPPORTED_DEVICE",
           4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT", 6: "FA_ERR_NO_ALLOC_LIMIT"}
-EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_noalloc", "fa_sync_status", "fa_status_string")
+EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_noalloc", "fa_fwd_qkv", "fa_sync_status", "fa_status_string")
 SCHEDULES = {"auto": 0, "whole_tiles": 1, "balanced": 2}
 
 _lib = None
@@ -41,6 +41,9 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd_ex.restype = c_int
     lib.fa_fwd_noalloc.argtypes = lib.fa_fwd_ex.argtypes
     lib.fa_fwd_noalloc.restype = c_int
+    lib.fa_fwd_qkv.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, ctypes.c_float, c_int,
+                               c_int, vp]
+    lib.fa_fwd_qkv.restype = c_int
     lib.fa_sync_status.argtypes = [vp]
     lib.fa_sync_status.restype = c_int
     lib.fa_status_string.argtypes = [c_int]
@@ -81,7 +84,9 @@ def _dtype_code(t) -> int:
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
             schedule: str = "auto"):
-    """Attention forward on CUDA tensors [B, H, N, D]; returns (O, LSE).
+    """Attention forward on CUDA tensors q [B, H, Nq, D], k and v [B, H, Nkv, D];
+    returns (O [B, H, Nq, D], LSE [B, H, Nq]).  With Nq != Nkv the causal mask
+    is aligned bottom-right (fa_fwd_qkv).
 
     ``out`` / ``lse`` may be given to write into existing buffers.
     ``schedule`` is "auto", "whole_tiles" or "balanced" (fa_schedule).
@@ -89,8 +94,8 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     (default: the current torch stream).
     """
     import torch
-    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
-        raise ValueError("q, k, v must share one [B, H, N, D] shape")
+    if q.dim() != 4 or k.shape != v.shape or k.dim() != 4 or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q must be [B, H, Nq, D] and k, v [B, H, Nkv, D]")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
     code = _dtype_code(q)
@@ -108,8 +113,13 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     st = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     if schedule not in SCHEDULES:
         raise ValueError(f"schedule must be one of {sorted(SCHEDULES)}")
-    rc = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D,
-                 int(bool(causal)), float(scale), code, st, SCHEDULES[schedule])
+    Nkv = k.shape[2]
+    if Nkv == N:
+        rc = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D,
+                     int(bool(causal)), float(scale), code, st, SCHEDULES[schedule])
+    else:
+        rc = load().fa_fwd_qkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, Nkv,
+                               D, int(bool(causal)), float(scale), code, SCHEDULES[schedule], st)
     if rc != 0:
         raise FAError(rc, "fa_fwd")
     return out, lse

@@ -139,6 +139,28 @@ FA_API fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void *O,
                     fa_dtype dtype, fa_schedule schedule, fa_stream_t stream);
 
 /*
+ * fa_fwd_qkv -- fa_fwd_ex for Nq queries against Nkv keys per head: cross
+ * attention, and decoding the last Nq positions of a longer sequence.
+ *
+ * Q, O : contiguous [B, H, Nq, D]; K, V : contiguous [B, H, Nkv, D];
+ * LSE  : contiguous [B, H, Nq] float32.  Nq, Nkv >= 1, B*H*Nq < 2^31 and
+ *        B*H*Nkv < 2^31; other arguments as for fa_fwd_ex.
+ * causal: query i sees keys j <= i + (Nkv - Nq) -- aligned bottom-right, so
+ *        the last query sees every key; with Nq = Nkv this is fa_fwd's mask.
+ *        A query that sees no key (possible when Nq > Nkv) gets O = 0 and
+ *        LSE = -inf.
+ *
+ * With few queries and many keys (decode) the balanced schedule splits each
+ * head's keys over many CTAs and merges the partial results by their
+ * log-sum-exp -- split-KV decoding; FA_SCHEDULE_AUTO picks it where it pays.
+ * The pages fix only the square case; the bottom-right alignment is this
+ * library's reading of the general one.
+ */
+FA_API fa_status fa_fwd_qkv(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                            int B, int H, int Nq, int Nkv, int D, int causal, float scale,
+                            fa_dtype dtype, fa_schedule schedule, fa_stream_t stream);
+
+/*
  * fa_fwd_noalloc -- fa_fwd_ex that allocates no memory, device or host, at
  * any call.  The pages describe nothing like it: the method itself needs no
  * scratch, and this entry point only concerns where this library's balanced

@@ -16,14 +16,16 @@ using namespace fa;
 
 static int check_schedule(const Schedule &s, bool planned);
 
-static int check(int N, int BH, int causal, int G, int split)
+static int check(int N, int Nkv, int BH, int causal, int G, int split)
 {
     Schedule s{};
     s.N = N;
+    s.Nkv = Nkv;
+    s.off = causal ? Nkv - N : 0;
     s.BH = BH;
     s.C = (N + 255) / 256;
     s.T = BH * s.C;
-    s.nkv = (N + 127) / 128;
+    s.nkv = (Nkv + 127) / 128;
     s.causal = causal;
     s.G = G;
     s.split = split;
@@ -36,9 +38,9 @@ static int check(int N, int BH, int causal, int G, int split)
 
 // The planner's schedule for `sms` SMs: valid, and a balanced one cuts no
 // tile into more parts than the merge handles.
-static int check_plan(int N, int BH, int causal, int sms)
+static int check_plan(int N, int Nkv, int BH, int causal, int sms)
 {
-    const Schedule s = sched_plan(N, BH, causal != 0, sms);
+    const Schedule s = sched_plan(N, Nkv, BH, causal != 0, sms);
     if (s.G < 1 || (!s.split && s.G != (s.T < sms ? s.T : sms))) {
         std::printf("bad grid %d\n", s.G);
         return 1;
@@ -150,16 +152,17 @@ static int check_schedule(const Schedule &s, bool planned)
 
 int main(int argc, char **argv)
 {
-    // "N BH causal G split" cases, repeated; or "plan" then "N BH causal sms" cases
+    // "N Nkv BH causal G split" cases, repeated; or "plan" then "N Nkv BH causal sms" cases
     int failures = 0, cases = 0;
     const bool plan = argc > 1 && std::string(argv[1]) == "plan";
-    const int width = plan ? 4 : 5;
+    const int width = plan ? 5 : 6;
     for (int i = plan ? 2 : 1; i + width <= argc; i += width) {
-        const int N = std::atoi(argv[i]), BH = std::atoi(argv[i + 1]), causal = std::atoi(argv[i + 2]);
-        const int G = std::atoi(argv[i + 3]), split = plan ? 0 : std::atoi(argv[i + 4]);
+        const int N = std::atoi(argv[i]), Nkv = std::atoi(argv[i + 1]), BH = std::atoi(argv[i + 2]);
+        const int causal = std::atoi(argv[i + 3]), G = std::atoi(argv[i + 4]), split = plan ? 0 : std::atoi(argv[i + 5]);
         ++cases;
-        if (plan ? check_plan(N, BH, causal, G) : check(N, BH, causal, G, split)) {
-            std::printf("FAILED N=%d BH=%d causal=%d G/sms=%d split=%d plan=%d\n", N, BH, causal, G, split, (int)plan);
+        if (plan ? check_plan(N, Nkv, BH, causal, G) : check(N, Nkv, BH, causal, G, split)) {
+            std::printf("FAILED N=%d Nkv=%d BH=%d causal=%d G/sms=%d split=%d plan=%d\n", N, Nkv, BH, causal, G, split,
+                        (int)plan);
             ++failures;
         }
     }

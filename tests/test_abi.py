@@ -117,3 +117,14 @@ def test_no_oracle_on_the_product_path():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "attn_ref" not in text, f
+
+
+def test_qkv_invalid_arguments_rejected(lib):
+    """fa_fwd_qkv validates Nq and Nkv before touching any device."""
+    import ctypes
+    a = GOOD
+    for nq, nkv in ((0, 16), (16, 0), (-1, 16), (1, 1 << 31 - 1)):
+        rc = lib.fa_fwd_qkv(a["q"], a["k"], a["v"], a["o"], a["lse"], 1, 2, nq, nkv, 64, 0, ctypes.c_float(0.125), 0,
+                            0, None)
+        assert rc == INVALID, (nq, nkv, rc)
+

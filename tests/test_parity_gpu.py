@@ -273,3 +273,64 @@ def test_rejects_host_memory():
     rc = fa.fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 256, 64, 0,
                     0.125, 0, 0)
     assert rc == 1   # FA_ERR_INVALID_VALUE
+
+
+# --- queries against a different number of keys (fa_fwd_qkv) ----------------
+
+RECT = [  # (B, H, Nq, Nkv, D, dtype)
+    (1, 8, 1, 4096, 64, "bf16"),        # decode: one query, long K/V
+    (2, 4, 16, 2000, 128, "fp16"),
+    (1, 4, 127, 1000, 64, "bf16"),
+    (2, 2, 200, 70, 128, "bf16"),       # more queries than keys
+    (1, 3, 513, 200, 64, "fp16"),       # causal: the first 313 rows see no key
+    (1, 2, 300, 1, 64, "bf16"),
+    (1, 2, 1000, 129, 128, "bf16"),
+]
+
+
+def _rect(B, H, Nq, Nkv, D, dtype, seed):
+    q = make_custom(B, H, Nq, D, dtype, seed=seed)[0]
+    _, k, v = make_custom(B, H, Nkv, D, dtype, seed=seed + 1)
+    return q, k, v
+
+
+@pytest.mark.parametrize("schedule", ["auto", "balanced"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,Nq,Nkv,D,dtype", RECT)
+def test_queries_against_other_key_counts(B, H, Nq, Nkv, D, dtype, causal, schedule):
+    q, k, v = _rect(B, H, Nq, Nkv, D, dtype, seed=Nq + Nkv)
+    scale = D ** -0.5
+    dev = torch.device("cuda:0")
+    o, lse = fa.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale, schedule=schedule)
+    assert fa.sync_status(torch.cuda.current_stream(dev).cuda_stream) == 0
+    o_ref, lse_ref = oracle.forward_qkv(q, k, v, causal, scale)
+    od = o.cpu().double().numpy()
+    ld = lse.cpu().double().numpy()
+    empty = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(ld), empty)
+    assert (od[empty] == 0.0).all()   # rows that see no key: O = 0 exactly
+    emax = float(np.abs(od - o_ref).max())
+    lmax = float(np.abs(ld[~empty] - lse_ref[~empty]).max()) if (~empty).any() else 0.0
+    print(f"Nq={Nq} Nkv={Nkv} D={D} {dtype} causal={int(causal)} {schedule}: max|dO|={emax:.3e} "
+          f"max|dLSE|={lmax:.3e} empty rows={int(empty.sum())}")
+    assert emax <= TOL_O[dtype] and lmax <= TOL_LSE
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_split_kv_decode_long_context(causal):
+    """Decoding 4 queries against 32768 keys over 32 heads: 32 CTA tiles of
+    256 steps, which the balanced schedule cuts into parts across the SMs and
+    merges by LSE (split-KV); compared in full with the oracle."""
+    q, k, v = _rect(1, 32, 4, 32768, 128, "bf16", seed=9)
+    dev = torch.device("cuda:0")
+    outs = {}
+    for schedule in ("whole_tiles", "balanced"):
+        outs[schedule] = fa.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=128 ** -0.5,
+                                    schedule=schedule)
+    assert fa.sync_status(torch.cuda.current_stream(dev).cuda_stream) == 0
+    o_ref, lse_ref = oracle.forward_qkv(q, k, v, causal, 128 ** -0.5)
+    for schedule, (o, lse) in outs.items():
+        emax = float(np.abs(o.cpu().double().numpy() - o_ref).max())
+        lmax = float(np.abs(lse.cpu().double().numpy() - lse_ref).max())
+        print(f"decode {schedule} causal={int(causal)}: max|dO|={emax:.3e} max|dLSE|={lmax:.3e}")
+        assert emax <= TOL_O["bf16"] and lmax <= TOL_LSE

@@ -20,7 +20,15 @@ for N in (1, 2, 127, 128, 129, 255, 256, 257, 383, 513, 1024, 3000, 4096, 16384,
                 for split in (0, 1):
                     if N * BH > 64 * 4096 and G != 152:
                         continue
-                    CASES.append((N, BH, causal, G, split))
+                    CASES.append((N, N, BH, causal, G, split))
+# queries against a different number of keys: decode, cross attention, and
+# Nq > Nkv (causal rows that see no key)
+for N, Nkv in ((1, 4096), (16, 8192), (64, 3000), (127, 1000), (200, 70), (513, 200), (300, 1), (1000, 129)):
+    for BH in (1, 5, 32):
+        for causal in (0, 1):
+            for G in (1, 7, 152):
+                for split in (0, 1):
+                    CASES.append((N, Nkv, BH, causal, G, split))
 
 
 @pytest.fixture(scope="module")
@@ -39,7 +47,11 @@ for N in (1, 2, 100, 256, 257, 513, 1000, 1024, 2048, 3000, 4096, 8192, 16384, 3
             for sms in (148, 152):
                 if N * BH > 64 * 16384:
                     continue
-                PLAN_CASES.append((N, BH, causal, sms))
+                PLAN_CASES.append((N, N, BH, causal, sms))
+for N, Nkv in ((1, 32768), (4, 131072), (64, 16384), (128, 4096), (513, 200), (4096, 64)):
+    for BH in (1, 8, 32, 128):
+        for causal in (0, 1):
+            PLAN_CASES.append((N, Nkv, BH, causal, 152))
 
 
 def test_schedule_planner(checker):
