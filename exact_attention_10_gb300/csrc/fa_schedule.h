@@ -389,11 +389,13 @@ FA_HD int sched_part_slots(const Schedule &s, int t, int nw, int *slots, int max
 // the machine idle in its last wave for more than ~4% of the run and for at
 // least kSchedMinGain steps (a split tile costs its parts a partial write and
 // one of them a merge); its grid is kept small enough that no tile is cut
-// into more than kSchedMaxParts parts.  The merge runs on the warps that
-// read accumulators out of TMEM, so it must not hold up the next part's
-// read-out: the balanced schedule is taken only where every CTA's range has
-// a whole tile after its partial parts (ranges of at least two tiles), and
-// for causal attention, whose short tiles leave no such room, not at all.
+// into more than kSchedMaxParts parts.  Parts have fixed costs (a partial
+// write, a merge, a pipeline start), so with many tiles the balanced schedule
+// is taken only where every CTA's range spans at least two tiles, and not
+// for causal attention, whose short tiles lose to those costs (measured).
+// With few long tiles -- decoding a few queries against many keys -- whole
+// tiles would leave most SMs idle, and the balanced schedule (split-KV) is
+// taken whenever it at least halves the makespan.
 constexpr int kSchedMinGain = 4;
 
 // mode: 0 = as above, 1 = round-robin, 2 = balanced wherever it can be built.
@@ -431,7 +433,10 @@ inline Schedule sched_plan(int N, int Nkv, int BH, bool causal, int sms, int mod
     if (G < 1)
         return s;
     const long long balanced = (s.U + G - 1) / G;
-    const bool pays = !causal && balanced >= 2LL * max_steps && rr * 100 > balanced * 104 && rr - balanced >= kSchedMinGain;
+    const bool many_tiles = !causal && balanced >= 2LL * max_steps && rr * 100 > balanced * 104 &&
+                            rr - balanced >= kSchedMinGain;
+    const bool few_long_tiles = 2LL * s.T <= sms && max_steps >= 32 && rr >= 2 * balanced;
+    const bool pays = many_tiles || few_long_tiles;
     if (mode == 2 || pays) {
         s.split = 1;
         s.G = (int)G;
