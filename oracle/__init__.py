@@ -50,6 +50,9 @@ def _load(path: str | None = None):
                                                                 ctypes.c_long, ctypes.c_long, ctypes.c_int,
                                                                 ctypes.c_double, c_double_p, c_double_p]
     lib.attn_ref_forward_qkv.restype = ctypes.c_int
+    lib.attn_ref_forward_band.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] + [ctypes.c_long] * 6 + [
+        ctypes.c_double, c_double_p, c_double_p]
+    lib.attn_ref_forward_band.restype = ctypes.c_int
     lib.attn_ref_rows.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_long, ctypes.c_long,
                                                          ctypes.c_long, ctypes.c_int, ctypes.c_double,
                                                          c_long_p, c_long_p, ctypes.c_long, c_double_p, c_double_p]
@@ -154,6 +157,30 @@ def forward_qkv(q, k, v, causal: bool, scale: float, lib=None):
     rc = (lib or _load()).attn_ref_forward_qkv(_ptr(qa), _ptr(ka), _ptr(va), _DTYPE_CODE[dt], BH, Nq, Nkv, D,
                                                int(bool(causal)), _scale_as_double(scale),
                                                _ptr(O, ctypes.c_double), _ptr(L, ctypes.c_double))
+    if rc != 0:
+        raise MemoryError("oracle forward failed to allocate scratch")
+    return O, L
+
+
+def forward_band(q, k, v, left: int, right: int, scale: float, lib=None):
+    """Exact attention of [..., Nq, D] queries against [..., Nkv, D] keys under
+    a band mask: query i sees keys j in [i' - left, i' + right], i' = i + Nkv
+    - Nq; a negative bound is unbounded.  A row whose band holds no key gets
+    O = 0, LSE = -inf.  Returns (O float64 [..., Nq, D], LSE float64 [..., Nq])."""
+    qa, dt = _as_input(q)
+    ka, dtk = _as_input(k)
+    va, dtv = _as_input(v)
+    if not (dt == dtk == dtv):
+        raise TypeError("q, k, v must share a dtype")
+    if ka.shape != va.shape or qa.ndim < 2 or qa.shape[:-2] != ka.shape[:-2] or qa.shape[-1] != ka.shape[-1]:
+        raise ValueError("q [..., Nq, D] and k, v [..., Nkv, D] must agree")
+    Nq, Nkv, D = qa.shape[-2], ka.shape[-2], qa.shape[-1]
+    BH = int(np.prod(qa.shape[:-2])) if qa.ndim > 2 else 1
+    O = np.empty(qa.shape, dtype=np.float64)
+    L = np.empty(qa.shape[:-1], dtype=np.float64)
+    rc = (lib or _load()).attn_ref_forward_band(_ptr(qa), _ptr(ka), _ptr(va), _DTYPE_CODE[dt], BH, Nq, Nkv, D,
+                                                int(left), int(right), _scale_as_double(scale),
+                                                _ptr(O, ctypes.c_double), _ptr(L, ctypes.c_double))
     if rc != 0:
         raise MemoryError("oracle forward failed to allocate scratch")
     return O, L

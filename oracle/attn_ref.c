@@ -40,6 +40,12 @@
  * alignment).  A query that sees no key (possible when Nq > Nkv) gets O = 0
  * and LSE = -inf, the empty sum's value.
  *
+ * attn_ref_forward_band() generalises the mask to a band (sliding window):
+ * with i' = i + (Nkv - Nq), query i sees keys j in [i' - left, i' + right]
+ * (a negative bound means unbounded on that side), so causal is the band
+ * (unbounded, 0) and no mask is (unbounded, unbounded); a row whose band holds
+ * no key gets O = 0 and LSE = -inf.
+ *
  * Besides the explicit definition, attn_ref_tiled() runs the tiled online-
  * softmax recurrence in fp64, step by step in the order the pages give it, so
  * the tests can show that the recurrence equals the definition on small
@@ -239,6 +245,56 @@ int attn_ref_forward_qkv(const void *Q, const void *K, const void *V, int dtype,
                     }
                     ref_row_vis(Qh + i * D, Kh, Vh, nvis, D, s, x, O + (size_t)bh * qslice + (size_t)i * D,
                                 LSE + (size_t)bh * Nq + i);
+                }
+            }
+            free(x);
+        }
+    }
+    free(Kh); free(Vh); free(Qh);
+    return failed ? -1 : 0;
+}
+
+/*
+ * Band-masked forward: Q and O are [BH, Nq, D], K and V are [BH, Nkv, D],
+ * LSE is [BH, Nq]; query i sees keys j with i' - left <= j <= i' + right,
+ * i' = i + Nkv - Nq (left or right < 0: unbounded).  Returns 0, or -1 if a
+ * scratch allocation failed.
+ */
+int attn_ref_forward_band(const void *Q, const void *K, const void *V, int dtype,
+                          long BH, long Nq, long Nkv, long D, long left, long right, double s,
+                          double *O, double *LSE)
+{
+    size_t qslice = (size_t)Nq * (size_t)D, kslice = (size_t)Nkv * (size_t)D;
+    double *Kh = (double *)malloc(kslice * sizeof(double));
+    double *Vh = (double *)malloc(kslice * sizeof(double));
+    double *Qh = (double *)malloc(qslice * sizeof(double));
+    if (!Kh || !Vh || !Qh) {
+        free(Kh); free(Vh); free(Qh);
+        return -1;
+    }
+    int failed = 0;
+    for (long bh = 0; bh < BH; ++bh) {
+        load_slice(Q, dtype, (size_t)bh * qslice, Nq, D, Qh);
+        load_slice(K, dtype, (size_t)bh * kslice, Nkv, D, Kh);
+        load_slice(V, dtype, (size_t)bh * kslice, Nkv, D, Vh);
+#pragma omp parallel
+        {
+            double *x = (double *)malloc((size_t)Nkv * sizeof(double));
+            if (!x) {
+#pragma omp atomic write
+                failed = 1;
+            } else {
+#pragma omp for schedule(dynamic, 8)
+                for (long i = 0; i < Nq; ++i) {
+                    const long ii = i + Nkv - Nq;                        /* the query's position among the keys */
+                    long lo = left < 0 ? 0 : ii - left, hi = right < 0 ? Nkv - 1 : ii + right;
+                    if (lo < 0)
+                        lo = 0;
+                    if (hi > Nkv - 1)
+                        hi = Nkv - 1;
+                    const long nvis = hi >= lo ? hi - lo + 1 : 0;        /* keys lo .. hi */
+                    ref_row_vis(Qh + i * D, Kh + (nvis > 0 ? lo : 0) * D, Vh + (nvis > 0 ? lo : 0) * D, nvis, D, s,
+                                x, O + (size_t)bh * qslice + (size_t)i * D, LSE + (size_t)bh * Nq + i);
                 }
             }
             free(x);

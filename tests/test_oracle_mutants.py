@@ -23,6 +23,8 @@ MUTANTS = {
     "causal_off_by_one": ("ref_row_vis(q, Kh, Vh, causal ? i + 1 : N,", "ref_row_vis(q, Kh, Vh, causal ? i + (i == 0) : N,"),
     "wrong_key_index": ("dot += q[d] * Kh[j * D + d];", "dot += q[d] * Kh[(nvis - 1 - j) * D + d];"),
     "qkv_top_left_causal": ("long last = i + Nkv - Nq;", "long last = i;"),
+    "band_left_off_by_one": ("long lo = left < 0 ? 0 : ii - left,", "long lo = left < 0 ? 0 : ii - left + 1,"),
+    "band_ignores_right": ("hi = right < 0 ? Nkv - 1 : ii + right;", "hi = Nkv - 1;"),
     "qkv_empty_row_lse": ("        *lse = -INFINITY;\n        return;", "        *lse = 0.0;\n        return;"),
     "k_instead_of_v": ("o[d] += w * Vh[j * D + d];", "o[d] += w * Kh[j * D + d];"),
     "no_normalisation": ("        o[d] /= l;", "        o[d] /= 1.0;"),

@@ -265,9 +265,61 @@ def pin_qkv_is_the_suffix_of_square_causal(lib):
         assert np.allclose(L, L_sq[:, Nkv - Nq:], rtol=0, atol=1e-13)
 
 
+def _band_sdpa(q, k, v, left, right, s):
+    """PyTorch fp64 reference under an explicit band mask (empty rows O = 0, LSE = -inf)."""
+    Nq, Nkv = q.shape[-2], k.shape[-2]
+    S = s * (q @ k.transpose(-1, -2))
+    ii = torch.arange(Nq).unsqueeze(1) + (Nkv - Nq)
+    j = torch.arange(Nkv).unsqueeze(0)
+    hide = torch.zeros(Nq, Nkv, dtype=torch.bool)
+    if left >= 0:
+        hide |= j < ii - left
+    if right >= 0:
+        hide |= j > ii + right
+    S = S.masked_fill(hide, float("-inf"))
+    lse = torch.logsumexp(S, dim=-1)
+    empty = torch.isinf(lse) & (lse < 0)
+    P = torch.softmax(S.masked_fill(empty.unsqueeze(-1), 0.0), dim=-1)
+    O = (P @ v).masked_fill(empty.unsqueeze(-1), 0.0)
+    return O.numpy(), lse.numpy()
+
+
+def pin_band_vs_torch(lib):
+    """Band (sliding-window) masks -- causal windows, two-sided windows, windows
+    wider than the sequence, Nq != Nkv -- equal PyTorch's fp64 softmax under an
+    explicit mask (an independent route), including empty rows."""
+    for (Nq, Nkv, left, right) in ((37, 37, 5, 0), (40, 70, 9, 3), (70, 40, 0, 0), (33, 33, -1, -1), (33, 33, -1, 0),
+                                   (50, 20, 2, 0), (16, 300, 100, -1)):
+        q = torch.from_numpy(_rand((2, Nq, 8), 51))
+        k = torch.from_numpy(_rand((2, Nkv, 8), 52))
+        v = torch.from_numpy(_rand((2, Nkv, 8), 53))
+        O, L = oracle.forward_band(q, k, v, left, right, 0.5, lib=lib)
+        O_ref, L_ref = _band_sdpa(q, k, v, left, right, 0.5)
+        assert np.array_equal(np.isneginf(L), np.isneginf(L_ref)), (Nq, Nkv, left, right)
+        fin = ~np.isneginf(L_ref)
+        assert np.allclose(L[fin], L_ref[fin], rtol=0, atol=1e-12)
+        assert np.allclose(O, O_ref, rtol=0, atol=1e-13)
+
+
+def pin_band_closed_forms(lib):
+    """A band of width one (left = right = 0) gives O = V[i'] and LSE = the one
+    score; an unbounded band equals the oracle's full attention; (unbounded, 0)
+    equals its causal attention."""
+    Nq = Nkv = 29
+    q, k, v = _rand((3, Nq, 4), 61), _rand((3, Nkv, 4), 62), _rand((3, Nkv, 4), 63)
+    O, L = oracle.forward_band(q, k, v, 0, 0, 0.25, lib=lib)
+    assert np.allclose(O, v, rtol=0, atol=1e-15)
+    assert np.allclose(L, 0.25 * np.einsum("bid,bid->bi", q, k), rtol=0, atol=1e-13)
+    for causal, (left, right) in ((False, (-1, -1)), (True, (-1, 0))):
+        O1, L1 = oracle.forward_band(q, k, v, left, right, 0.25, lib=lib)
+        O2, L2 = oracle.forward(q, k, v, causal, 0.25, lib=lib)
+        assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
 PINS = [pin_decode, pin_rows_sum_to_one, pin_probs_vs_scipy, pin_constant_v, pin_identical_keys,
         pin_zero_query, pin_causal_row0, pin_one_hot, pin_vs_torch_sdpa, pin_tiled_equals_explicit,
-        pin_unbalanced_magnitudes, pin_first_step_rescale, pin_qkv_vs_torch, pin_qkv_is_the_suffix_of_square_causal]
+        pin_unbalanced_magnitudes, pin_first_step_rescale, pin_qkv_vs_torch, pin_qkv_is_the_suffix_of_square_causal,
+        pin_band_vs_torch, pin_band_closed_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
