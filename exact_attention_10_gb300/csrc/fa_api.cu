@@ -189,7 +189,8 @@ namespace fa_launch {
 fa_status launch_whole(int D, bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k,
                        const CUtensorMap &v, const fa::FwdParams &p, int grid, cudaStream_t s, int dev)
 {
-    return launch_any<false>(D, bf16, causal, q, k, v, p, grid, s, dev);
+    return causal ? launch_mask<fa::kMaskCausal, false>(D, bf16, q, k, v, p, grid, s, dev)
+                  : launch_mask<fa::kMaskNone, false>(D, bf16, q, k, v, p, grid, s, dev);
 }
 
 bool take_status_word_whole(unsigned int *word)
@@ -201,13 +202,20 @@ bool take_status_word_whole(unsigned int *word)
 
 namespace {
 
-// fa_fwd_ex, fa_fwd_qkv and fa_fwd_noalloc: N query rows against Nkv keys
-// per head (Nkv = N but for fa_fwd_qkv); no_alloc takes a balanced schedule's
-// workspace from the library's static array.
+// Every entry point: N query rows against Nkv keys per head (Nkv = N but for
+// fa_fwd_qkv / fa_fwd_band), masked by the band [i' - left, i' + right] with
+// i' = i + Nkv - N (a negative bound: unbounded; causal = (-1, 0), no mask =
+// (-1, -1)); no_alloc takes a balanced schedule's workspace from the
+// library's static array.
 fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N, int Nkv,
-                   int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule, fa_stream_t stream,
+                   int D, int left, int right, float scale, fa_dtype dtype, fa_schedule schedule, fa_stream_t stream,
                    bool no_alloc)
 {
+    int wl = left, wr = right;   // bounds that cannot bind are dropped: a band of no bounds runs unmasked
+    if (N >= 1 && Nkv >= 1)
+        fa::sched_band_normalize(N, Nkv, wl, wr);
+    const int causal = (wl < fa::kSchedUnbounded || wr < fa::kSchedUnbounded) ? 1 : 0;   // masked at all
+    const bool band = wl < fa::kSchedUnbounded;   // bounded on the left: the kMaskBand kernels
     // Arguments first: nothing below touches the device until they are sound.
     if (dtype != FA_BF16 && dtype != FA_FP16)
         return FA_ERR_INVALID_VALUE;
@@ -215,7 +223,7 @@ fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *
         return FA_ERR_INVALID_VALUE;
     if (D != 64 && D != 128)
         return FA_ERR_INVALID_VALUE;
-    if (B < 1 || H < 1 || N < 1 || Nkv < 1 || (causal != 0 && causal != 1))
+    if (B < 1 || H < 1 || N < 1 || Nkv < 1)
         return FA_ERR_INVALID_VALUE;
     if (!std::isfinite(scale) || !(scale > 0.f))
         return FA_ERR_INVALID_VALUE;
@@ -262,7 +270,7 @@ fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *
     p.Nkv = Nkv;
     p.off = causal ? Nkv - N : 0;
     p.qk_scale = scale * 1.4426950408889634f;   // scale * log2(e)
-    p.sch = fa::sched_plan(N, Nkv, (int)BH, causal != 0, di->sms, (int)schedule);
+    p.sch = fa::sched_plan(N, Nkv, (int)BH, causal != 0, di->sms, (int)schedule, wl, wr);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (p.sch.split) {
         const fa_status ws =
@@ -271,8 +279,10 @@ fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *
             return ws;
     }
     if (p.sch.split)
-        return fa_launch::launch_split(D, bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
-    return fa_launch::launch_whole(D, bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
+        return band ? fa_launch::launch_band(D, bf16, true, tq, tk, tv, p, p.sch.G, s, dev)
+                    : fa_launch::launch_split(D, bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
+    return band ? fa_launch::launch_band(D, bf16, false, tq, tk, tv, p, p.sch.G, s, dev)
+                : fa_launch::launch_whole(D, bf16, causal != 0, tq, tk, tv, p, p.sch.G, s, dev);
 }
 
 }  // namespace
@@ -281,21 +291,35 @@ extern "C" fa_status fa_fwd_ex(const void *Q, const void *K, const void *V, void
                                int N, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
                                fa_stream_t stream)
 {
-    return fwd_impl(Q, K, V, O, LSE, B, H, N, N, D, causal, scale, dtype, schedule, stream, false);
+    if (causal != 0 && causal != 1)
+        return FA_ERR_INVALID_VALUE;
+    return fwd_impl(Q, K, V, O, LSE, B, H, N, N, D, -1, causal ? 0 : -1, scale, dtype, schedule, stream, false);
 }
 
 extern "C" fa_status fa_fwd_qkv(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                                 int Nq, int Nkv, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
                                 fa_stream_t stream)
 {
-    return fwd_impl(Q, K, V, O, LSE, B, H, Nq, Nkv, D, causal, scale, dtype, schedule, stream, false);
+    if (causal != 0 && causal != 1)
+        return FA_ERR_INVALID_VALUE;
+    return fwd_impl(Q, K, V, O, LSE, B, H, Nq, Nkv, D, -1, causal ? 0 : -1, scale, dtype, schedule, stream, false);
+}
+
+extern "C" fa_status fa_fwd_band(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                                 int Nq, int Nkv, int D, int window_left, int window_right, float scale, fa_dtype dtype,
+                                 fa_schedule schedule, fa_stream_t stream)
+{
+    return fwd_impl(Q, K, V, O, LSE, B, H, Nq, Nkv, D, window_left, window_right, scale, dtype, schedule, stream,
+                    false);
 }
 
 extern "C" fa_status fa_fwd_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                                     int N, int D, int causal, float scale, fa_dtype dtype, fa_schedule schedule,
                                     fa_stream_t stream)
 {
-    return fwd_impl(Q, K, V, O, LSE, B, H, N, N, D, causal, scale, dtype, schedule, stream, true);
+    if (causal != 0 && causal != 1)
+        return FA_ERR_INVALID_VALUE;
+    return fwd_impl(Q, K, V, O, LSE, B, H, N, N, D, -1, causal ? 0 : -1, scale, dtype, schedule, stream, true);
 }
 
 extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
@@ -310,10 +334,11 @@ extern "C" fa_status fa_sync_status(fa_stream_t stream)
         cudaGetLastError();
         return FA_ERR_CUDA;
     }
-    unsigned int w_whole = 0, w_split = 0;
-    if (!fa_launch::take_status_word_whole(&w_whole) || !fa_launch::take_status_word_split(&w_split))
+    unsigned int w_whole = 0, w_split = 0, w_band = 0;
+    if (!fa_launch::take_status_word_whole(&w_whole) || !fa_launch::take_status_word_split(&w_split) ||
+        !fa_launch::take_status_word_band(&w_band))
         return FA_ERR_CUDA;
-    if ((w_whole | w_split) != 0) {
+    if ((w_whole | w_split | w_band) != 0) {
         // an aborted launch may have left split-tile counters non-zero
         int dev = -1;
         cudaGetDevice(&dev);

@@ -86,6 +86,14 @@ constexpr int kBN = 128;        // keys per K/V tile
 constexpr int kQTiles = 2;      // Q tiles per CTA tile
 constexpr int kCtaRows = kBM * kQTiles;
 constexpr int kThreads = 512;
+// Masks, a template parameter of the kernel: none; keys up to a bound after
+// the query (causal, or any band unbounded on the left: K/V steps start at 0
+// and one compare per score masks); a band with a left bound (K/V steps start
+// where the tile's band does, two-sided masking).  Separate variants keep the
+// causal hot loop free of the band's extra compares.
+constexpr int kMaskNone = 0;
+constexpr int kMaskCausal = 1;
+constexpr int kMaskBand = 2;
 constexpr int kEpilogueWarpgroup = 2;
 constexpr int kLoadWarp = 12;
 constexpr int kMmaWarp = 13;          // MMA issuer(s): warp 13 (and 14 at D = 64)
@@ -271,7 +279,7 @@ struct Bars {
 // TMA producer, run by a whole warp; one elected lane issues the copies.
 // Per CTA tile: both Q tiles into the Q buffer, then for each step j the
 // pair K_j, V_j into the next stage of the ring.
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, int MASK, bool SPLIT>
 __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
                           const FwdParams &p, uint32_t sQ, uint32_t sStage, Bars<D> b, Ctl c)
 {
@@ -282,9 +290,9 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
     PartIter parts;
     parts.init_t<SPLIT>(p.sch, blockIdx.x);
     Part pt;
-    while (ok && parts.next_t<SPLIT>(p.sch, pt)) {
+    while (ok && parts.next_t<SPLIT, MASK == kMaskBand>(p.sch, pt)) {
         int bh, ct;
-        sched_decode_t<SPLIT>(p.sch, pt.tile, bh, ct);
+        sched_decode_t<SPLIT, MASK == kMaskBand>(p.sch, pt.tile, bh, ct);
         const int qb = it % C::kQBufs;
         const uint32_t quse = (uint32_t)(it / C::kQBufs);
         if (!warp_wait(b.q_empty(qb), (quse & 1u) ^ 1u, c, kSiteLoadQEmpty)) { ok = false; break; }
@@ -298,6 +306,7 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
         }
         __syncwarp();
         ++it;
+        const int ks = (MASK == kMaskBand) ? sched_kv_start(p.sch, ct) : 0;   // the tile's first key step
         for (int j = pt.kb; j < pt.ke; ++j, ++step) {
             const int st = step % C::kStages;
             const uint32_t use = (uint32_t)(step / C::kStages);
@@ -306,9 +315,10 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
                 const uint32_t dst = sStage + st * C::kStageBytes;
                 ptx::mbar_arrive_expect_tx(b.full(st), C::kStageBytes);
                 for (int x = 0; x < C::kBoxes; ++x)
-                    ptx::tma_load_3d(dst + x * C::kBoxBytes, tmK, b.full(st), x * 64, j * kBN, bh);
+                    ptx::tma_load_3d(dst + x * C::kBoxBytes, tmK, b.full(st), x * 64, (ks + j) * kBN, bh);
                 for (int x = 0; x < C::kBoxes; ++x)
-                    ptx::tma_load_3d(dst + C::kTileBytes + x * C::kBoxBytes, tmV, b.full(st), x * 64, j * kBN, bh);
+                    ptx::tma_load_3d(dst + C::kTileBytes + x * C::kBoxBytes, tmV, b.full(st), x * 64, (ks + j) * kBN,
+                                     bh);
             }
             __syncwarp();
         }
@@ -508,7 +518,7 @@ __device__ bool tile_interleaved(MmaIssuer<D, BF16> &m0, MmaIssuer<D, BF16> &m1,
     return true;
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, int MASK, bool SPLIT>
 __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage, uint32_t tmem, Bars<D> b, Ctl c)
 {
     using C = Cfg<D>;
@@ -530,10 +540,10 @@ __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage
     PartIter parts;
     parts.init_t<SPLIT>(p.sch, blockIdx.x);
     Part pt;
-    while (parts.next_t<SPLIT>(p.sch, pt)) {
+    while (parts.next_t<SPLIT, MASK == kMaskBand>(p.sch, pt)) {
         int bh, ct;
-        sched_decode_t<SPLIT>(p.sch, pt.tile, bh, ct);
-        const int n0 = part_steps(pt, sched_kv_tiles(p.sch, ct, 0)), n1 = part_steps(pt, sched_kv_tiles(p.sch, ct, 1));
+        sched_decode_t<SPLIT, MASK == kMaskBand>(p.sch, pt.tile, bh, ct);
+        const int n0 = part_steps(pt, sched_kv_tiles_t<MASK == kMaskBand>(p.sch, ct, 0)), n1 = part_steps(pt, sched_kv_tiles_t<MASK == kMaskBand>(p.sch, ct, 1));
         const int n = pt.ke - pt.kb;
         const int qb = it % C::kQBufs;
         if (!warp_wait(b.q_full(qb), (uint32_t)(it / C::kQBufs) & 1u, c, kSiteMmaQFull))
@@ -559,10 +569,11 @@ __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage
 
 // ------------------------------------------------------------------ softmax
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, int MASK, bool SPLIT>
 __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, float2 *handoff)
 {
     using C = Cfg<D>;
+    constexpr bool CAUSAL = MASK != kMaskNone;
     const int w = threadIdx.x / 128;              // Q tile of this warpgroup
     const int t = threadIdx.x % 128;              // row within the Q tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(t & ~31) << 16;
@@ -575,16 +586,29 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
     PartIter parts;
     parts.init_t<SPLIT>(p.sch, blockIdx.x);
     Part pt;
-    while (parts.next_t<SPLIT>(p.sch, pt)) {
+    while (parts.next_t<SPLIT, MASK == kMaskBand>(p.sch, pt)) {
         int bh, ct;
-        sched_decode_t<SPLIT>(p.sch, pt.tile, bh, ct);
-        const int nw = sched_kv_tiles(p.sch, ct, w);    // steps of this Q tile in the whole tile
+        sched_decode_t<SPLIT, MASK == kMaskBand>(p.sch, pt.tile, bh, ct);
+        const int nw = sched_kv_tiles_t<MASK == kMaskBand>(p.sch, ct, w);    // steps of this Q tile in the whole tile
         const int np = part_steps(pt, nw);              // ... of which this part holds steps kb .. kb + np - 1
         if (np == 0)
             continue;
         const int row = ct * kCtaRows + w * kBM + t;                // query index (may be >= N: padding)
-        const int row_limit = CAUSAL ? min(p.Nkv, row + 1 + p.off) : p.Nkv;   // keys < row_limit are visible (may be <= 0)
-        const int first_row = ct * kCtaRows + w * kBM;                // the Q tile's first row sees keys <= first_row + off
+        // Masked attention sees a band of keys: this row [row_lo, row_hi); a
+        // step needs masking where some row's band edge or the key count ends
+        // inside it: past the Q tile's first row's upper edge, before its last
+        // row's lower edge (kMaskBand only), or past Nkv.
+        const int ks = (MASK == kMaskBand) ? sched_kv_start(p.sch, ct) : 0;   // the tile's first key step
+        int row_lo = 0, row_hi = p.Nkv, edge_lo = 0, edge_hi = p.Nkv;
+        if (CAUSAL) {
+            const int first = ct * kCtaRows + w * kBM, r = min(row, p.N - 1);
+            row_hi = sched_row_hi(p.sch, r);
+            edge_hi = sched_row_hi(p.sch, first);
+            if (MASK == kMaskBand) {
+                row_lo = sched_row_lo(p.sch, r);
+                edge_lo = sched_row_lo(p.sch, min(first + kBM - 1, p.N - 1));
+            }
+        }
         float m = -INFINITY, l = 0.f;                               // running max (log2 units), row sum
 
         for (int jr = 0; jr < np; ++jr) {
@@ -608,13 +632,21 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             for (int i = 0; i < 128; ++i)
                 s[i] = __uint_as_float(r[i / 64][i % 64]);
 
-            // Steps with keys past what the tile's first row sees (the diagonal,
-            // which crosses one or two steps), and the ragged last step.
-            if ((CAUSAL && (j + 1) * kBN > first_row + p.off + 1) || (j + 1) * kBN > p.Nkv) {
-                const int lim = row_limit - j * kBN;
+            const int kb0 = (ks + j) * kBN;   // this step's first key
+            if (MASK == kMaskBand) {
+                if (kb0 < edge_lo || kb0 + kBN > edge_hi) {   // (edge_hi <= Nkv)
+                    // key kb0 + i is visible iff row_lo <= kb0 + i < row_hi (one unsigned compare)
+                    const int lo = row_lo - kb0;
+                    const uint32_t width = (uint32_t)(row_hi - row_lo);
+#pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        s[i] = ((uint32_t)(i - lo) < width) ? s[i] : -INFINITY;
+                }
+            } else if ((CAUSAL && kb0 + kBN > edge_hi) || kb0 + kBN > p.Nkv) {
+                const int hi = row_hi - kb0;   // keys kb0 + i with i < hi are visible
 #pragma unroll
                 for (int i = 0; i < 128; ++i)
-                    s[i] = (i < lim) ? s[i] : -INFINITY;
+                    s[i] = (i < hi) ? s[i] : -INFINITY;
             }
 
             float mx[8];   // eight partial maxima: s[0..15] pairwise, then s[16..127] two at a time
@@ -916,7 +948,7 @@ __device__ void merge_role(const FwdParams &p, uint32_t sbuf, uint32_t sml, cons
 // writes O = acc / l in the input type and LSE = (m + log2 l) ln 2; a part of
 // a split tile writes its partial result to its workspace slot, and the part
 // that finishes last hands the merge of that Q tile to the merge warp.
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, int MASK, bool SPLIT>
 __device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, uint32_t s_handoff, uint32_t s_flag,
                               uint32_t s_jobs)
 {
@@ -962,13 +994,13 @@ __device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl 
     PartIter parts;
     parts.init_t<SPLIT>(p.sch, blockIdx.x);
     Part pt;
-    while (parts.next_t<SPLIT>(p.sch, pt)) {
+    while (parts.next_t<SPLIT, MASK == kMaskBand>(p.sch, pt)) {
         int bh, ct;
-        sched_decode_t<SPLIT>(p.sch, pt.tile, bh, ct);
+        sched_decode_t<SPLIT, MASK == kMaskBand>(p.sch, pt.tile, bh, ct);
         uint32_t published = 0;                   // bit w: Q tile w wrote a partial result
 #pragma unroll
         for (int w = 0; w < kQTiles; ++w) {
-            const int nw = sched_kv_tiles(p.sch, ct, w);
+            const int nw = sched_kv_tiles_t<MASK == kMaskBand>(p.sch, ct, w);
             const int np = part_steps(pt, nw);
             if (np == 0)
                 continue;
@@ -1053,7 +1085,7 @@ __device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl 
             for (int w = 0; w < kQTiles; ++w) {
                 if (!(published >> w & 1u))
                     continue;
-                const int nw = sched_kv_tiles(p.sch, ct, w);
+                const int nw = sched_kv_tiles_t<MASK == kMaskBand>(p.sch, ct, w);
                 int expected = 0, slot;
                 for (int cc = clo; cc <= chi; ++cc)
                     expected += sched_part_slot(p.sch, pt.ts, n, nw, cc, slot) ? 1 : 0;
@@ -1072,7 +1104,7 @@ __device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl 
         for (int w = 0; w < kQTiles; ++w) {
             if (!(last >> w & 1))
                 continue;
-            const int nw = sched_kv_tiles(p.sch, ct, w);
+            const int nw = sched_kv_tiles_t<MASK == kMaskBand>(p.sch, ct, w);
             int nparts = 0, slot;
             for (int cc = clo; cc <= chi; ++cc)
                 nparts += sched_part_slot(p.sch, pt.ts, n, nw, cc, slot) ? 1 : 0;
@@ -1088,12 +1120,13 @@ __device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl 
 
 // ------------------------------------------------------------------ kernel
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, int MASK, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p)
 {
     using C = Cfg<D>;
+    constexpr bool CAUSAL = MASK != kMaskNone;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;    // 128-byte swizzle atoms need 1024-byte alignment
@@ -1155,16 +1188,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (wg < kEpilogueWarpgroup) {
         ptx::regs_increase<kRegsSoftmax>();
-        softmax_role<D, BF16, CAUSAL, SPLIT>(p, tmem, b, c, handoff);
+        softmax_role<D, BF16, MASK, SPLIT>(p, tmem, b, c, handoff);
     } else if (wg == kEpilogueWarpgroup) {
         ptx::regs_decrease<kRegsEpilogue>();
-        epilogue_role<D, BF16, CAUSAL, SPLIT>(p, tmem, b, c, base + C::kHandOff, base + C::kMiscOff + 8, base + C::kJobOff);
+        epilogue_role<D, BF16, MASK, SPLIT>(p, tmem, b, c, base + C::kHandOff, base + C::kMiscOff + 8, base + C::kJobOff);
     } else {
         ptx::regs_decrease<kRegsProducer>();
         if (warp == kLoadWarp)
-            load_role<D, CAUSAL, SPLIT>(&tmQ, &tmK, &tmV, p, sQ, sStage, b, c);
+            load_role<D, MASK, SPLIT>(&tmQ, &tmK, &tmV, p, sQ, sStage, b, c);
         else if (warp < kMmaWarp + C::kMmaWarps)
-            mma_role<D, BF16, CAUSAL, SPLIT>(warp - kMmaWarp, p, sQ, sStage, tmem, b, c);
+            mma_role<D, BF16, MASK, SPLIT>(warp - kMmaWarp, p, sQ, sStage, tmem, b, c);
         else if (SPLIT && warp == kMergeWarp)
             merge_role<D, BF16>(p, base + C::kMergeOff, base + C::kMlOff,
                                 reinterpret_cast<const MergeJob *>(base_ptr + C::kJobOff), b, c);

@@ -1,7 +1,9 @@
-// fa_launch.cuh -- kernel selection and launch, shared by the two translation
-// units that instantiate the kernels: fa_api.cu (whole-tile variants, with the
-// C ABI) and fa_split.cu (balanced-schedule variants).  Two units keep each
-// nvcc run to eight kernels and let the build compile them in parallel.
+// fa_launch.cuh -- kernel selection and launch, shared by the three
+// translation units that instantiate the kernels: fa_api.cu (whole-tile
+// variants without a mask or with the causal one, and the C ABI), fa_split.cu
+// (the same for the balanced schedule) and fa_band.cu (left-bounded band
+// masks, both schedules).  Three units keep each nvcc run to eight kernels and
+// let the build compile them in parallel.
 #pragma once
 
 #include <cuda.h>
@@ -24,13 +26,13 @@ namespace {
 
 // Launch one variant on `grid` CTAs.  The dynamic shared-memory limit is
 // raised once per device and variant.
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, int MASK, bool SPLIT>
 fa_status launch_variant(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const fa::FwdParams &p,
                          int grid, cudaStream_t stream, int dev)
 {
     static std::mutex mu;
     static bool attr_set[kMaxDevices] = {};
-    auto kern = fa::fa_fwd_sm103<D, BF16, CAUSAL, SPLIT>;
+    auto kern = fa::fa_fwd_sm103<D, BF16, MASK, SPLIT>;
     constexpr int smem = fa::Cfg<D>::smem_bytes(SPLIT);
     if (dev < 0 || dev >= kMaxDevices)
         return FA_ERR_UNSUPPORTED_DEVICE;
@@ -50,22 +52,16 @@ fa_status launch_variant(const CUtensorMap &q, const CUtensorMap &k, const CUten
     return FA_OK;
 }
 
-template <bool SPLIT>
-fa_status launch_any(int D, bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                     const fa::FwdParams &p, int grid, cudaStream_t s, int dev)
+// The variants of one mask (kMaskNone, kMaskCausal or kMaskBand) and schedule.
+template <int MASK, bool SPLIT>
+fa_status launch_mask(int D, bool bf16, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                      const fa::FwdParams &p, int grid, cudaStream_t s, int dev)
 {
-    if (D == 64) {
-        if (bf16)
-            return causal ? launch_variant<64, true, true, SPLIT>(q, k, v, p, grid, s, dev)
-                          : launch_variant<64, true, false, SPLIT>(q, k, v, p, grid, s, dev);
-        return causal ? launch_variant<64, false, true, SPLIT>(q, k, v, p, grid, s, dev)
-                      : launch_variant<64, false, false, SPLIT>(q, k, v, p, grid, s, dev);
-    }
-    if (bf16)
-        return causal ? launch_variant<128, true, true, SPLIT>(q, k, v, p, grid, s, dev)
-                      : launch_variant<128, true, false, SPLIT>(q, k, v, p, grid, s, dev);
-    return causal ? launch_variant<128, false, true, SPLIT>(q, k, v, p, grid, s, dev)
-                  : launch_variant<128, false, false, SPLIT>(q, k, v, p, grid, s, dev);
+    if (D == 64)
+        return bf16 ? launch_variant<64, true, MASK, SPLIT>(q, k, v, p, grid, s, dev)
+                    : launch_variant<64, false, MASK, SPLIT>(q, k, v, p, grid, s, dev);
+    return bf16 ? launch_variant<128, true, MASK, SPLIT>(q, k, v, p, grid, s, dev)
+                : launch_variant<128, false, MASK, SPLIT>(q, k, v, p, grid, s, dev);
 }
 
 // Read and clear this translation unit's device status word (current
@@ -89,13 +85,17 @@ inline bool take_status_word_here(unsigned int *word)
 
 }  // namespace
 
-// Defined in fa_api.cu and fa_split.cu respectively.
+// Defined in fa_api.cu, fa_split.cu and fa_band.cu respectively; `causal`
+// selects kMaskCausal over kMaskNone, `split` the balanced schedule.
 fa_status launch_whole(int D, bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k,
                        const CUtensorMap &v, const fa::FwdParams &p, int grid, cudaStream_t s, int dev);
 fa_status launch_split(int D, bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k,
                        const CUtensorMap &v, const fa::FwdParams &p, int grid, cudaStream_t s, int dev);
+fa_status launch_band(int D, bool bf16, bool split, const CUtensorMap &q, const CUtensorMap &k,
+                      const CUtensorMap &v, const fa::FwdParams &p, int grid, cudaStream_t s, int dev);
 bool take_status_word_whole(unsigned int *word);
 bool take_status_word_split(unsigned int *word);
+bool take_status_word_band(unsigned int *word);
 
 // The static workspace of fa_fwd_noalloc (fa_split.cu): points p's partial
 // buffers into it for schedule `sc` and head size D, and clears the counters

@@ -45,35 +45,89 @@ constexpr int kSchedCtaRows = 256;   // rows per CTA tile
 constexpr int kSchedMaxGrid = 160;   // CTAs of a balanced-schedule launch, at most
 constexpr long long kSchedMaxUnits = 0x3fffffffLL;   // units of a balanced schedule, at most (32-bit unit indices)
 constexpr int kSchedMaxParts = 8;                    // parts of one tile in a balanced schedule, at most
+constexpr int kSchedUnbounded = 0x3fffffff;          // a band bound that never binds
 
 struct Schedule {
     int N;          // query rows per head
     int Nkv;        // keys per head
-    int off;        // causal alignment: query i sees keys j <= i + off (off = Nkv - N, bottom-right)
+    int off;        // masked ("causal"): query i sits at key position i + off (off = Nkv - N, bottom-right)
+    int wl, wr;     // masked: query i sees keys [i + off - wl, i + off + wr] (kSchedUnbounded: no bound);
+                    // a bound that cannot bind is stored as kSchedUnbounded (sched_band_normalize)
+    int ka, ra;     // masked: the first key of row r lies in step ((r + ra) >> 7) + ka (floor division of r + off - wl)
+    int kb, rb;     // masked: the last key of row r lies in step ((r + rb) >> 7) + kb (floor division of r + off + wr)
     int BH;         // batch * heads
     int C;          // CTA tiles per head: ceil(N / 256)
     int T;          // CTA tiles: BH * C
     int nkv;        // K/V steps of a full row: ceil(Nkv / 128)
     int causal;     // 0 or 1
+    int rev;        // masked: 1 if the first tile row is longer than the last (a band bounded on the left only)
     int G;          // CTAs in the grid
     int split;      // 1: balanced schedule with partial tiles
     long long U;    // total units (the balanced schedule requires U <= kSchedMaxUnits)
     int range[kSchedMaxGrid + 1];   // balanced: range[c] = floor(U c / G), filled by sched_fill_ranges
 };
 
-// Causal steps of rows up to `last`: up to the step holding key last + off.
-// Rows that see no key at all (last + off < 0) still take one step, fully
-// masked, so that their O = 0 and LSE = -inf get written.
-FA_HD int sched_causal_steps(const Schedule &s, int last)
+// Band bounds that cannot bind become kSchedUnbounded: with off = Nkv - N,
+// query rows sit at positions off .. Nkv - 1, so wl >= Nkv clips nothing on
+// the left and wr >= N - 1 nothing on the right.  After this, r + off - wl
+// and the step offsets below stay within 32-bit range for any valid sizes.
+FA_HD void sched_band_normalize(int N, int Nkv, int &wl, int &wr)
 {
-    const int vis = last + s.off;
-    if (vis < 0)
-        return 1;
-    const int n = vis / kSchedBN + 1;
-    return n < s.nkv ? n : s.nkv;
+    if (wl < 0 || wl >= Nkv || wl >= kSchedUnbounded)
+        wl = kSchedUnbounded;
+    if (wr < 0 || wr >= N - 1 || wr >= kSchedUnbounded)
+        wr = kSchedUnbounded;
 }
 
-// K/V steps visited by Q tile w (0 or 1) of CTA tile ct; 0 if it holds no valid row.
+// Masked attention (a band, of which causal is one case): rows first .. last
+// see keys [first + off - wl, last + off + wr]; the K/V steps holding them are
+// [ks, ke).  Rows whose bands hold no key still take one step, fully masked,
+// so that their O = 0 and LSE = -inf get written.  (32-bit arithmetic on the
+// offsets that sched_plan precomputes: floor((r + x) / 128) = ((r + rx) >> 7) + kx
+// with x = 128 kx + rx, 0 <= rx < 128.)
+FA_HD void sched_band_steps(const Schedule &s, int first, int last, int &ks, int &ke)
+{
+    int a = (int)(((uint32_t)first + (uint32_t)s.ra) >> 7) + s.ka;
+    int b = (int)(((uint32_t)last + (uint32_t)s.rb) >> 7) + s.kb + 1;
+    a = a < 0 ? 0 : (a > s.nkv - 1 ? s.nkv - 1 : a);
+    b = b > s.nkv ? s.nkv : b;
+    ks = a;
+    ke = b <= a ? a + 1 : b;
+}
+
+// Keys of query row r (0 <= r < N) under the band, clipped to [0, Nkv):
+// [sched_row_lo, sched_row_hi), empty when they are equal.
+FA_HD int sched_row_lo(const Schedule &s, int r)
+{
+    const int lo = r + s.off - s.wl;   // (normalised wl < Nkv: no overflow)
+    return (s.wl >= kSchedUnbounded || lo < 0) ? 0 : lo;
+}
+
+FA_HD int sched_row_hi(const Schedule &s, int r)
+{
+    const int pos = r + s.off;   // <= Nkv - 1
+    if (s.wr >= kSchedUnbounded || s.wr >= s.Nkv - pos - 1)
+        return s.Nkv;
+    const int hi = pos + s.wr + 1;
+    return hi < 0 ? 0 : hi;
+}
+
+// First K/V step of CTA tile ct (its rows' earliest visible key); 0 unmasked.
+FA_HD int sched_kv_start(const Schedule &s, int ct)
+{
+    if (!s.causal)
+        return 0;
+    const int first = ct * kSchedCtaRows;
+    const int last = (first + kSchedCtaRows - 1 < s.N - 1) ? first + kSchedCtaRows - 1 : s.N - 1;
+    int ks, ke;
+    sched_band_steps(s, first, last, ks, ke);
+    return ks;
+}
+
+// K/V steps visited by Q tile w (0 or 1) of CTA tile ct, counted from the
+// tile's first step sched_kv_start(ct) (a Q tile's steps are a prefix of its
+// CTA tile's: a later Q tile may take a first step that is fully masked for
+// it); 0 if it holds no valid row.
 FA_HD int sched_kv_tiles(const Schedule &s, int ct, int w)
 {
     const int r0 = ct * kSchedCtaRows + w * kSchedBM;
@@ -82,16 +136,57 @@ FA_HD int sched_kv_tiles(const Schedule &s, int ct, int w)
     if (!s.causal)
         return s.nkv;
     const int last = (r0 + kSchedBM - 1 < s.N - 1) ? r0 + kSchedBM - 1 : s.N - 1;
-    return sched_causal_steps(s, last);
+    int ks, ke;
+    sched_band_steps(s, r0, last, ks, ke);
+    return ke - sched_kv_start(s, ct);
 }
 
-// Steps of CTA tile ct: those of its last valid Q tile.
+// Masks without a left bound start every row's steps at 0: the steps of rows
+// up to `last` end at this step (the end half of sched_band_steps alone).
+FA_HD int sched_step_end(const Schedule &s, int last)
+{
+    const int b = (int)(((uint32_t)last + (uint32_t)s.rb) >> 7) + s.kb + 1;
+    return b < 1 ? 1 : (b > s.nkv ? s.nkv : b);
+}
+
+// sched_kv_tiles in the kernel: BAND (a left bound) takes the general form,
+// other masks the step end alone.
+template <bool BAND>
+FA_HD int sched_kv_tiles_t(const Schedule &s, int ct, int w)
+{
+    if (BAND)
+        return sched_kv_tiles(s, ct, w);
+    const int r0 = ct * kSchedCtaRows + w * kSchedBM;
+    if (r0 >= s.N)
+        return 0;
+    if (!s.causal)
+        return s.nkv;
+    return sched_step_end(s, (r0 + kSchedBM - 1 < s.N - 1) ? r0 + kSchedBM - 1 : s.N - 1);
+}
+
+// Steps of CTA tile ct: from its first step to its last valid row's last.
 FA_HD int sched_steps_ct(const Schedule &s, int ct)
 {
     if (!s.causal)
         return s.nkv;
-    const int last = (ct * kSchedCtaRows + kSchedCtaRows - 1 < s.N - 1) ? ct * kSchedCtaRows + kSchedCtaRows - 1 : s.N - 1;
-    return sched_causal_steps(s, last);
+    const int first = ct * kSchedCtaRows;
+    const int last = (first + kSchedCtaRows - 1 < s.N - 1) ? first + kSchedCtaRows - 1 : s.N - 1;
+    int ks, ke;
+    sched_band_steps(s, first, last, ks, ke);
+    return ke - ks;
+}
+
+// Tile rows by length: the q-th longest and the q-th shortest (step counts
+// are monotone in the row for causal masks and one-sided bands, and equal but
+// for the clipped ends for two-sided ones).
+FA_HD int sched_long_row(const Schedule &s, int q)
+{
+    return s.rev ? q : s.C - 1 - q;
+}
+
+FA_HD int sched_short_row(const Schedule &s, int q)
+{
+    return s.rev ? s.C - 1 - q : q;
 }
 
 FA_HD void sched_decode(const Schedule &s, int t, int &bh, int &ct)
@@ -101,13 +196,13 @@ FA_HD void sched_decode(const Schedule &s, int t, int &bh, int &ct)
         if (q < s.C / 2) {
             const int i = t - q * 2 * s.BH;
             bh = i / 2;
-            ct = (i & 1) ? q : s.C - 1 - q;
+            ct = (i & 1) ? sched_short_row(s, q) : sched_long_row(s, q);
         } else {                  // the middle row of an odd C
             bh = t - q * 2 * s.BH;
             ct = s.C / 2;
         }
     } else if (s.causal) {        // one tile row per group, longest first, heads interleaved
-        ct = s.C - 1 - t / s.BH;
+        ct = sched_long_row(s, t / s.BH);
         bh = t % s.BH;
     } else {          // head-major: neighbouring CTAs share a head's K/V in L2
         bh = t / s.C;
@@ -119,7 +214,7 @@ FA_HD void sched_decode(const Schedule &s, int t, int &bh, int &ct)
 FA_HD void sched_decode_rr(const Schedule &s, int t, int &bh, int &ct)
 {
     if (s.causal) {
-        ct = s.C - 1 - t / s.BH;
+        ct = sched_long_row(s, t / s.BH);
         bh = t % s.BH;
     } else {
         bh = t / s.C;
@@ -131,16 +226,36 @@ FA_HD int sched_steps_rr(const Schedule &s, int t)
 {
     if (!s.causal)
         return s.nkv;
-    return sched_steps_ct(s, s.C - 1 - t / s.BH);
+    return sched_steps_ct(s, sched_long_row(s, t / s.BH));
 }
 
-template <bool SPLIT>
+// The kernel's forms: BAND = false (no left bound) knows that rows are
+// longest last (rev = 0) and that steps start at 0.
+template <bool SPLIT, bool BAND = true>
 FA_HD void sched_decode_t(const Schedule &s, int t, int &bh, int &ct)
 {
-    if (SPLIT)
+    if (SPLIT) {
         sched_decode(s, t, bh, ct);
-    else
+    } else if (BAND) {
         sched_decode_rr(s, t, bh, ct);
+    } else if (s.causal) {
+        ct = s.C - 1 - t / s.BH;
+        bh = t % s.BH;
+    } else {
+        bh = t / s.C;
+        ct = t % s.C;
+    }
+}
+
+template <bool BAND>
+FA_HD int sched_steps_rr_t(const Schedule &s, int t)
+{
+    if (BAND)
+        return sched_steps_rr(s, t);
+    if (!s.causal)
+        return s.nkv;
+    const int first = (s.C - 1 - t / s.BH) * kSchedCtaRows;
+    return sched_step_end(s, (first + kSchedCtaRows - 1 < s.N - 1) ? first + kSchedCtaRows - 1 : s.N - 1);
 }
 
 FA_HD int sched_steps(const Schedule &s, int t)
@@ -159,10 +274,10 @@ FA_HD long long sched_prefix(const Schedule &s, int t)
         const int q = t / (2 * s.BH);
         long long acc = 0;
         for (int r = 0; r < q; ++r)
-            acc += (long long)s.BH * (sched_steps_ct(s, s.C - 1 - r) + sched_steps_ct(s, r));
+            acc += (long long)s.BH * (sched_steps_ct(s, sched_long_row(s, r)) + sched_steps_ct(s, sched_short_row(s, r)));
         const int i = t - q * 2 * s.BH;
         if (q < s.C / 2) {
-            const int lg = sched_steps_ct(s, s.C - 1 - q), sh = sched_steps_ct(s, q);
+            const int lg = sched_steps_ct(s, sched_long_row(s, q)), sh = sched_steps_ct(s, sched_short_row(s, q));
             return acc + (long long)(i / 2) * (lg + sh) + ((i & 1) ? lg : 0);
         }
         return acc + (long long)i * sched_steps_ct(s, s.C / 2);
@@ -170,8 +285,8 @@ FA_HD long long sched_prefix(const Schedule &s, int t)
     const int g = t / s.BH;   // tiles come in groups of BH with equal step counts
     long long acc = 0;
     for (int q = 0; q < g; ++q)
-        acc += (long long)s.BH * sched_steps_ct(s, s.C - 1 - q);
-    return acc + (long long)(t - g * s.BH) * sched_steps_ct(s, s.C - 1 - g);
+        acc += (long long)s.BH * sched_steps_ct(s, sched_long_row(s, q));
+    return acc + (long long)(t - g * s.BH) * sched_steps_ct(s, sched_long_row(s, g));
 }
 
 FA_HD long long sched_total_units(const Schedule &s)
@@ -213,7 +328,7 @@ FA_HD int sched_tile_of_unit(const Schedule &s, int u, int &tstart)
     // (balanced schedules only) pairs of tile rows, then the middle row of an odd C
     int acc = 0;
     for (int q = 0; q < s.C / 2; ++q) {
-        const int lg = sched_steps_ct(s, s.C - 1 - q), sh = sched_steps_ct(s, q);
+        const int lg = sched_steps_ct(s, sched_long_row(s, q)), sh = sched_steps_ct(s, sched_short_row(s, q));
         const int gu = s.BH * (lg + sh);
         if (u < acc + gu) {
             const int rel = u - acc, pair = rel / (lg + sh), rem = rel - pair * (lg + sh);
@@ -286,7 +401,7 @@ struct PartIter {
         }
     }
 
-    template <bool SPLIT>
+    template <bool SPLIT, bool BAND = true>
     FA_HD bool next_t(const Schedule &s, Part &p)
     {
         if (SPLIT) {
@@ -318,7 +433,7 @@ struct PartIter {
             return false;
         p.tile = t;
         p.kb = 0;
-        p.ke = sched_steps_rr(s, t);
+        p.ke = sched_steps_rr_t<BAND>(s, t);
         p.slot = -1;
         p.ts = 0;
         ++u;
@@ -405,19 +520,50 @@ FA_HD int sched_part_slots(const Schedule &s, int t, int nw, int *slots, int max
 constexpr int kSchedMinGain = 4;
 
 // mode: 0 = as above, 1 = round-robin, 2 = balanced wherever it can be built.
-// N query rows against Nkv keys per head.
-inline Schedule sched_plan(int N, int Nkv, int BH, bool causal, int sms, int mode = 0)
+// N query rows against Nkv keys per head; `causal` here means masked by the
+// band [i + off - wl, i + off + wr] (causal proper: wl unbounded, wr = 0).
+inline Schedule sched_plan(int N, int Nkv, int BH, bool causal, int sms, int mode = 0, int wl = kSchedUnbounded,
+                           int wr = 0)
 {
     Schedule s{};
     s.N = N;
     s.Nkv = Nkv;
     s.off = causal ? Nkv - N : 0;
+    if (!causal) {
+        wl = kSchedUnbounded;
+        wr = kSchedUnbounded;
+    }
+    sched_band_normalize(N, Nkv, wl, wr);
+    s.wl = wl;
+    s.wr = wr;
+    {
+        const long long lo_off = (long long)s.off - wl, hi_off = (long long)s.off + wr;
+        const long long ka = (lo_off >= 0) ? lo_off / kSchedBN : -((-lo_off + kSchedBN - 1) / kSchedBN);
+        const long long kb = (hi_off >= 0) ? hi_off / kSchedBN : -((-hi_off + kSchedBN - 1) / kSchedBN);
+        s.ka = (wl >= kSchedUnbounded) ? -(1 << 29) : (int)ka;
+        s.ra = (wl >= kSchedUnbounded) ? 0 : (int)(lo_off - ka * kSchedBN);
+        s.kb = (wr >= kSchedUnbounded) ? (1 << 29) : (int)kb;
+        s.rb = (wr >= kSchedUnbounded) ? 0 : (int)(hi_off - kb * kSchedBN);
+    }
     s.BH = BH;
     s.C = (N + kSchedCtaRows - 1) / kSchedCtaRows;
     s.T = BH * s.C;
     s.nkv = (Nkv + kSchedBN - 1) / kSchedBN;
     s.causal = causal ? 1 : 0;
+    s.rev = 0;
     s.split = 0;
+    // the longest tile row: an end row for causal masks and one-sided bands,
+    // any unclipped row for two-sided ones -- found by looking at every row
+    int max_steps = 0;
+    if (causal) {
+        s.rev = sched_steps_ct(s, 0) > sched_steps_ct(s, s.C - 1) ? 1 : 0;
+        for (int ct = 0; ct < s.C; ++ct) {
+            const int n = sched_steps_ct(s, ct);
+            max_steps = n > max_steps ? n : max_steps;
+        }
+    } else {
+        max_steps = s.nkv;
+    }
     s.G = s.T < sms ? s.T : sms;
     if (s.G > kSchedMaxGrid)   // (a larger part than this library targets runs on kSchedMaxGrid CTAs)
         s.G = kSchedMaxGrid;
@@ -435,7 +581,6 @@ inline Schedule sched_plan(int N, int Nkv, int BH, bool causal, int sms, int mod
     }
     if (s.U > kSchedMaxUnits || mode == 1)
         return s;
-    const int max_steps = sched_steps_ct(s, s.C - 1);   // the last tile row is the longest
     long long G = (s.U < sms) ? s.U : sms;
     if (G > kSchedMaxGrid)
         G = kSchedMaxGrid;

@@ -9,7 +9,8 @@ namespace fa_launch {
 fa_status launch_split(int D, bool bf16, bool causal, const CUtensorMap &q, const CUtensorMap &k,
                        const CUtensorMap &v, const fa::FwdParams &p, int grid, cudaStream_t s, int dev)
 {
-    return launch_any<true>(D, bf16, causal, q, k, v, p, grid, s, dev);
+    return causal ? launch_mask<fa::kMaskCausal, true>(D, bf16, q, k, v, p, grid, s, dev)
+                  : launch_mask<fa::kMaskNone, true>(D, bf16, q, k, v, p, grid, s, dev);
 }
 
 bool take_status_word_split(unsigned int *word)

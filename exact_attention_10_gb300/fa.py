@@ -14,7 +14,7 @@ from .build import LIB_PATH
 FA_BF16, FA_FP16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_MISALIGNED", 3: "FA_ERR_UNSUPPORTED_DEVICE",
           4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT", 6: "FA_ERR_NO_ALLOC_LIMIT"}
-EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_noalloc", "fa_fwd_qkv", "fa_sync_status", "fa_status_string")
+EXPORTS = ("fa_fwd", "fa_fwd_band", "fa_fwd_ex", "fa_fwd_noalloc", "fa_fwd_qkv", "fa_sync_status", "fa_status_string")
 SCHEDULES = {"auto": 0, "whole_tiles": 1, "balanced": 2}
 
 _lib = None
@@ -44,6 +44,9 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd_qkv.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, ctypes.c_float, c_int,
                                c_int, vp]
     lib.fa_fwd_qkv.restype = c_int
+    lib.fa_fwd_band.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int, ctypes.c_float,
+                                c_int, c_int, vp]
+    lib.fa_fwd_band.restype = c_int
     lib.fa_sync_status.argtypes = [vp]
     lib.fa_sync_status.restype = c_int
     lib.fa_status_string.argtypes = [c_int]
@@ -83,10 +86,12 @@ def _dtype_code(t) -> int:
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
-            schedule: str = "auto"):
+            schedule: str = "auto", window: tuple[int, int] | None = None):
     """Attention forward on CUDA tensors q [B, H, Nq, D], k and v [B, H, Nkv, D];
     returns (O [B, H, Nq, D], LSE [B, H, Nq]).  With Nq != Nkv the causal mask
-    is aligned bottom-right (fa_fwd_qkv).
+    is aligned bottom-right (fa_fwd_qkv).  ``window = (left, right)`` masks
+    with a band instead (fa_fwd_band; a negative bound is unbounded; causal
+    is ignored then).
 
     ``out`` / ``lse`` may be given to write into existing buffers.
     ``schedule`` is "auto", "whole_tiles" or "balanced" (fa_schedule).
@@ -114,7 +119,10 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     if schedule not in SCHEDULES:
         raise ValueError(f"schedule must be one of {sorted(SCHEDULES)}")
     Nkv = k.shape[2]
-    if Nkv == N:
+    if window is not None:
+        rc = load().fa_fwd_band(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, Nkv,
+                                D, int(window[0]), int(window[1]), float(scale), code, SCHEDULES[schedule], st)
+    elif Nkv == N:
         rc = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D,
                      int(bool(causal)), float(scale), code, st, SCHEDULES[schedule])
     else:

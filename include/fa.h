@@ -161,6 +161,19 @@ FA_API fa_status fa_fwd_qkv(const void *Q, const void *K, const void *V, void *O
                             fa_dtype dtype, fa_schedule schedule, fa_stream_t stream);
 
 /*
+ * fa_fwd_band -- fa_fwd_qkv with a sliding-window (band) mask: with
+ * i' = i + (Nkv - Nq), query i sees keys j in [i' - window_left,
+ * i' + window_right]; a negative bound is unbounded on that side.  Causal is
+ * (-1, 0), no mask (-1, -1), a causal window of W keys (W - 1, 0).  A query
+ * whose band holds no key gets O = 0 and LSE = -inf.  Key tiles wholly
+ * outside every row's band are skipped, not masked.  Other arguments as for
+ * fa_fwd_qkv.
+ */
+FA_API fa_status fa_fwd_band(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                             int B, int H, int Nq, int Nkv, int D, int window_left, int window_right,
+                             float scale, fa_dtype dtype, fa_schedule schedule, fa_stream_t stream);
+
+/*
  * fa_fwd_noalloc -- fa_fwd_ex that allocates no memory, device or host, at
  * any call.  The pages describe nothing like it: the method itself needs no
  * scratch, and this entry point only concerns where this library's balanced

@@ -14,43 +14,128 @@
 
 using namespace fa;
 
-static int check_schedule(const Schedule &s, bool planned);
+static int check_schedule(const Schedule &s, bool planned, int wl, int wr);
 
-static int check(int N, int Nkv, int BH, int causal, int G, int split)
+// A schedule of G CTAs, balanced or not, for the band (wl, wr) as given
+// (kSchedUnbounded: no bound); the planner supplies its mask fields.
+static int check(int N, int Nkv, int BH, int causal, int G, int split, int wl, int wr)
 {
-    Schedule s{};
-    s.N = N;
-    s.Nkv = Nkv;
-    s.off = causal ? Nkv - N : 0;
-    s.BH = BH;
-    s.C = (N + 255) / 256;
-    s.T = BH * s.C;
-    s.nkv = (Nkv + 127) / 128;
-    s.causal = causal;
+    if (G > kSchedMaxGrid)
+        return 0;
+    Schedule s = sched_plan(N, Nkv, BH, causal != 0, G, 1, wl, wr);
     s.G = G;
     s.split = split;
     s.U = sched_total_units(s);
-    if (G > kSchedMaxGrid || s.U > kSchedMaxUnits)
+    if (s.U > kSchedMaxUnits)
         return 0;
     sched_fill_ranges(s);
-    return check_schedule(s, false);
+    return check_schedule(s, false, wl, wr);
 }
 
 // The planner's schedule for `sms` SMs: valid, and a balanced one cuts no
 // tile into more parts than the merge handles.
-static int check_plan(int N, int Nkv, int BH, int causal, int sms)
+static int check_plan(int N, int Nkv, int BH, int causal, int sms, int wl, int wr)
 {
-    const Schedule s = sched_plan(N, Nkv, BH, causal != 0, sms);
-    if (s.G < 1 || (!s.split && s.G != (s.T < sms ? s.T : sms))) {
-        std::printf("bad grid %d\n", s.G);
-        return 1;
+    for (int mode : {0, 2}) {   // as planned (auto), and the balanced schedule forced
+        const Schedule s = sched_plan(N, Nkv, BH, causal != 0, sms, mode, wl, wr);
+        const int rr_grid = s.T < sms ? s.T : sms;
+        if (s.G < 1 || (!s.split && s.G != (rr_grid < kSchedMaxGrid ? rr_grid : kSchedMaxGrid))) {
+            std::printf("bad grid %d (mode %d)\n", s.G, mode);
+            return 1;
+        }
+        if (check_schedule(s, true, wl, wr)) {
+            std::printf("(mode %d)\n", mode);
+            return 1;
+        }
     }
-    return check_schedule(s, true);
+    return 0;
 }
 
-static int check_schedule(const Schedule &s, bool planned)
+// Every key a row of a Q tile sees lies in that Q tile's steps, which are a
+// prefix of its CTA tile's steps, and each row's [sched_row_lo, sched_row_hi)
+// is exactly its visible keys (brute force over the rows' bands as given,
+// before the planner drops bounds that cannot bind).
+static int check_key_ranges(const Schedule &s, int wl, int wr)
+{
+    for (int ct = 0; ct < s.C; ++ct) {
+        const int ks = sched_kv_start(s, ct), n = sched_steps_ct(s, ct);
+        for (int w = 0; w < 2; ++w) {
+            const int r0 = ct * 256 + w * 128;
+            const int nw = sched_kv_tiles(s, ct, w);
+            if (r0 >= s.N) {
+                if (nw != 0) { std::printf("padding Q tile has steps\n"); return 1; }
+                continue;
+            }
+            if (nw < 1 || nw > n) { std::printf("ct %d w %d: %d steps of %d\n", ct, w, nw, n); return 1; }
+            if (s.wl >= kSchedUnbounded && sched_kv_tiles_t<false>(s, ct, w) != nw) {   // the no-left-bound form
+                std::printf("ct %d w %d: %d steps by the step-end form, %d in general\n", ct, w,
+                            sched_kv_tiles_t<false>(s, ct, w), nw);
+                return 1;
+            }
+            for (int r = r0; r < r0 + 128 && r < s.N; ++r) {
+                long long lo = 0, hi = s.Nkv - 1;
+                if (s.causal) {
+                    if (wl < kSchedUnbounded) lo = (long long)r + s.off - wl;
+                    if (wr < kSchedUnbounded) hi = (long long)r + s.off + wr;
+                    if (lo < 0) lo = 0;
+                    if (hi > s.Nkv - 1) hi = s.Nkv - 1;
+                    const int rl = sched_row_lo(s, r), rh = sched_row_hi(s, r);
+                    const bool same = (hi < lo) ? (rl == rh) : (rl == lo && rh == hi + 1);
+                    if (!same) {
+                        std::printf("row %d: keys [%lld, %lld], row bounds [%d, %d)\n", r, lo, hi, rl, rh);
+                        return 1;
+                    }
+                }
+                if (hi < lo)
+                    continue;   // this row sees no key
+                if (lo / 128 < ks || hi / 128 >= ks + nw) {
+                    std::printf("ct %d w %d row %d keys [%lld, %lld] outside steps [%d, %d)\n", ct, w, r, lo, hi, ks,
+                                ks + nw);
+                    return 1;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+// Without a left bound the kernel walks whole tiles with the step-end forms
+// (PartIter::next_t<false, false>, sched_decode_t<false, false>): the same
+// parts and tiles as the general forms.
+static int check_no_band_forms(const Schedule &s)
+{
+    if (s.split || s.wl < kSchedUnbounded)
+        return 0;
+    for (int c = 0; c < s.G; ++c) {
+        PartIter a, b;
+        a.init_t<false>(s, c);
+        b.init_t<false>(s, c);
+        Part pa, pb;
+        for (;;) {
+            const bool ma = a.next_t<false, true>(s, pa), mb = b.next_t<false, false>(s, pb);
+            if (ma != mb || (ma && (pa.tile != pb.tile || pa.kb != pb.kb || pa.ke != pb.ke))) {
+                std::printf("c=%d: step-end walk differs at tile %d\n", c, pa.tile);
+                return 1;
+            }
+            if (!ma)
+                break;
+            int bh1, ct1, bh2, ct2;
+            sched_decode_t<false, true>(s, pa.tile, bh1, ct1);
+            sched_decode_t<false, false>(s, pa.tile, bh2, ct2);
+            if (bh1 != bh2 || ct1 != ct2) {
+                std::printf("tile %d decodes differently\n", pa.tile);
+                return 1;
+            }
+        }
+    }
+    return 0;
+}
+
+static int check_schedule(const Schedule &s, bool planned, int wl, int wr)
 {
     const int G = s.G, split = s.split;
+    if (check_key_ranges(s, wl, wr) || check_no_band_forms(s))
+        return 1;
     std::vector<std::vector<int>> cover(s.T);
     for (int t = 0; t < s.T; ++t)
         cover[t].assign(sched_steps(s, t), 0);
@@ -152,17 +237,21 @@ static int check_schedule(const Schedule &s, bool planned)
 
 int main(int argc, char **argv)
 {
-    // "N Nkv BH causal G split" cases, repeated; or "plan" then "N Nkv BH causal sms" cases
+    // "N Nkv BH causal G split wl wr" cases, repeated; or "plan" then "N Nkv BH causal sms wl wr" cases
+    // (wl, wr < 0: unbounded)
     int failures = 0, cases = 0;
     const bool plan = argc > 1 && std::string(argv[1]) == "plan";
-    const int width = plan ? 5 : 6;
+    const int width = plan ? 7 : 8;
     for (int i = plan ? 2 : 1; i + width <= argc; i += width) {
         const int N = std::atoi(argv[i]), Nkv = std::atoi(argv[i + 1]), BH = std::atoi(argv[i + 2]);
         const int causal = std::atoi(argv[i + 3]), G = std::atoi(argv[i + 4]), split = plan ? 0 : std::atoi(argv[i + 5]);
+        int wl = std::atoi(argv[i + width - 2]), wr = std::atoi(argv[i + width - 1]);
+        wl = wl < 0 ? kSchedUnbounded : wl;
+        wr = wr < 0 ? kSchedUnbounded : wr;
         ++cases;
-        if (plan ? check_plan(N, Nkv, BH, causal, G) : check(N, Nkv, BH, causal, G, split)) {
-            std::printf("FAILED N=%d Nkv=%d BH=%d causal=%d G/sms=%d split=%d plan=%d\n", N, Nkv, BH, causal, G, split,
-                        (int)plan);
+        if (plan ? check_plan(N, Nkv, BH, causal, G, wl, wr) : check(N, Nkv, BH, causal, G, split, wl, wr)) {
+            std::printf("FAILED N=%d Nkv=%d BH=%d causal=%d G/sms=%d split=%d plan=%d wl=%d wr=%d\n", N, Nkv, BH, causal, G,
+                        split, (int)plan, wl, wr);
             ++failures;
         }
     }

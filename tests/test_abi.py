@@ -128,3 +128,23 @@ def test_qkv_invalid_arguments_rejected(lib):
                             0, None)
         assert rc == INVALID, (nq, nkv, rc)
 
+
+
+def test_band_arguments(lib):
+    """fa_fwd_band validates its sizes like fa_fwd_qkv; any window bound is
+    valid (a negative one is unbounded), so sound sizes reach the device check."""
+    import ctypes
+    a = GOOD
+    for nq, nkv in ((0, 16), (16, 0), (-1, 16)):
+        rc = lib.fa_fwd_band(a["q"], a["k"], a["v"], a["o"], a["lse"], 1, 2, nq, nkv, 64, 3, 0,
+                             ctypes.c_float(0.125), 0, 0, None)
+        assert rc == INVALID, (nq, nkv, rc)
+    rc = lib.fa_fwd_band(a["q"], a["k"], a["v"], a["o"], a["lse"], 1, 2, 16, 16, 64, 3, 0, ctypes.c_float(0.0), 0, 0,
+                         None)
+    assert rc == INVALID
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        for window in ((-1, -1), (-1, 0), (0, 0), (5, -7), (1 << 30, 1 << 30)):
+            rc = lib.fa_fwd_band(a["q"], a["k"], a["v"], a["o"], a["lse"], 1, 2, 16, 300, 64, window[0], window[1],
+                                 ctypes.c_float(0.125), 0, 0, None)
+            assert rc == UNSUPPORTED, (window, rc)

@@ -20,7 +20,7 @@ for N in (1, 2, 127, 128, 129, 255, 256, 257, 383, 513, 1024, 3000, 4096, 16384,
                 for split in (0, 1):
                     if N * BH > 64 * 4096 and G != 152:
                         continue
-                    CASES.append((N, N, BH, causal, G, split))
+                    CASES.append((N, N, BH, causal, G, split, -1, 0))
 # queries against a different number of keys: decode, cross attention, and
 # Nq > Nkv (causal rows that see no key)
 for N, Nkv in ((1, 4096), (16, 8192), (64, 3000), (127, 1000), (200, 70), (513, 200), (300, 1), (1000, 129)):
@@ -28,7 +28,15 @@ for N, Nkv in ((1, 4096), (16, 8192), (64, 3000), (127, 1000), (200, 70), (513, 
         for causal in (0, 1):
             for G in (1, 7, 152):
                 for split in (0, 1):
-                    CASES.append((N, Nkv, BH, causal, G, split))
+                    CASES.append((N, Nkv, BH, causal, G, split, -1, 0))
+# band (sliding-window) masks: windows narrower and wider than a step, two-sided
+for N, Nkv in ((1000, 1000), (4096, 4096), (300, 2000), (2000, 300), (1, 4096), (129, 129), (257, 5000)):
+    for wl, wr in ((0, 0), (127, 0), (128, 0), (1000, 0), (64, 64), (300, -1), (5, 700), (0, 5), (4095, 0),
+                   (-1, 128), (1 << 29, 3)):
+        for BH in (1, 7):
+            for G in (7, 152):
+                for split in (0, 1):
+                    CASES.append((N, Nkv, BH, 1, G, split, wl, wr))
 
 
 @pytest.fixture(scope="module")
@@ -47,11 +55,16 @@ for N in (1, 2, 100, 256, 257, 513, 1000, 1024, 2048, 3000, 4096, 8192, 16384, 3
             for sms in (148, 152):
                 if N * BH > 64 * 16384:
                     continue
-                PLAN_CASES.append((N, N, BH, causal, sms))
+                PLAN_CASES.append((N, N, BH, causal, sms, -1, 0))
 for N, Nkv in ((1, 32768), (4, 131072), (64, 16384), (128, 4096), (513, 200), (4096, 64)):
     for BH in (1, 8, 32, 128):
         for causal in (0, 1):
-            PLAN_CASES.append((N, Nkv, BH, causal, 152))
+            PLAN_CASES.append((N, Nkv, BH, causal, 152, -1, 0))
+for N, Nkv, wl, wr in ((32768, 32768, 4096, 0), (8192, 8192, 255, 0), (1, 131072, 8192, 0), (4096, 4096, 512, 512),
+                       (1500, 1500, 300, -1), (8192, 8192, 1000, -1), (3000, 3000, -1, 200), (4, 65536, 8191, 0),
+                       (300, 2000, 511, 0), (513, 200, 50, 10)):
+    for BH in (1, 3, 32):
+        PLAN_CASES.append((N, Nkv, BH, 1, 152, wl, wr))
 
 
 def test_schedule_planner(checker):
