@@ -53,6 +53,9 @@ def _load(path: str | None = None):
     lib.attn_ref_forward_band.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] + [ctypes.c_long] * 6 + [
         ctypes.c_double, c_double_p, c_double_p]
     lib.attn_ref_forward_band.restype = ctypes.c_int
+    lib.attn_ref_backward_band.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_long] * 6 + [
+        ctypes.c_double] + [c_double_p] * 4
+    lib.attn_ref_backward_band.restype = ctypes.c_int
     lib.attn_ref_rows.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_long, ctypes.c_long,
                                                          ctypes.c_long, ctypes.c_int, ctypes.c_double,
                                                          c_long_p, c_long_p, ctypes.c_long, c_double_p, c_double_p]
@@ -184,6 +187,40 @@ def forward_band(q, k, v, left: int, right: int, scale: float, lib=None):
     if rc != 0:
         raise MemoryError("oracle forward failed to allocate scratch")
     return O, L
+
+
+def backward_band(q, k, v, do, left: int, right: int, scale: float, with_delta: bool = False, lib=None):
+    """Gradients of the band-masked attention of ``forward_band`` for the
+    upstream gradient ``do`` (shape of O): returns float64 (dQ, dK, dV), and
+    delta = rowsum(P * dP) [..., Nq] as a fourth item if ``with_delta``."""
+    qa, dt = _as_input(q)
+    ka, dtk = _as_input(k)
+    va, dtv = _as_input(v)
+    da, dtd = _as_input(do)
+    if not (dt == dtk == dtv == dtd):
+        raise TypeError("q, k, v, do must share a dtype")
+    if (ka.shape != va.shape or da.shape != qa.shape or qa.ndim < 2 or qa.shape[:-2] != ka.shape[:-2]
+            or qa.shape[-1] != ka.shape[-1]):
+        raise ValueError("q, do [..., Nq, D] and k, v [..., Nkv, D] must agree")
+    Nq, Nkv, D = qa.shape[-2], ka.shape[-2], qa.shape[-1]
+    BH = int(np.prod(qa.shape[:-2])) if qa.ndim > 2 else 1
+    dQ = np.empty(qa.shape, dtype=np.float64)
+    dK = np.empty(ka.shape, dtype=np.float64)
+    dV = np.empty(ka.shape, dtype=np.float64)
+    delta = np.empty(qa.shape[:-1], dtype=np.float64)
+    rc = (lib or _load()).attn_ref_backward_band(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), _DTYPE_CODE[dt], BH, Nq,
+                                                 Nkv, D, int(left), int(right), _scale_as_double(scale),
+                                                 _ptr(dQ, ctypes.c_double), _ptr(dK, ctypes.c_double),
+                                                 _ptr(dV, ctypes.c_double), _ptr(delta, ctypes.c_double))
+    if rc != 0:
+        raise MemoryError("oracle backward failed to allocate scratch")
+    return (dQ, dK, dV, delta) if with_delta else (dQ, dK, dV)
+
+
+def backward(q, k, v, do, causal: bool, scale: float, lib=None):
+    """Gradients (dQ, dK, dV) of the square attention of ``forward``
+    (bottom-right causal when Nq != Nkv): the band (unbounded, 0) or none."""
+    return backward_band(q, k, v, do, -1, 0 if causal else -1, scale, lib=lib)
 
 
 def rows(q, k, v, causal: bool, scale: float, bh_idx, row_idx, lib=None):

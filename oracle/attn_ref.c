@@ -46,6 +46,9 @@
  * (unbounded, 0) and no mask is (unbounded, unbounded); a row whose band holds
  * no key gets O = 0 and LSE = -inf.
  *
+ * attn_ref_backward_band() gives the gradients of that attention for an
+ * upstream gradient dO (the same band mask; see its comment).
+ *
  * Besides the explicit definition, attn_ref_tiled() runs the tiled online-
  * softmax recurrence in fp64, step by step in the order the pages give it, so
  * the tests can show that the recurrence equals the definition on small
@@ -301,6 +304,146 @@ int attn_ref_forward_band(const void *Q, const void *K, const void *V, int dtype
         }
     }
     free(Kh); free(Vh); free(Qh);
+    return failed ? -1 : 0;
+}
+
+/*
+ * Gradients of O = softmax(S) V, S = s Q K^T under the band mask of
+ * attn_ref_forward_band, for an upstream gradient dO (same shape as O).  With
+ * J_i the keys query i sees and L_i its log-sum-exp:
+ *
+ *   P[i,j]  = exp(s q_i.k_j - L_i)             for j in J_i, else 0
+ *   dV[j,:] = sum_i P[i,j] dO[i,:]
+ *   dP[i,j] = dO[i,:] . V[j,:]
+ *   delta_i = sum_j P[i,j] dP[i,j]
+ *   dS[i,j] = P[i,j] (dP[i,j] - delta_i)       (the softmax's Jacobian applied to dP)
+ *   dQ[i,:] = s sum_j dS[i,j] K[j,:]
+ *   dK[j,:] = s sum_i dS[i,j] Q[i,:]
+ *
+ * These are the chain rule through the definition, written out; the pages
+ * name the backward's ingredients rather than its formulas ("FlashAttention 2
+ * from PyTorch to Triton", What I am building: P is recovered as exp(S - L)
+ * from the saved L; and its list of limitations: a precomputed
+ * D = rowsum(dO o O), which equals delta_i here, since
+ * dO_i . O_i = sum_j P[i,j] dO_i . V_j).  A row that sees no key has P = 0:
+ * its dQ row is 0 and it adds nothing to dK or dV.
+ *
+ * Q, dO are [BH, Nq, D]; K, V are [BH, Nkv, D]; outputs are float64:
+ * dQ [BH, Nq, D], dK and dV [BH, Nkv, D], and DELTA [BH, Nq] if not NULL.
+ * Two passes per head: over query rows (L_i, delta_i, dQ_i), then over key
+ * rows (dK_j, dV_j), each recomputing the P and dP entries it needs, so no
+ * Nq x Nkv matrix is stored.  Returns 0, or -1 if a scratch allocation failed.
+ */
+static void band_range(long i, long Nq, long Nkv, long left, long right, long *lo, long *hi)
+{
+    const long ii = i + Nkv - Nq;   /* the query's position among the keys */
+    long a = left < 0 ? 0 : ii - left, b = right < 0 ? Nkv - 1 : ii + right;
+    if (a < 0)
+        a = 0;
+    if (b > Nkv - 1)
+        b = Nkv - 1;
+    *lo = a;
+    *hi = b;   /* keys a .. b; none if b < a */
+}
+
+static double dot_d(const double *a, const double *b, long D)
+{
+    double acc = 0.0;
+    for (long d = 0; d < D; ++d)
+        acc += a[d] * b[d];
+    return acc;
+}
+
+int attn_ref_backward_band(const void *Q, const void *K, const void *V, const void *dO, int dtype,
+                           long BH, long Nq, long Nkv, long D, long left, long right, double s,
+                           double *dQ, double *dK, double *dV, double *DELTA)
+{
+    size_t qslice = (size_t)Nq * (size_t)D, kslice = (size_t)Nkv * (size_t)D;
+    double *Kh = (double *)malloc(kslice * sizeof(double));
+    double *Vh = (double *)malloc(kslice * sizeof(double));
+    double *Qh = (double *)malloc(qslice * sizeof(double));
+    double *dOh = (double *)malloc(qslice * sizeof(double));
+    double *Lr = (double *)malloc((size_t)Nq * sizeof(double));
+    double *Dr = (double *)malloc((size_t)Nq * sizeof(double));
+    if (!Kh || !Vh || !Qh || !dOh || !Lr || !Dr) {
+        free(Kh); free(Vh); free(Qh); free(dOh); free(Lr); free(Dr);
+        return -1;
+    }
+    int failed = 0;
+    for (long bh = 0; bh < BH; ++bh) {
+        load_slice(Q, dtype, (size_t)bh * qslice, Nq, D, Qh);
+        load_slice(dO, dtype, (size_t)bh * qslice, Nq, D, dOh);
+        load_slice(K, dtype, (size_t)bh * kslice, Nkv, D, Kh);
+        load_slice(V, dtype, (size_t)bh * kslice, Nkv, D, Vh);
+        double *dQh = dQ + (size_t)bh * qslice, *dKh = dK + (size_t)bh * kslice, *dVh = dV + (size_t)bh * kslice;
+        /* Pass 1, query rows: L_i, delta_i, dQ_i. */
+#pragma omp parallel
+        {
+            double *x = (double *)malloc((size_t)Nkv * sizeof(double));
+            if (!x) {
+#pragma omp atomic write
+                failed = 1;
+            } else {
+#pragma omp for schedule(dynamic, 8)
+                for (long i = 0; i < Nq; ++i) {
+                    long lo, hi;
+                    band_range(i, Nq, Nkv, left, right, &lo, &hi);
+                    double *dq = dQh + (size_t)i * D;
+                    for (long d = 0; d < D; ++d)
+                        dq[d] = 0.0;
+                    if (hi < lo) {   /* no key: P = 0 */
+                        Lr[i] = -INFINITY;
+                        Dr[i] = 0.0;
+                        continue;
+                    }
+                    double m = -INFINITY;
+                    for (long j = lo; j <= hi; ++j) {
+                        x[j] = s * dot_d(Qh + i * D, Kh + j * D, D);
+                        if (x[j] > m)
+                            m = x[j];
+                    }
+                    double l = 0.0;
+                    for (long j = lo; j <= hi; ++j)
+                        l += exp(x[j] - m);
+                    const double L = m + log(l);
+                    double delta = 0.0;
+                    for (long j = lo; j <= hi; ++j)
+                        delta += exp(x[j] - L) * dot_d(dOh + i * D, Vh + j * D, D);
+                    for (long j = lo; j <= hi; ++j) {
+                        const double p = exp(x[j] - L);
+                        const double ds = p * (dot_d(dOh + i * D, Vh + j * D, D) - delta);
+                        for (long d = 0; d < D; ++d)
+                            dq[d] += s * ds * Kh[j * D + d];
+                    }
+                    Lr[i] = L;
+                    Dr[i] = delta;
+                }
+            }
+            free(x);
+        }
+        /* Pass 2, key rows: dK_j, dV_j over the queries that see key j. */
+#pragma omp parallel for schedule(dynamic, 8)
+        for (long j = 0; j < Nkv; ++j) {
+            double *dk = dKh + (size_t)j * D, *dv = dVh + (size_t)j * D;
+            for (long d = 0; d < D; ++d)
+                dk[d] = dv[d] = 0.0;
+            for (long i = 0; i < Nq; ++i) {
+                long lo, hi;
+                band_range(i, Nq, Nkv, left, right, &lo, &hi);
+                if (j < lo || j > hi)
+                    continue;
+                const double p = exp(s * dot_d(Qh + i * D, Kh + j * D, D) - Lr[i]);
+                const double ds = p * (dot_d(dOh + i * D, Vh + j * D, D) - Dr[i]);
+                for (long d = 0; d < D; ++d) {
+                    dv[d] += p * dOh[i * D + d];
+                    dk[d] += s * ds * Qh[i * D + d];
+                }
+            }
+        }
+        if (DELTA)
+            memcpy(DELTA + (size_t)bh * Nq, Dr, (size_t)Nq * sizeof(double));
+    }
+    free(Kh); free(Vh); free(Qh); free(dOh); free(Lr); free(Dr);
     return failed ? -1 : 0;
 }
 

@@ -5,7 +5,8 @@ temporary library.  The pins of ``test_oracle_pins.py`` are rerun against it;
 at least one must fail.  This shows the pins constrain every part of the
 oracle: the scale, the causal index, the operands, the normalisation, the
 LSE's log base and shift, the rescale direction of the recurrence, its causal
-loop bound, and the bf16/fp16 decoders.  No mutant indexes outside its arrays.
+loop bound, the bf16/fp16 decoders, and the backward's terms (delta, scales,
+operands, normalisation, band).  No mutant indexes outside its arrays.
 """
 from __future__ import annotations
 
@@ -36,6 +37,18 @@ MUTANTS = {
     "tiled_no_acc_rescale": ("acc[r * D + d] = alpha * acc[r * D + d] + pv;", "acc[r * D + d] = acc[r * D + d] + pv;"),
     "tiled_skips_diagonal": ("hi = (q0 + BM < N) ? q0 + BM : N;", "hi = q0;"),
     "tiled_no_key_mask": ("if (kj >= N || (causal && kj > qi)) {", "if (kj >= N) {"),
+    "bwd_dq_drops_delta": ("const double ds = p * (dot_d(dOh + i * D, Vh + j * D, D) - delta);",
+                           "const double ds = p * (dot_d(dOh + i * D, Vh + j * D, D) - 0.0);"),
+    "bwd_dk_drops_delta": ("const double ds = p * (dot_d(dOh + i * D, Vh + j * D, D) - Dr[i]);",
+                           "const double ds = p * (dot_d(dOh + i * D, Vh + j * D, D) - 0.0);"),
+    "bwd_dk_no_scale": ("dk[d] += s * ds * Qh[i * D + d];", "dk[d] += ds * Qh[i * D + d];"),
+    "bwd_dv_uses_ds": ("dv[d] += p * dOh[i * D + d];", "dv[d] += ds * dOh[i * D + d];"),
+    "bwd_dq_uses_v": ("dq[d] += s * ds * Kh[j * D + d];", "dq[d] += s * ds * Vh[j * D + d];"),
+    "bwd_p_unnormalised": ("            const double p = exp(x[j] - L);", "            const double p = exp(x[j] - m);"),
+    "bwd_delta_uses_k": ("delta += exp(x[j] - L) * dot_d(dOh + i * D, Vh + j * D, D);",
+                         "delta += exp(x[j] - L) * dot_d(dOh + i * D, Kh + j * D, D);"),
+    "bwd_keys_ignore_band": ("                if (j < lo || j > hi)\n                    continue;",
+                             "                if (j < 0)\n                    continue;"),
     "bf16_shift": ("uint32_t u = ((uint32_t)h) << 16;", "uint32_t u = ((uint32_t)h) << 15;"),
     "fp16_bias": ("v = ldexp((double)(f + 1024), e - 25);", "v = ldexp((double)(f + 1024), e - 24);"),
 }

@@ -316,10 +316,119 @@ def pin_band_closed_forms(lib):
         assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
 
 
+# --- backward -----------------------------------------------------------------
+
+BWD_SHAPES = ((5, 5, -1, -1), (5, 5, -1, 0), (4, 7, 2, 1), (6, 3, -1, 0), (7, 7, 1, 1))   # (Nq, Nkv, left, right)
+
+
+def pin_backward_finite_differences(lib):
+    """The gradients of loss = sum(O * dO) by central differences of the
+    oracle's own (separately pinned) forward, element by element, on tiny fp64
+    inputs: unmasked, causal, a band with Nq != Nkv, rows that see no key, and
+    a two-sided band.  Pins every term of the backward without restating it."""
+    h = 1e-6
+    for n, (Nq, Nkv, left, right) in enumerate(BWD_SHAPES):
+        D = 3
+        q, k, v = _rand((2, Nq, D), 71 + n), _rand((2, Nkv, D), 81 + n), _rand((2, Nkv, D), 91 + n)
+        do = _rand((2, Nq, D), 101 + n)
+        dq, dk, dv = oracle.backward_band(q, k, v, do, left, right, 0.5, lib=lib)
+
+        def loss(qq, kk, vv):
+            O, _ = oracle.forward_band(qq, kk, vv, left, right, 0.5, lib=lib)
+            return float((O * do).sum())
+
+        for x, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+            num = np.empty_like(x)
+            for idx in np.ndindex(*x.shape):
+                args = [q.copy(), k.copy(), v.copy()]
+                args[which][idx] += h
+                up = loss(*args)
+                args[which][idx] -= 2 * h
+                num[idx] = (up - loss(*args)) / (2 * h)
+            assert np.allclose(g, num, rtol=0, atol=1e-7), (Nq, Nkv, left, right, which, float(np.abs(g - num).max()))
+
+
+def _band_autograd(q, k, v, do, left, right, s):
+    """PyTorch fp64 autograd through softmax(s Q K^T) V under an explicit band
+    mask (rows that see no key give O = 0)."""
+    q, k, v = (torch.from_numpy(x).clone().requires_grad_(True) for x in (q, k, v))
+    Nq, Nkv = q.shape[-2], k.shape[-2]
+    ii = torch.arange(Nq).unsqueeze(1) + (Nkv - Nq)
+    j = torch.arange(Nkv).unsqueeze(0)
+    hide = torch.zeros(Nq, Nkv, dtype=torch.bool)
+    if left >= 0:
+        hide |= j < ii - left
+    if right >= 0:
+        hide |= j > ii + right
+    empty = hide.all(dim=-1, keepdim=True)
+    S = (s * (q @ k.transpose(-1, -2))).masked_fill(hide, float("-inf")).masked_fill(empty, 0.0)
+    O = (torch.softmax(S, dim=-1) @ v).masked_fill(empty, 0.0)
+    O.backward(torch.from_numpy(do))
+    return q.grad.numpy(), k.grad.numpy(), v.grad.numpy()
+
+
+def pin_backward_vs_torch_autograd(lib):
+    """dQ, dK, dV equal PyTorch's fp64 autograd through the explicit softmax
+    formula (an independent route), for unmasked, causal, band, Nq != Nkv and
+    empty-row cases at moderate sizes."""
+    for n, (Nq, Nkv, left, right) in enumerate(((33, 33, -1, -1), (33, 33, -1, 0), (40, 70, 9, 3), (70, 40, 0, 0),
+                                                (50, 20, 2, 0), (16, 300, 100, -1))):
+        q, k, v = _rand((2, Nq, 8), 111 + n), _rand((2, Nkv, 8), 121 + n), _rand((2, Nkv, 8), 131 + n)
+        do = _rand((2, Nq, 8), 141 + n)
+        got = oracle.backward_band(q, k, v, do, left, right, 0.5, lib=lib)
+        ref = _band_autograd(q, k, v, do, left, right, 0.5)
+        for a, b in zip(got, ref):
+            assert np.allclose(a, b, rtol=0, atol=1e-12), (Nq, Nkv, left, right, float(np.abs(a - b).max()))
+
+
+def pin_backward_invariants(lib):
+    """Each row of dS = P (dP - delta) sums to zero, so the key rows of dK sum
+    to zero; each visible row of P sums to one, so the key rows of dV sum to the
+    dO rows of queries that see a key.  (bf16 inputs, causal and band masks.)"""
+    from exact_attention_10_gb300.inputs import make_custom
+    for (Nq, Nkv, left, right) in ((64, 64, -1, 0), (40, 70, 7, 3), (70, 40, -1, 0)):
+        q = make_custom(1, 2, Nq, 16, "bf16", seed=Nq)[0]
+        _, k, v = make_custom(1, 2, Nkv, 16, "bf16", seed=Nkv + 1)
+        do = make_custom(1, 2, Nq, 16, "bf16", seed=Nq + 2)[0]
+        dq, dk, dv = oracle.backward_band(q, k, v, do, left, right, 0.25, lib=lib)
+        _, L = oracle.forward_band(q, k, v, left, right, 0.25, lib=lib)
+        seen = ~np.isneginf(L)
+        dod = oracle.decode(do.view(torch.int16).numpy().view(np.uint16), "bf16", lib=lib).reshape(do.shape)
+        assert np.allclose(dk.sum(axis=-2), 0.0, rtol=0, atol=1e-12)
+        assert np.allclose(dv.sum(axis=-2), (dod * seen[..., None]).sum(axis=-2), rtol=0, atol=1e-12)
+        assert (dq[~seen] == 0).all()
+
+
+def pin_backward_constant_v(lib):
+    """With every V row equal, O does not depend on Q or K: dQ = dK = 0, and
+    dV = P^T dO with P from the oracle's (separately pinned) probabilities."""
+    N, D = 24, 5
+    q, k = _rand((1, N, D), 151), _rand((1, N, D), 152)
+    v = np.repeat(_rand((1, 1, D), 153), N, axis=1)
+    do = _rand((1, N, D), 154)
+    for causal in (False, True):
+        dq, dk, dv = oracle.backward(q, k, v, do, causal, 0.5, lib=lib)
+        assert np.allclose(dq, 0.0, rtol=0, atol=1e-13) and np.allclose(dk, 0.0, rtol=0, atol=1e-13)
+        P = oracle.probs(q[0], k[0], causal, 0.5, lib=lib)
+        assert np.allclose(dv[0], P.T @ do[0], rtol=0, atol=1e-13)
+
+
+def pin_backward_delta_is_rowsum_do_o(lib):
+    """The softmax Jacobian's delta_i = sum_j P_ij dP_ij equals the pages'
+    D = rowsum(dO o O) with O from the oracle's forward."""
+    for (Nq, Nkv, left, right) in ((33, 33, -1, 0), (40, 70, 9, 3), (70, 40, 0, 0)):
+        q, k, v = _rand((2, Nq, 8), 161), _rand((2, Nkv, 8), 162), _rand((2, Nkv, 8), 163)
+        do = _rand((2, Nq, 8), 164)
+        *_, delta = oracle.backward_band(q, k, v, do, left, right, 0.5, with_delta=True, lib=lib)
+        O, _ = oracle.forward_band(q, k, v, left, right, 0.5, lib=lib)
+        assert np.allclose(delta, (do * O).sum(axis=-1), rtol=0, atol=1e-12)
+
+
 PINS = [pin_decode, pin_rows_sum_to_one, pin_probs_vs_scipy, pin_constant_v, pin_identical_keys,
         pin_zero_query, pin_causal_row0, pin_one_hot, pin_vs_torch_sdpa, pin_tiled_equals_explicit,
         pin_unbalanced_magnitudes, pin_first_step_rescale, pin_qkv_vs_torch, pin_qkv_is_the_suffix_of_square_causal,
-        pin_band_vs_torch, pin_band_closed_forms]
+        pin_band_vs_torch, pin_band_closed_forms, pin_backward_finite_differences, pin_backward_vs_torch_autograd,
+        pin_backward_invariants, pin_backward_constant_v, pin_backward_delta_is_rowsum_do_o]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
