@@ -1,11 +1,11 @@
 """Build the CUDA library (libfa_gb300.so) in-tree with nvcc for sm_103a.
 
-Three translation units, compiled in parallel and linked into one shared
+Four translation units, compiled in parallel and linked into one shared
 library: csrc/fa_api.cu (the C ABI and the whole-tile kernel variants without
 a mask or with the causal one), csrc/fa_split.cu (the same for the balanced
-schedule) and csrc/fa_band.cu (left-bounded band masks, both schedules), so
-the build stays quick on both the x86_64 build machine and the aarch64 GPU
-host.
+schedule), csrc/fa_band.cu (left-bounded band masks, both schedules) and
+csrc/fa_bwd.cu (the backward), so the build stays quick on both the x86_64
+build machine and the aarch64 GPU host.
 The runtime is linked statically and the driver's tensor-map encoder is
 resolved at run time, so the library loads on a machine without a GPU driver
 (its compute calls then return FA_ERR_UNSUPPORTED_DEVICE).
@@ -18,7 +18,7 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRCS = [os.path.join(PKG, "csrc", f) for f in ("fa_api.cu", "fa_split.cu", "fa_band.cu")]
+SRCS = [os.path.join(PKG, "csrc", f) for f in ("fa_api.cu", "fa_split.cu", "fa_band.cu", "fa_bwd.cu")]
 LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -15,6 +15,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "fa_bwd_launch.h"
 #include "fa_launch.cuh"
 
 namespace {
@@ -182,6 +183,49 @@ fa_status workspace_for(int dev, cudaStream_t stream, const fa::Schedule &sc, in
     return FA_OK;
 }
 
+// Per-(device, stream) scratch of the backward: lg and delta per query row,
+// [B*H][Npad] fp32 each.  Grown like the forward's workspace; calls on one
+// stream reuse it in stream order.
+struct BwdWorkspace {
+    int dev;
+    cudaStream_t stream;
+    void *ptr;
+    size_t bytes;
+};
+BwdWorkspace g_bws[kMaxWorkspaces];
+int g_bws_count = 0;
+
+void *bwd_workspace(int dev, cudaStream_t stream, size_t need)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    BwdWorkspace *w = nullptr;
+    for (int i = 0; i < g_bws_count; ++i)
+        if (g_bws[i].dev == dev && g_bws[i].stream == stream)
+            w = &g_bws[i];
+    if (!w) {
+        if (g_bws_count == kMaxWorkspaces)
+            return nullptr;
+        w = &g_bws[g_bws_count++];
+        *w = BwdWorkspace{dev, stream, nullptr, 0};
+    }
+    if (w->bytes < need) {
+        if (w->ptr) {
+            if (cudaStreamSynchronize(stream) != cudaSuccess || cudaFree(w->ptr) != cudaSuccess) {
+                cudaGetLastError();
+                return nullptr;
+            }
+            w->ptr = nullptr;
+            w->bytes = 0;
+        }
+        if (cudaMalloc(&w->ptr, need) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        w->bytes = need;
+    }
+    return w->ptr;
+}
+
 }  // namespace
 
 namespace fa_launch {
@@ -328,17 +372,99 @@ extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O
     return fa_fwd_ex(Q, K, V, O, LSE, B, H, N, D, causal, scale, dtype, FA_SCHEDULE_AUTO, stream);
 }
 
+extern "C" fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                            const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D, int causal,
+                            float scale, fa_dtype dtype, fa_stream_t stream)
+{
+    // Arguments first: nothing below touches the device until they are sound.
+    if (dtype != FA_BF16 && dtype != FA_FP16)
+        return FA_ERR_INVALID_VALUE;
+    if (D != 64 && D != 128)
+        return FA_ERR_INVALID_VALUE;
+    if (B < 1 || H < 1 || N < 1 || (causal != 0 && causal != 1))
+        return FA_ERR_INVALID_VALUE;
+    if (!std::isfinite(scale) || !(scale > 0.f))
+        return FA_ERR_INVALID_VALUE;
+    const long long BH = (long long)B * H;
+    const long long Npad = ((long long)N + 127) / 128 * 128;
+    if (BH * Npad >= (1ll << 31))
+        return FA_ERR_INVALID_VALUE;
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV)
+        return FA_ERR_INVALID_VALUE;
+    const uintptr_t any = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                          reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
+                          reinterpret_cast<uintptr_t>(dO) | reinterpret_cast<uintptr_t>(LSE) |
+                          reinterpret_cast<uintptr_t>(dQ) | reinterpret_cast<uintptr_t>(dK) |
+                          reinterpret_cast<uintptr_t>(dV);
+    if (any & 15u)
+        return FA_ERR_MISALIGNED;
+    const size_t tbytes = (size_t)BH * N * D * 2, lbytes = (size_t)BH * N * sizeof(float);
+    const void *ins[6] = {Q, K, V, O, dO, LSE};
+    const size_t in_bytes[6] = {tbytes, tbytes, tbytes, tbytes, tbytes, lbytes};
+    void *outs[3] = {dQ, dK, dV};
+    for (int o = 0; o < 3; ++o) {   // outputs overlap no input and no other output
+        for (int i = 0; i < 6; ++i)
+            if (ranges_overlap(outs[o], tbytes, ins[i], in_bytes[i]))
+                return FA_ERR_INVALID_VALUE;
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (ranges_overlap(outs[o], tbytes, outs[o2], tbytes))
+                return FA_ERR_INVALID_VALUE;
+    }
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_UNSUPPORTED_DEVICE;
+    }
+    const DeviceInfo *di = device_info(dev);
+    if (!di || !di->supported)
+        return FA_ERR_UNSUPPORTED_DEVICE;
+    for (int i = 0; i < 6; ++i)
+        if (!is_device_pointer(ins[i], dev))
+            return FA_ERR_INVALID_VALUE;
+    for (int o = 0; o < 3; ++o)
+        if (!is_device_pointer(outs[o], dev))
+            return FA_ERR_INVALID_VALUE;
+
+    const bool bf16 = dtype == FA_BF16;
+    fa_launch::BwdLaunch a{};
+    if (!encode_map(&a.tq, Q, (int)BH, N, D, bf16) || !encode_map(&a.tk, K, (int)BH, N, D, bf16) ||
+        !encode_map(&a.tv, V, (int)BH, N, D, bf16) || !encode_map(&a.tdo, dO, (int)BH, N, D, bf16))
+        return FA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float *ws = static_cast<float *>(bwd_workspace(dev, s, (size_t)2 * BH * Npad * sizeof(float)));
+    if (!ws)
+        return FA_ERR_CUDA;
+    a.O = O;
+    a.dO = dO;
+    a.LSE = LSE;
+    a.dQ = dQ;
+    a.dK = dK;
+    a.dV = dV;
+    a.lg = ws;
+    a.dl = ws + BH * Npad;
+    a.BH = (int)BH;
+    a.N = N;
+    a.Npad = (int)Npad;
+    a.D = D;
+    a.sms = di->sms;
+    a.bf16 = bf16;
+    a.causal = causal != 0;
+    a.scale = scale;
+    return fa_launch::launch_bwd(a, s, dev);
+}
+
 extern "C" fa_status fa_sync_status(fa_stream_t stream)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return FA_ERR_CUDA;
     }
-    unsigned int w_whole = 0, w_split = 0, w_band = 0;
+    unsigned int w_whole = 0, w_split = 0, w_band = 0, w_bwd = 0;
     if (!fa_launch::take_status_word_whole(&w_whole) || !fa_launch::take_status_word_split(&w_split) ||
-        !fa_launch::take_status_word_band(&w_band))
+        !fa_launch::take_status_word_band(&w_band) || !fa_launch::take_status_word_bwd(&w_bwd))
         return FA_ERR_CUDA;
-    if ((w_whole | w_split | w_band) != 0) {
+    if ((w_whole | w_split | w_band | w_bwd) != 0) {
         // an aborted launch may have left split-tile counters non-zero
         int dev = -1;
         cudaGetDevice(&dev);

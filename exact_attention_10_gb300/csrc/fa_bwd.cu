@@ -1,0 +1,102 @@
+// fa_bwd.cu -- the backward kernels (fa_bwd_kernel.cuh) and their launch:
+// the per-row pre-pass, then the dQ pass and the dK/dV pass on one stream.
+#include "fa_bwd_launch.h"
+
+#include <mutex>
+
+#include "fa_bwd_kernel.cuh"
+
+namespace fa_launch {
+
+namespace {
+
+constexpr int kMaxDev = 64;
+
+template <int D, bool BF16, bool CAUSAL, bool KV>
+fa_status launch_pass(const CUtensorMap &r0, const CUtensorMap &r1, const CUtensorMap &s0, const CUtensorMap &s1,
+                      const fa::bwd::Params &p, int grid, cudaStream_t stream, int dev)
+{
+    static std::mutex mu;
+    static bool attr_set[kMaxDev] = {};
+    auto kern = fa::bwd::fa_bwd_sm103<D, BF16, CAUSAL, KV>;
+    constexpr int smem = fa::bwd::BCfg<D, KV>::kSmem;
+    if (dev < 0 || dev >= kMaxDev)
+        return FA_ERR_UNSUPPORTED_DEVICE;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+                cudaGetLastError();
+                return FA_ERR_CUDA;
+            }
+            attr_set[dev] = true;
+        }
+    }
+    kern<<<grid, fa::bwd::kThreads, smem, stream>>>(r0, r1, s0, s1, p);
+    if (cudaGetLastError() != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+fa_status launch_all(const BwdLaunch &a, cudaStream_t s, int dev)
+{
+    const long long rows = (long long)a.BH * a.Npad;
+    const long long threads = rows * (D / 8);
+    fa::bwd::fa_bwd_prep<D, BF16><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+        static_cast<const uint16_t *>(a.O), static_cast<const uint16_t *>(a.dO), a.LSE, a.lg, a.dl, a.N, a.Npad, rows);
+    if (cudaGetLastError() != cudaSuccess)
+        return FA_ERR_CUDA;
+    fa::bwd::Params p{};
+    p.lg = a.lg;
+    p.dl = a.dl;
+    p.N = a.N;
+    p.Npad = a.Npad;
+    p.BH = a.BH;
+    p.nt = a.Npad / fa::bwd::kTile;
+    p.T = a.BH * p.nt;
+    p.qk2 = a.scale * 1.4426950408889634f;
+    p.scale = a.scale;
+    const int grid = p.T < a.sms ? p.T : a.sms;
+    p.dA = a.dQ;
+    p.dB = nullptr;
+    fa_status st = launch_pass<D, BF16, CAUSAL, false>(a.tq, a.tdo, a.tk, a.tv, p, grid, s, dev);
+    if (st != FA_OK)
+        return st;
+    p.dA = a.dK;
+    p.dB = a.dV;
+    return launch_pass<D, BF16, CAUSAL, true>(a.tk, a.tv, a.tq, a.tdo, p, grid, s, dev);
+}
+
+}  // namespace
+
+fa_status launch_bwd(const BwdLaunch &a, cudaStream_t s, int dev)
+{
+    if (a.D == 64) {
+        if (a.bf16)
+            return a.causal ? launch_all<64, true, true>(a, s, dev) : launch_all<64, true, false>(a, s, dev);
+        return a.causal ? launch_all<64, false, true>(a, s, dev) : launch_all<64, false, false>(a, s, dev);
+    }
+    if (a.bf16)
+        return a.causal ? launch_all<128, true, true>(a, s, dev) : launch_all<128, true, false>(a, s, dev);
+    return a.causal ? launch_all<128, false, true>(a, s, dev) : launch_all<128, false, false>(a, s, dev);
+}
+
+bool take_status_word_bwd(unsigned int *word)
+{
+    *word = 0;
+    if (cudaMemcpyFromSymbol(word, fa::g_status_word, sizeof *word) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (*word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(fa::g_status_word, &zero, sizeof zero) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+    }
+    return true;
+}
+
+}  // namespace fa_launch

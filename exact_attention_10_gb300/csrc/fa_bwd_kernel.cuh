@@ -1,0 +1,597 @@
+// fa_bwd_kernel.cuh -- FlashAttention-2 backward for GB300 (sm_103a).
+//
+// What it computes, for an upstream gradient dO and the forward's O and LSE
+// (per batch*head slice; P recomputed from the saved LSE, never stored):
+//   P[i,j]  = exp(s q_i.k_j - LSE_i)    (0 where the causal mask hides j > i)
+//   delta_i = sum_d dO[i,d] O[i,d]
+//   dS[i,j] = P[i,j] (dO_i.v_j - delta_i)
+//   dV_j = sum_i P[i,j] dO_i,   dK_j = s sum_i dS[i,j] q_i,   dQ_i = s sum_j dS[i,j] k_j
+// ("FlashAttention 2 from PyTorch to Triton", What I am building: the
+// backward recovers P as exp(S - L) from the saved L; its limitations list:
+// a precomputed D = rowsum(dO o O), dK and dV built per key tile by iterating
+// over query tiles, dQ accumulated by atomics or in a second pass.)
+//
+// Three kernels, in stream order:
+//   fa_bwd_prep   per query row: delta = rowsum(dO o O) and lg = LSE * log2(e),
+//                 laid out [B*H][N rounded up to 128], with lg = +inf on the
+//                 padding rows (and rows that see no key) so their P is 0;
+//   fa_bwd_sm103<..., KV = true>   dK, dV: a CTA holds one 128-key tile of K
+//                 and V and streams the query tiles (Q, dO, lg, delta) past it;
+//   fa_bwd_sm103<..., KV = false>  dQ: a CTA holds one 128-row tile of Q and
+//                 dO and streams the key tiles (K, V) past it -- the second
+//                 pass, which keeps dQ deterministic and out of atomics.
+// Both main passes recompute S and dP; that costs two extra tile products
+// per (query tile, key tile) pair over a single pass with atomic dQ.
+//
+// Per (resident tile, streamed tile) step, with M = 128 lanes of TMEM on the
+// resident tile's rows:
+//   KV:  S^T = K Q^T,  dP^T = V dO^T  (tcgen05, both operands K-major in smem)
+//        compute warps: P^T = exp2(S^T * s log2 e - lg), dS^T = P^T (dP^T - delta)
+//        dV += P^T dO,  dK += dS^T Q  (P^T, dS^T from TMEM; dO, Q MN-major)
+//   dQ:  S = Q K^T,  dP = dO V^T;  P = exp2(S * s log2 e - lg), dS = P (dP - delta)
+//        dQ += dS K  (dS from TMEM, K MN-major)
+// The scale s is applied to dK and dQ when they are written out.
+//
+// Warp roles (384 threads): warpgroups 0 and 1 compute (warpgroup h takes
+// columns [64h, 64h + 64) of S and dP for all 128 lanes) and write the
+// accumulators out at the end of a tile; warp 8 is the TMA producer; warp 9
+// issues the MMAs and owns TMEM.
+//
+// Tensor memory (512 columns): S or S^T [0,128), dP or dP^T [128,256), then
+// the accumulators: dV [256, 256+D) and dK [256+D, 256+2D) (KV) or dQ
+// [256, 256+D).  P (KV only) and dS are written as 16-bit pairs over the
+// scores they came from: warpgroup h's 64 columns become 32 columns at
+// 64h within the same region, so neither warpgroup overwrites scores the
+// other still has to read.  MMAs from one thread run in issue order, so the
+// next step's S and dP are issued after the MMAs that read P and dS.
+//
+// Every mbarrier wait is bounded as in the forward kernel; on expiry the
+// kernel records the site in the status word, leaves its loops, waits (with a
+// time bound) for its copies and MMAs in flight, frees TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int kThreads = 384;
+constexpr int kComputeThreads = 256;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kTile = 128;   // rows of a resident or streamed tile (keys or queries)
+
+// Wait sites (status word), after the forward's.
+enum : uint32_t {
+    kSiteBwdResEmpty = 32, kSiteBwdSlotEmpty, kSiteBwdResFull, kSiteBwdSlotFull, kSiteBwdPFull, kSiteBwdAccFree,
+    kSiteBwdSdFull, kSiteBwdAccFull, kSiteBwdDrain, kSiteBwdTail
+};
+
+struct Params {
+    void *dA;          // KV: dK; dQ pass: dQ   ([B*H, N, D], the input type)
+    void *dB;          // KV: dV; dQ pass: unused
+    const float *lg;   // LSE * log2(e) per query row, [B*H][Npad]; +inf on padding rows and rows without keys
+    const float *dl;   // delta = rowsum(dO o O) per query row, [B*H][Npad]
+    int N;             // rows per head (queries = keys)
+    int Npad;          // N rounded up to a multiple of 128
+    int BH;
+    int nt;            // 128-row tiles per head
+    int T;             // work tiles: BH * nt
+    float qk2;         // scale * log2(e)
+    float scale;
+};
+
+template <int D, bool KV>
+struct BCfg {
+    static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kBoxBytes = kTile * 128;     // [128 rows, 64 columns] of 16-bit
+    static constexpr int kTileBytes = kTile * D * 2;
+    static constexpr int kVecBytes = KV ? 2 * kTile * 4 : 0;   // lg and delta of the streamed query tile
+    static constexpr int kStages = (D == 64) ? 3 : 2;
+    static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;   // a multiple of 1024
+    static constexpr int kResOff = 0;                                 // the resident pair of tiles
+    static constexpr int kStageOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    // full[kStages], empty[kStages], res_full, res_empty, sd_full, p_full, acc_full, acc_free, drain
+    static constexpr int kNumBars = 2 * kStages + 7;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;           // TMEM address, abort flag
+    static constexpr int kSmem = kMiscOff + 16 + 1024;                // + slack to align the base to 1024
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+    static_assert(kStageBytes % 1024 == 0, "stages keep the tiles' 1024-byte swizzle alignment");
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+};
+
+template <int D, bool KV>
+struct BBars {
+    uint32_t base;
+    __device__ uint32_t full(int s) const { return base + 8u * s; }
+    __device__ uint32_t empty(int s) const { return base + 8u * (BCfg<D, KV>::kStages + s); }
+    __device__ uint32_t at(int k) const { return base + 8u * (2 * BCfg<D, KV>::kStages + k); }
+    __device__ uint32_t res_full() const { return at(0); }    // TMA -> MMA: resident tiles landed
+    __device__ uint32_t res_empty() const { return at(1); }   // MMA -> TMA: the tile's last MMAs done
+    __device__ uint32_t sd_full() const { return at(2); }     // MMA -> compute: S and dP of a step ready
+    __device__ uint32_t p_full() const { return at(3); }      // compute -> MMA: P / dS written
+    __device__ uint32_t acc_full() const { return at(4); }    // MMA -> compute: a tile's accumulators final
+    __device__ uint32_t acc_free() const { return at(5); }    // compute -> MMA: accumulators read out
+    __device__ uint32_t drain() const { return at(6); }
+};
+
+// Work tile t -> (head, resident tile index), and the streamed tiles it
+// visits, [s0, s0 + n).  Causal: the dK/dV pass's key tile kt sees query
+// tiles kt .. nt-1, the dQ pass's query tile qt sees key tiles 0 .. qt; tiles
+// go longest first, heads interleaved.  Unmasked: head-major.
+template <bool KV>
+__device__ __forceinline__ void bwd_decode(const Params &p, bool causal, int t, int &bh, int &rt, int &s0, int &n)
+{
+    if (causal) {
+        const int g = t / p.BH;
+        bh = t - g * p.BH;
+        rt = KV ? g : p.nt - 1 - g;
+        s0 = KV ? rt : 0;
+        n = KV ? p.nt - rt : rt + 1;
+    } else {
+        bh = t / p.nt;
+        rt = t - bh * p.nt;
+        s0 = 0;
+        n = p.nt;
+    }
+}
+
+// Work tiles of CTA c on a grid of G: serpentine rounds (c-th tile of even
+// rounds, (G-1-c)-th of odd rounds), as in the forward's whole-tile schedule.
+__device__ __forceinline__ int bwd_tile(int r, int c, int G)
+{
+    return r * G + ((r & 1) ? G - 1 - c : c);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// TMEM column of the 16-bit A operand's k-block kk (16 rows of the streamed
+// tile): warpgroup kk / 4 wrote it, 8 columns per block within its 64.
+__device__ __forceinline__ uint32_t a_col(int kk)
+{
+    return (uint32_t)(64 * (kk / 4) + 8 * (kk % 4));
+}
+
+// ------------------------------------------------------------------ producer
+
+template <int D, bool KV>
+__device__ void bwd_load(const CUtensorMap *tmR0, const CUtensorMap *tmR1, const CUtensorMap *tmS0,
+                         const CUtensorMap *tmS1, const Params &p, bool causal, uint32_t sRes, uint32_t sStage,
+                         BBars<D, KV> b, Ctl c)
+{
+    using C = BCfg<D, KV>;
+    int step = 0, tiles = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int t = bwd_tile(r, blockIdx.x, gridDim.x);
+        if (t >= p.T)
+            break;
+        int bh, rt, s0, n;
+        bwd_decode<KV>(p, causal, t, bh, rt, s0, n);
+        if (tiles > 0 && !warp_wait(b.res_empty(), (uint32_t)(tiles - 1) & 1u, c, kSiteBwdResEmpty))
+            break;
+        if (ptx::elect_one()) {
+            ptx::mbar_arrive_expect_tx(b.res_full(), 2 * C::kTileBytes);
+            for (int x = 0; x < C::kBoxes; ++x) {
+                ptx::tma_load_3d(sRes + x * C::kBoxBytes, tmR0, b.res_full(), x * 64, rt * kTile, bh);
+                ptx::tma_load_3d(sRes + C::kTileBytes + x * C::kBoxBytes, tmR1, b.res_full(), x * 64, rt * kTile, bh);
+            }
+        }
+        __syncwarp();
+        ++tiles;
+        for (int j = 0; j < n; ++j, ++step) {
+            const int st = step % C::kStages;
+            const uint32_t use = (uint32_t)(step / C::kStages);
+            if (!warp_wait(b.empty(st), (use & 1u) ^ 1u, c, kSiteBwdSlotEmpty)) {
+                ok = false;
+                break;
+            }
+            const int row = (s0 + j) * kTile;
+            if (ptx::elect_one()) {
+                const uint32_t dst = sStage + st * C::kStageBytes;
+                ptx::mbar_arrive_expect_tx(b.full(st), C::kStageBytes);
+                for (int x = 0; x < C::kBoxes; ++x) {
+                    ptx::tma_load_3d(dst + x * C::kBoxBytes, tmS0, b.full(st), x * 64, row, bh);
+                    ptx::tma_load_3d(dst + C::kTileBytes + x * C::kBoxBytes, tmS1, b.full(st), x * 64, row, bh);
+                }
+                if (KV) {   // the query tile's lg and delta: 512 bytes each, 16-byte aligned (Npad % 128 == 0)
+                    const size_t off = (size_t)bh * p.Npad + row;
+                    ptx::bulk_load(dst + 2 * C::kTileBytes, p.lg + off, kTile * 4, b.full(st));
+                    ptx::bulk_load(dst + 2 * C::kTileBytes + kTile * 4, p.dl + off, kTile * 4, b.full(st));
+                }
+            }
+            __syncwarp();
+        }
+    }
+    // Tail: every copy issued has landed (time-bounded), so no asynchronous
+    // write targets this CTA's shared memory after exit.
+    for (int s = 0; s < C::kStages && s < step; ++s) {
+        const int last = step - 1 - ((step - 1 - s) % C::kStages);
+        wait_landed(b.full(s), (uint32_t)(last / C::kStages) & 1u, c, kSiteBwdTail);
+    }
+    if (tiles > 0)
+        wait_landed(b.res_full(), (uint32_t)(tiles - 1) & 1u, c, kSiteBwdTail);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+
+template <int D, bool BF16, bool KV>
+__device__ void bwd_mma(const Params &p, bool causal, uint32_t sRes, uint32_t sStage, uint32_t tmem,
+                        BBars<D, KV> b, Ctl c)
+{
+    using C = BCfg<D, KV>;
+    constexpr uint32_t kIdescSS = instr_desc_f16(BF16, kTile, kTile, false);   // both operands K-major
+    constexpr uint32_t kIdescTS = instr_desc_f16(BF16, kTile, D, true);        // B MN-major
+    const uint32_t r0_lo = desc_lo(sRes, 16), r1_lo = desc_lo(sRes + C::kTileBytes, 16);
+    const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
+    const uint32_t tAcc0 = tmem + C::kColAcc0, tAcc1 = tmem + C::kColAcc1;
+    int step = 0, tiles = 0;
+    uint32_t n_p = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int t = bwd_tile(r, blockIdx.x, gridDim.x);
+        if (t >= p.T)
+            break;
+        int bh, rt, s0, n;
+        bwd_decode<KV>(p, causal, t, bh, rt, s0, n);
+        if (!warp_wait(b.res_full(), (uint32_t)tiles & 1u, c, kSiteBwdResFull))
+            break;
+        ptx::tc_fence_after_sync();
+        for (int j = 0; j < n; ++j, ++step) {
+            const int st = step % C::kStages;
+            if (!warp_wait(b.full(st), (uint32_t)(step / C::kStages) & 1u, c, kSiteBwdSlotFull)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            const uint32_t sa = sStage + st * C::kStageBytes;
+            const uint32_t s0_lo = desc_lo(sa, 16), s1_lo = desc_lo(sa + C::kTileBytes, 16);
+            if (ptx::elect_one()) {
+                // S (S^T) = R0 S0^T and dP (dP^T) = R1 S1^T over D / 16 k-steps:
+                // K-major operands advance 32 bytes per step inside a 128-byte
+                // swizzle row and one box (16 KB) per 64 columns.
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)((kk / 4) * (C::kBoxBytes >> 4) + (kk % 4) * 2);
+                    ptx::mma_ss(tS, desc_from_lo(r0_lo + off), desc_from_lo(s0_lo + off), kIdescSS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)((kk / 4) * (C::kBoxBytes >> 4) + (kk % 4) * 2);
+                    ptx::mma_ss(tDP, desc_from_lo(r1_lo + off), desc_from_lo(s1_lo + off), kIdescSS,
+                                kk > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(b.sd_full());
+            }
+            __syncwarp();
+            if (j == 0 && tiles > 0 &&   // the accumulators are overwritten: the previous tile's were read
+                !warp_wait(b.acc_free(), (uint32_t)(tiles - 1) & 1u, c, kSiteBwdAccFree)) {
+                ok = false;
+                break;
+            }
+            if (!warp_wait(b.p_full(), n_p & 1u, c, kSiteBwdPFull)) {
+                ok = false;
+                break;
+            }
+            ++n_p;
+            ptx::tc_fence_after_sync();
+            // KV:  dV += P^T dO (P^T in the S columns), dK += dS^T Q (dS^T in the dP columns)
+            // dQ:  dQ += dS K (dS in the S columns)
+            // The 16-bit A operand comes from TMEM, 8 columns per 16 rows of the
+            // streamed tile; the B operand is the streamed tile read MN-major
+            // (16 rows = 2 KB per k-step, leading byte offset = the box stride).
+            const uint32_t m0_lo = desc_lo(sa + (KV ? C::kTileBytes : 0), C::kBoxBytes);   // KV: dO; dQ: K
+            const uint32_t m1_lo = desc_lo(sa, C::kBoxBytes);                               // KV: Q
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    ptx::mma_ts(tAcc0, tS + a_col(kk), desc_from_lo(m0_lo + kk * (2048 >> 4)), kIdescTS,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                if (KV) {
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        ptx::mma_ts(tAcc1, tDP + a_col(kk), desc_from_lo(m1_lo + kk * (2048 >> 4)), kIdescTS,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(b.empty(st));
+                if (j == n - 1) {
+                    ptx::mma_commit(b.acc_full());
+                    ptx::mma_commit(b.res_empty());
+                }
+            }
+            __syncwarp();
+        }
+        ++tiles;
+    }
+    // Drain: every MMA this warp issued has completed before TMEM is freed.
+    if (ptx::elect_one())
+        ptx::mma_commit(b.drain());
+    __syncwarp();
+    wait_landed(b.drain(), 0u, c, kSiteBwdDrain);
+}
+
+// ------------------------------------------------------------------ compute
+
+// Write 32 fp32 columns of one accumulator row (times `mul`) as 16-bit values
+// to global memory at `dst` (64 bytes, 16-byte aligned).
+template <bool BF16>
+__device__ __forceinline__ void store_row32(void *dst, const uint32_t (&v)[32], float mul)
+{
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float a = __uint_as_float(v[2 * i]) * mul, bb = __uint_as_float(v[2 * i + 1]) * mul;
+        pk[i] = BF16 ? ptx::pack_bf16x2(a, bb) : ptx::pack_f16x2(a, bb);
+    }
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        ptx::st_global_v4(d4 + q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+
+template <int D, bool BF16, bool CAUSAL, bool KV>
+__device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBars<D, KV> b, Ctl c)
+{
+    using C = BCfg<D, KV>;
+    const int h = threadIdx.x / 128;                // column half of S and dP
+    const int warp = threadIdx.x / 32;
+    const int lane_row = (warp % 4) * 32 + threadIdx.x % 32;   // TMEM lane = row of the resident tile
+    const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
+    const uint32_t tS = tmem + C::kColS + lane_off, tDP = tmem + C::kColDP + lane_off;
+    int step = 0, tiles = 0;
+    for (int r = 0;; ++r) {
+        const int t = bwd_tile(r, blockIdx.x, gridDim.x);
+        if (t >= p.T)
+            break;
+        int bh, rt, s0, n;
+        bwd_decode<KV>(p, CAUSAL, t, bh, rt, s0, n);
+        // dQ pass: this thread's query row has one lg and delta for the tile.
+        float lg_row = 0.f, dl_row = 0.f;
+        if (!KV) {
+            const size_t off = (size_t)bh * p.Npad + (size_t)rt * kTile + lane_row;
+            lg_row = p.lg[off];
+            dl_row = p.dl[off];
+        }
+        for (int j = 0; j < n; ++j, ++step) {
+            const int st = step % C::kStages;
+            const int si = s0 + j;   // streamed tile index
+            if (!warp_wait(b.sd_full(), (uint32_t)step & 1u, c, kSiteBwdSdFull))
+                return;
+            ptx::tc_fence_after_sync();
+            const uint32_t vec = sStage + st * C::kStageBytes + 2 * C::kTileBytes;   // KV: lg[128], delta[128]
+            // Masks: the causal diagonal tile (key > query hidden) and, in the
+            // dQ pass, keys past N in the last key tile.  (Padding queries
+            // have lg = +inf, so their P is already 0.)
+            const bool diag = CAUSAL && si == rt;
+            const int key_limit = KV ? kTile : p.N - si * kTile;   // dQ pass: columns >= key_limit are past N
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                const int c0 = 64 * h + 32 * ch;   // first column of this chunk
+                uint32_t sv[32];
+                ptx::tmem_ld32(tS + c0, sv);
+                ptx::tmem_wait_ld();
+                float pr[32];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    float4 lg4 = make_float4(lg_row, lg_row, lg_row, lg_row);
+                    if (KV)
+                        lg4 = ptx::ld_shared_v4f32(vec + (uint32_t)(c0 + i) * 4);
+                    const float l4[4] = {lg4.x, lg4.y, lg4.z, lg4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = c0 + i + e;
+                        // KV: lane = key, column = query; dQ: lane = query, column = key
+                        const bool hidden = KV ? (diag && lane_row > col) : ((diag && col > lane_row) || col >= key_limit);
+                        const float x = __uint_as_float(sv[i + e]) * p.qk2 - l4[e];
+                        pr[i + e] = hidden ? 0.f : ptx::ex2(x);
+                    }
+                }
+                if (KV) {   // P^T, 16-bit pairs, over this chunk's first 16 columns
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = BF16 ? ptx::pack_bf16x2(pr[2 * i], pr[2 * i + 1]) : ptx::pack_f16x2(pr[2 * i], pr[2 * i + 1]);
+                    tmem_st16(tS + 64 * h + 16 * ch, pk);
+                }
+                uint32_t dv[32];
+                ptx::tmem_ld32(tDP + c0, dv);
+                ptx::tmem_wait_ld();
+                uint32_t dk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    float4 d4 = make_float4(dl_row, dl_row, dl_row, dl_row);
+                    if (KV)
+                        d4 = ptx::ld_shared_v4f32(vec + kTile * 4 + (uint32_t)(c0 + i) * 4);
+                    const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float ds[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        ds[e] = pr[i + e] * (__uint_as_float(dv[i + e]) - dd[e]);
+                    dk[i / 2] = BF16 ? ptx::pack_bf16x2(ds[0], ds[1]) : ptx::pack_f16x2(ds[0], ds[1]);
+                    dk[i / 2 + 1] = BF16 ? ptx::pack_bf16x2(ds[2], ds[3]) : ptx::pack_f16x2(ds[2], ds[3]);
+                }
+                // dS (dS^T): KV over the dP columns, dQ pass over the S columns
+                tmem_st16((KV ? tDP : tS) + 64 * h + 16 * ch, dk);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(b.p_full());
+        }
+        // The tile's accumulators, written out once: KV: warpgroup 0 writes dV,
+        // warpgroup 1 dK (times the scale); dQ pass: warpgroup h writes
+        // columns [h D/2, (h+1) D/2) of dQ (times the scale).
+        if (!warp_wait(b.acc_full(), (uint32_t)tiles & 1u, c, kSiteBwdAccFull))
+            return;
+        ptx::tc_fence_after_sync();
+        const int grow = rt * kTile + lane_row;   // row within the head
+        if (KV) {
+            const uint32_t tA = tmem + (h ? C::kColAcc1 : C::kColAcc0) + lane_off;
+            char *dst = static_cast<char *>(h ? p.dA : p.dB) + ((size_t)bh * p.N + grow) * D * 2;
+            const float mul = h ? p.scale : 1.f;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tA + 32 * cc, v);
+                ptx::tmem_wait_ld();
+                if (grow < p.N)
+                    store_row32<BF16>(dst + cc * 64, v, mul);
+            }
+        } else {
+            const uint32_t tA = tmem + C::kColAcc0 + lane_off;
+            char *dst = static_cast<char *>(p.dA) + ((size_t)bh * p.N + grow) * D * 2;
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+                const int col = h * (D / 2) + 32 * cc;
+                uint32_t v[32];
+                ptx::tmem_ld32(tA + col, v);
+                ptx::tmem_wait_ld();
+                if (grow < p.N)
+                    store_row32<BF16>(dst + col * 2, v, p.scale);
+            }
+        }
+        ptx::tc_fence_before_sync();
+        ptx::mbar_arrive(b.acc_free());
+        ++tiles;
+    }
+}
+
+// ------------------------------------------------------------------ kernels
+
+// KV = true:  tmR0 = K, tmR1 = V (resident), tmS0 = Q, tmS1 = dO (streamed)
+// KV = false: tmR0 = Q, tmR1 = dO (resident), tmS0 = K, tmS1 = V (streamed)
+template <int D, bool BF16, bool CAUSAL, bool KV>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_sm103(const __grid_constant__ CUtensorMap tmR0, const __grid_constant__ CUtensorMap tmR1,
+                 const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
+                 const __grid_constant__ Params p)
+{
+    using C = BCfg<D, KV>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // 128-byte swizzle atoms need 1024-byte alignment
+    uint8_t *base_ptr = smem_raw + (base - raw);
+    const uint32_t sRes = base + C::kResOff;
+    const uint32_t sStage = base + C::kStageOff;
+    BBars<D, KV> b{base + C::kBarOff};
+    uint32_t *misc = reinterpret_cast<uint32_t *>(base_ptr + C::kMiscOff);
+    Ctl c{reinterpret_cast<volatile int *>(misc + 1)};
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            ptx::mbar_init(b.full(s), 1);
+            ptx::mbar_init(b.empty(s), 1);
+        }
+        ptx::mbar_init(b.res_full(), 1);
+        ptx::mbar_init(b.res_empty(), 1);
+        ptx::mbar_init(b.sd_full(), 1);
+        ptx::mbar_init(b.p_full(), kComputeThreads);
+        ptx::mbar_init(b.acc_full(), 1);
+        ptx::mbar_init(b.acc_free(), kComputeThreads);
+        ptx::mbar_init(b.drain(), 1);
+        *c.abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(misc), C::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        ptx::prefetch_tensormap(&tmR0);
+        ptx::prefetch_tensormap(&tmR1);
+        ptx::prefetch_tensormap(&tmS0);
+        ptx::prefetch_tensormap(&tmS1);
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc);
+
+    if (threadIdx.x < kComputeThreads)
+        bwd_compute<D, BF16, CAUSAL, KV>(p, tmem, sStage, b, c);
+    else if (warp == kLoadWarp)
+        bwd_load<D, KV>(&tmR0, &tmR1, &tmS0, &tmS1, p, CAUSAL, sRes, sStage, b, c);
+    else if (warp == kMmaWarp)
+        bwd_mma<D, BF16, KV>(p, CAUSAL, sRes, sStage, tmem, b, c);
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// delta = rowsum(dO o O) and lg = LSE * log2(e) per query row, padded to
+// whole 128-row tiles: D / 8 threads per row, 16 bytes each.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+    fa_bwd_prep(const uint16_t *O, const uint16_t *dO, const float *LSE, float *lg, float *dl, int N, int Npad,
+                long long rows)
+{
+    constexpr int kTpr = D / 8;   // threads per row: 8 or 16, a divisor of 32
+    const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long row = g / kTpr;
+    const int part = (int)(g % kTpr);
+    if (row >= rows)   // whole row groups leave together (kTpr divides the warp)
+        return;
+    const long long bh = row / Npad;
+    const int i = (int)(row - bh * Npad);
+    float acc = 0.f;
+    if (i < N) {
+        const size_t e = ((size_t)bh * N + i) * D + 8 * part;
+        const uint4 o4 = *reinterpret_cast<const uint4 *>(O + e);
+        const uint4 d4 = *reinterpret_cast<const uint4 *>(dO + e);
+        const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float o0, o1, d0, d1;
+            if (BF16) {
+                o0 = __uint_as_float(ow[k] << 16);
+                o1 = __uint_as_float(ow[k] & 0xffff0000u);
+                d0 = __uint_as_float(dw[k] << 16);
+                d1 = __uint_as_float(dw[k] & 0xffff0000u);
+            } else {
+                o0 = __half2float(__ushort_as_half((unsigned short)(ow[k] & 0xffffu)));
+                o1 = __half2float(__ushort_as_half((unsigned short)(ow[k] >> 16)));
+                d0 = __half2float(__ushort_as_half((unsigned short)(dw[k] & 0xffffu)));
+                d1 = __half2float(__ushort_as_half((unsigned short)(dw[k] >> 16)));
+            }
+            acc = fmaf(o0, d0, acc);
+            acc = fmaf(o1, d1, acc);
+        }
+    }
+    const int lane = threadIdx.x % 32;
+    const uint32_t group = ((1u << kTpr) - 1u) << (lane & ~(kTpr - 1));
+#pragma unroll
+    for (int m = kTpr / 2; m > 0; m /= 2)
+        acc += __shfl_xor_sync(group, acc, m);
+    if (part == 0) {
+        float l = INFINITY;
+        if (i < N) {
+            const float lse = LSE[(size_t)bh * N + i];
+            l = (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;   // a row without keys: P = 0
+        }
+        lg[row] = l;
+        dl[row] = (i < N) ? acc : 0.f;
+    }
+}
+
+}  // namespace bwd
+}  // namespace fa

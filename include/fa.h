@@ -213,6 +213,39 @@ FA_API fa_status fa_fwd_noalloc(const void *Q, const void *K, const void *V, voi
                                 fa_dtype dtype, fa_schedule schedule, fa_stream_t stream);
 
 /*
+ * fa_bwd -- attention backward: the gradients of fa_fwd's O with respect to
+ * Q, K and V for an upstream gradient dO, from the forward's O and LSE.
+ *
+ * Q, K, V, O, dO : device pointers to contiguous [B, H, N, D] tensors of
+ *                  `dtype` (O and LSE as fa_fwd wrote them for the same Q, K,
+ *                  V, causal and scale).  Only read; they may alias one
+ *                  another.
+ * LSE            : device pointer to contiguous [B, H, N] float32.
+ * dQ, dK, dV     : device pointers to contiguous [B, H, N, D] tensors of
+ *                  `dtype`; every element is written.  None may overlap an
+ *                  input or another output.
+ * B, H, N, D, causal, scale, dtype, stream : as for fa_fwd; B*H*ceil(N/128)*128
+ *                  must stay below 2^31.
+ *
+ * With P = exp(scale * Q K^T - LSE) (0 where causal hides key j > query i)
+ * and delta = rowsum(dO o O):  dV = P^T dO,  dS = P o (dO V^T - delta),
+ * dQ = scale * dS K,  dK = scale * dS^T Q.  P and dS are rounded to `dtype`
+ * for the tensor-core products, which accumulate in fp32.  P is recomputed
+ * from LSE ("FlashAttention 2 from PyTorch to Triton", What I am building);
+ * dK and dV are accumulated per key tile over the query tiles, dQ in a second
+ * pass over the key tiles (its list of limitations), so no atomics are used
+ * and the result is deterministic.
+ *
+ * Scratch: 8 bytes per query row (rounded up to 128 rows per head) for delta
+ * and LSE * log2(e), allocated per (device, stream) on first use like the
+ * balanced schedule's workspace.  Errors as for fa_fwd; FA_ERR_CUDA if the
+ * scratch cannot be allocated.
+ */
+FA_API fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                        const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D, int causal,
+                        float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
  * fa_sync_status -- synchronise `stream`, then return and clear the device
  * status word of the current device: FA_OK, FA_ERR_DEVICE_TIMEOUT if a kernel
  * gave up on a wait since the last call, or FA_ERR_CUDA if the synchronise

@@ -148,3 +148,32 @@ def test_band_arguments(lib):
             rc = lib.fa_fwd_band(a["q"], a["k"], a["v"], a["o"], a["lse"], 1, 2, 16, 300, 64, window[0], window[1],
                                  ctypes.c_float(0.125), 0, 0, None)
             assert rc == UNSUPPORTED, (window, rc)
+
+
+def test_bwd_invalid_arguments_rejected(lib):
+    """fa_bwd validates everything before touching a device: sizes, flags,
+    scale, NULL and misaligned pointers, and outputs overlapping an input or
+    each other."""
+    import ctypes
+    base = dict(q=A, k=A + 0x1000000, v=A + 0x2000000, o=A + 0x3000000, do=A + 0x4000000, lse=A + 0x5000000,
+                dq=A + 0x6000000, dk=A + 0x7000000, dv=A + 0x8000000, B=1, H=2, N=256, D=64, causal=0, scale=0.125,
+                dtype=0)
+
+    def call(**over):
+        a = dict(base, **over)
+        return lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"], a["B"],
+                          a["H"], a["N"], a["D"], a["causal"], ctypes.c_float(a["scale"]), a["dtype"], None)
+
+    for over in (dict(D=96), dict(B=0), dict(N=0), dict(causal=2), dict(dtype=3), dict(scale=0.0),
+                 dict(scale=float("nan")), dict(q=0), dict(do=0), dict(lse=0), dict(dv=0),
+                 dict(B=1 << 16, H=1 << 8, N=129),                   # B*H*Npad >= 2^31
+                 dict(dq=A + 0x1000000),                              # dQ aliases K
+                 dict(dk=A + 0x6000000 + 64),                         # dK overlaps dQ
+                 dict(dv=A + 0x5000000)):                             # dV overlaps LSE
+        assert call(**over) == INVALID, over
+    for f in ("q", "do", "lse", "dk"):
+        assert call(**{f: base[f] + 8}) == MISALIGNED, f
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert call() == UNSUPPORTED
+        assert call(causal=1, D=128, dtype=1) == UNSUPPORTED
