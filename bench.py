@@ -235,6 +235,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--bwd-steps", type=int, default=50, help="timed backward calls per mask (0: skip)")
     args = ap.parse_args(argv)
 
     from exact_attention_10_gb300.inputs import WORKLOADS
@@ -342,6 +343,39 @@ def main(argv=None):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     e2e_value = job_tflops(world, e2e_steps, F[False] + F[True], e2e_ms)
 
+    # backward (fa_bwd) on the same workload, from this forward's O and LSE and
+    # a seeded upstream gradient; timed per call like the forward, outside the
+    # step above.  FLOPs in the usual convention: 2.5 x the forward's (five
+    # tile products per (query tile, key tile) pair: S, dP, dV, dK, dQ).
+    bwd_info = None
+    if args.bwd_steps > 0:
+        from exact_attention_10_gb300.inputs import make_custom
+        do = make_custom(w.B, w.H, w.N, w.D, w.dtype, seed=1)[0].to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bwd_info = {"flops_convention": "2.5 x forward (five tile products per tile pair)",
+                    "kernels_per_call": 3}
+        for c in modes:
+            call(c)
+            for _ in range(3):
+                fa.backward(q, k, v, o, do, lse, causal=c, scale=w.scale, dq=dq, dk=dk, dv=dv)
+            bs = [torch.cuda.Event(enable_timing=True) for _ in range(args.bwd_steps)]
+            be = [torch.cuda.Event(enable_timing=True) for _ in range(args.bwd_steps)]
+            barrier()
+            for i in range(args.bwd_steps):
+                flush.zero_()
+                bs[i].record(stream)
+                fa.backward(q, k, v, o, do, lse, causal=c, scale=w.scale, dq=dq, dk=dk, dv=dv)
+                be[i].record(stream)
+            barrier()
+            rc = fa.sync_status(sp)
+            if rc != 0:
+                raise fa.FAError(rc, "backward")
+            bms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in zip(bs, be))
+            btf = 2.5 * F[c] / (bms * 1e-3) / 1e12
+            bwd_info["causal" if c else "noncausal"] = {"ms_mean": bms, "tflops": btf,
+                                                       "frac_of_measured_peak": btf / _peaks()[0],
+                                                       "flops_per_call": 2.5 * F[c]}
+
     peak, peak_sus, _, peak_src = _peaks()
     mode_info = {}
     for c in modes:
@@ -367,6 +401,8 @@ def main(argv=None):
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
             "clocks": clk, "gpu_launches": args.steps * len(modes), "wall_s_timed_region": wall}
+    if bwd_info is not None:
+        line["backward"] = bwd_info
     if rank == 0 and not args.no_cpu_baseline:
         v_cpu, desc, cores, spent = cpu_oracle_sample(w, args.cpu_budget)
         line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",

@@ -64,11 +64,15 @@ constexpr int kComputeThreads = 256;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTile = 128;   // rows of a resident or streamed tile (keys or queries)
+// Registers per thread after setmaxnreg: 2 x 128 x 200 + 128 x 96 = 63488, within
+// the 384 x 168 = 64512 the block is launched with.
+constexpr uint32_t kRegsCompute = 200;
+constexpr uint32_t kRegsProducer = 96;
 
 // Wait sites (status word), after the forward's.
 enum : uint32_t {
     kSiteBwdResEmpty = 32, kSiteBwdSlotEmpty, kSiteBwdResFull, kSiteBwdSlotFull, kSiteBwdPFull, kSiteBwdAccFree,
-    kSiteBwdSdFull, kSiteBwdAccFull, kSiteBwdDrain, kSiteBwdTail
+    kSiteBwdSdFull, kSiteBwdAccFull, kSiteBwdDrain, kSiteBwdTail, kSiteBwdSdFree, kSiteBwdPdFree
 };
 
 struct Params {
@@ -97,14 +101,20 @@ struct BCfg {
     static constexpr int kResOff = 0;                                 // the resident pair of tiles
     static constexpr int kStageOff = 2 * kTileBytes;
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-    // full[kStages], empty[kStages], res_full, res_empty, sd_full, p_full, acc_full, acc_free, drain
-    static constexpr int kNumBars = 2 * kStages + 7;
+    // full[kStages], empty[kStages], res_full, res_empty, sd_full, p_full, acc_full, acc_free, drain, sd_free,
+    // pd_free
+    static constexpr int kNumBars = 2 * kStages + 9;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;           // TMEM address, abort flag
     static constexpr int kSmem = kMiscOff + 16 + 1024;                // + slack to align the base to 1024
     static_assert(kSmem <= 232448, "shared memory per CTA");
     static_assert(kStageBytes % 1024 == 0, "stages keep the tiles' 1024-byte swizzle alignment");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+    // Pipelined passes (D = 64): dQ pass: two 64-column dS buffers after dQ (dS of
+    // step g in buffer g % 2); KV pass: one P^T and one dS^T buffer after dV, dK.
+    static constexpr uint32_t kColDS = KV ? 256 + 2 * D + 64 : 256 + D;
+    static constexpr uint32_t kColP = 256 + 2 * D;
+    static_assert(D != 64 || (KV ? kColDS + 64 : kColDS + 128) <= kTmemCols, "pipelined buffers fit TMEM");
 };
 
 template <int D, bool KV>
@@ -120,6 +130,8 @@ struct BBars {
     __device__ uint32_t acc_full() const { return at(4); }    // MMA -> compute: a tile's accumulators final
     __device__ uint32_t acc_free() const { return at(5); }    // compute -> MMA: accumulators read out
     __device__ uint32_t drain() const { return at(6); }
+    __device__ uint32_t sd_free() const { return at(7); }     // compute -> MMA: S and dP loaded (pipelined)
+    __device__ uint32_t pd_free() const { return at(8); }     // MMA -> compute: P / dS buffers read (pipelined KV)
 };
 
 // Work tile t -> (head, resident tile index), and the streamed tiles it
@@ -379,26 +391,42 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
             // have lg = +inf, so their P is already 0.)
             const bool diag = CAUSAL && si == rt;
             const int key_limit = KV ? kTile : p.N - si * kTile;   // dQ pass: columns >= key_limit are past N
+            const bool masked = diag || key_limit < kTile;          // warp-uniform
+            const uint64_t qk2 = ptx::f2_pack(p.qk2, p.qk2);
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
                 const int c0 = 64 * h + 32 * ch;   // first column of this chunk
-                uint32_t sv[32];
-                ptx::tmem_ld32(tS + c0, sv);
+                uint32_t sv[32], dv[32];
+                ptx::tmem_ld32(tS + c0, sv);        // S and dP of the chunk, one wait
+                ptx::tmem_ld32(tDP + c0, dv);
                 ptx::tmem_wait_ld();
                 float pr[32];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
-                    float4 lg4 = make_float4(lg_row, lg_row, lg_row, lg_row);
-                    if (KV)
-                        lg4 = ptx::ld_shared_v4f32(vec + (uint32_t)(c0 + i) * 4);
-                    const float l4[4] = {lg4.x, lg4.y, lg4.z, lg4.w};
+                    uint64_t nl01, nl23;   // -lg for the four columns, as pairs
+                    if (KV) {
+                        const float4 lg4 = ptx::ld_shared_v4f32(vec + (uint32_t)(c0 + i) * 4);
+                        nl01 = ptx::f2_pack(-lg4.x, -lg4.y);
+                        nl23 = ptx::f2_pack(-lg4.z, -lg4.w);
+                    } else {
+                        nl01 = nl23 = ptx::f2_pack(-lg_row, -lg_row);
+                    }
+                    float x[4];
+                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), qk2, nl01),
+                                   x[0], x[1]);
+                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), qk2,
+                                               nl23),
+                                   x[2], x[3]);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int col = c0 + i + e;
-                        // KV: lane = key, column = query; dQ: lane = query, column = key
+                    for (int e = 0; e < 4; ++e)
+                        pr[i + e] = ptx::ex2(x[e]);
+                }
+                if (masked) {   // KV: lane = key, column = query; dQ pass: lane = query, column = key
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = c0 + i;
                         const bool hidden = KV ? (diag && lane_row > col) : ((diag && col > lane_row) || col >= key_limit);
-                        const float x = __uint_as_float(sv[i + e]) * p.qk2 - l4[e];
-                        pr[i + e] = hidden ? 0.f : ptx::ex2(x);
+                        pr[i] = hidden ? 0.f : pr[i];
                     }
                 }
                 if (KV) {   // P^T, 16-bit pairs, over this chunk's first 16 columns
@@ -408,20 +436,24 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
                         pk[i] = BF16 ? ptx::pack_bf16x2(pr[2 * i], pr[2 * i + 1]) : ptx::pack_f16x2(pr[2 * i], pr[2 * i + 1]);
                     tmem_st16(tS + 64 * h + 16 * ch, pk);
                 }
-                uint32_t dv[32];
-                ptx::tmem_ld32(tDP + c0, dv);
-                ptx::tmem_wait_ld();
                 uint32_t dk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
-                    float4 d4 = make_float4(dl_row, dl_row, dl_row, dl_row);
-                    if (KV)
-                        d4 = ptx::ld_shared_v4f32(vec + kTile * 4 + (uint32_t)(c0 + i) * 4);
-                    const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+                    uint64_t nd01, nd23;   // -delta, as pairs
+                    if (KV) {
+                        const float4 d4 = ptx::ld_shared_v4f32(vec + kTile * 4 + (uint32_t)(c0 + i) * 4);
+                        nd01 = ptx::f2_pack(-d4.x, -d4.y);
+                        nd23 = ptx::f2_pack(-d4.z, -d4.w);
+                    } else {
+                        nd01 = nd23 = ptx::f2_pack(-dl_row, -dl_row);
+                    }
                     float ds[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        ds[e] = pr[i + e] * (__uint_as_float(dv[i + e]) - dd[e]);
+                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(pr[i], pr[i + 1]),
+                                               ptx::f2_add(ptx::f2_pack(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), nd01)),
+                                   ds[0], ds[1]);
+                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(pr[i + 2], pr[i + 3]),
+                                               ptx::f2_add(ptx::f2_pack(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), nd23)),
+                                   ds[2], ds[3]);
                     dk[i / 2] = BF16 ? ptx::pack_bf16x2(ds[0], ds[1]) : ptx::pack_f16x2(ds[0], ds[1]);
                     dk[i / 2 + 1] = BF16 ? ptx::pack_bf16x2(ds[2], ds[3]) : ptx::pack_f16x2(ds[2], ds[3]);
                 }
@@ -470,6 +502,261 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
     }
 }
 
+// ------------------------------------------------------------------ dQ pass, pipelined
+
+// Pipelined at D = 64 only.  The pipelined order wants S_{g+2} right after
+// the products of step g, and stage g + 2 can only be loaded once they have
+// released stage g; with the two stages that fit beside the resident tiles at
+// D = 128 that load is exposed on every step (measured on the dQ pass: 892 ->
+// 840 TFLOP/s at N = 16384), and the KV pass has no TMEM left for separate
+// P^T / dS^T buffers at D = 128; so D = 128 keeps the serialized step
+// (S and dP, compute, accumulating products).
+template <int D>
+constexpr bool kPipeline = (D == 64);
+
+// The dQ pass overlaps the compute warps with the tensor core: as soon as the
+// compute warps have loaded S_g and dP_g into registers (sd_free), the next
+// step's S_{g+1} and dP_{g+1} are issued into the same columns, and dQ += dS_g K_g
+// follows once dS_g is written (p_full).  dS alternates between two TMEM
+// buffers; the compute warps write buffer g % 2 only after waiting for
+// sd_full of step g, whose commit follows the MMA that read the buffer at
+// step g - 2, so no extra barrier guards it.  Tensor-pipe order per step:
+// S_{g+1}, dP_{g+1}, dQ_g.
+template <int D, bool BF16, bool KV>
+__device__ void bwd_mma_pipe(const Params &p, bool causal, uint32_t sRes, uint32_t sStage, uint32_t tmem,
+                             BBars<D, KV> b, Ctl c)
+{
+    using C = BCfg<D, KV>;
+    constexpr uint32_t kIdescSS = instr_desc_f16(BF16, kTile, kTile, false);
+    constexpr uint32_t kIdescTS = instr_desc_f16(BF16, kTile, D, true);
+    const uint32_t r0_lo = desc_lo(sRes, 16), r1_lo = desc_lo(sRes + C::kTileBytes, 16);
+    const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
+    const uint32_t tAcc0 = tmem + C::kColAcc0, tAcc1 = tmem + C::kColAcc1;
+    int g = 0, tiles = 0;   // global step, tiles started
+    bool ok = true;
+
+    // S_g = R0 S0_g^T and dP_g = R1 S1_g^T into their columns (the previous
+    // step's S and dP must have been loaded by the compute warps).
+    auto issue_sd = [&](int gs) -> bool {
+        const int st = gs % C::kStages;
+        if (gs > 0 && !warp_wait(b.sd_free(), (uint32_t)(gs - 1) & 1u, c, kSiteBwdSdFree))
+            return false;
+        if (!warp_wait(b.full(st), (uint32_t)(gs / C::kStages) & 1u, c, kSiteBwdSlotFull))
+            return false;
+        ptx::tc_fence_after_sync();
+        const uint32_t sa = sStage + st * C::kStageBytes;
+        const uint32_t s0_lo = desc_lo(sa, 16), s1_lo = desc_lo(sa + C::kTileBytes, 16);
+        if (ptx::elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)((kk / 4) * (C::kBoxBytes >> 4) + (kk % 4) * 2);
+                ptx::mma_ss(tS, desc_from_lo(r0_lo + off), desc_from_lo(s0_lo + off), kIdescSS, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)((kk / 4) * (C::kBoxBytes >> 4) + (kk % 4) * 2);
+                ptx::mma_ss(tDP, desc_from_lo(r1_lo + off), desc_from_lo(s1_lo + off), kIdescSS, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(b.sd_full());
+        }
+        __syncwarp();
+        return true;
+    };
+
+    for (int r = 0; ok; ++r) {
+        const int t = bwd_tile(r, blockIdx.x, gridDim.x);
+        if (t >= p.T)
+            break;
+        int bh, rt, s0, n;
+        bwd_decode<KV>(p, causal, t, bh, rt, s0, n);
+        if (!warp_wait(b.res_full(), (uint32_t)tiles & 1u, c, kSiteBwdResFull))
+            break;
+        ptx::tc_fence_after_sync();
+        if (!issue_sd(g))
+            break;
+        for (int j = 0; j < n; ++j, ++g) {
+            if (j + 1 < n && !issue_sd(g + 1)) {
+                ok = false;
+                break;
+            }
+            if (j == 0 && tiles > 0 &&   // the accumulators are overwritten: the previous tile's were read out
+                !warp_wait(b.acc_free(), (uint32_t)(tiles - 1) & 1u, c, kSiteBwdAccFree)) {
+                ok = false;
+                break;
+            }
+            if (!warp_wait(b.p_full(), (uint32_t)g & 1u, c, kSiteBwdPFull)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            const int st = g % C::kStages;
+            // KV:  dV += P^T_g dO_g, dK += dS^T_g Q_g;  dQ pass: dQ += dS_g K_g.
+            // The A operand comes from a TMEM buffer (8 columns per 16 rows of the
+            // streamed tile), the B operand is the streamed tile read MN-major
+            // (16 rows = 2 KB per k-step).
+            const uint32_t sa = sStage + st * C::kStageBytes;
+            const uint32_t m0_lo = desc_lo(sa + (KV ? C::kTileBytes : 0), C::kBoxBytes);   // KV: dO; dQ: K
+            const uint32_t m1_lo = desc_lo(sa, C::kBoxBytes);                               // KV: Q
+            const uint32_t tA0 = tmem + (KV ? C::kColP : C::kColDS + 64u * (uint32_t)(g & 1));
+            const uint32_t tA1 = tmem + C::kColDS;
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    ptx::mma_ts(tAcc0, tA0 + 8 * kk, desc_from_lo(m0_lo + kk * (2048 >> 4)), kIdescTS,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                if (KV) {
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        ptx::mma_ts(tAcc1, tA1 + 8 * kk, desc_from_lo(m1_lo + kk * (2048 >> 4)), kIdescTS,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(b.pd_free());
+                }
+                ptx::mma_commit(b.empty(st));
+                if (j == n - 1) {
+                    ptx::mma_commit(b.acc_full());
+                    ptx::mma_commit(b.res_empty());
+                }
+            }
+            __syncwarp();
+        }
+        ++tiles;
+    }
+    if (ptx::elect_one())
+        ptx::mma_commit(b.drain());
+    __syncwarp();
+    wait_landed(b.drain(), 0u, c, kSiteBwdDrain);
+}
+
+template <int D, bool BF16, bool CAUSAL, bool KV>
+__device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage, BBars<D, KV> b, Ctl c)
+{
+    using C = BCfg<D, KV>;
+    const int h = threadIdx.x / 128;                            // column half of S and dP
+    const int warp = threadIdx.x / 32;
+    const int row = (warp % 4) * 32 + threadIdx.x % 32;         // TMEM lane = row of the resident tile
+    const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
+    const uint32_t tS = tmem + C::kColS + lane_off + 64 * h, tDP = tmem + C::kColDP + lane_off + 64 * h;
+    const uint64_t qk2 = ptx::f2_pack(p.qk2, p.qk2);
+    int g = 0, tiles = 0;
+    for (int r = 0;; ++r) {
+        const int t = bwd_tile(r, blockIdx.x, gridDim.x);
+        if (t >= p.T)
+            break;
+        int bh, rt, s0, n;
+        bwd_decode<KV>(p, CAUSAL, t, bh, rt, s0, n);
+        uint64_t nlg = 0, ndl = 0;   // dQ pass: this thread's query row's -lg and -delta
+        if (!KV) {
+            const size_t off = (size_t)bh * p.Npad + (size_t)rt * kTile + row;
+            nlg = ptx::f2_pack(-p.lg[off], -p.lg[off]);
+            ndl = ptx::f2_pack(-p.dl[off], -p.dl[off]);
+        }
+        for (int j = 0; j < n; ++j, ++g) {
+            const int si = s0 + j;   // streamed tile
+            if (!warp_wait(b.sd_full(), (uint32_t)g & 1u, c, kSiteBwdSdFull))
+                return;
+            ptx::tc_fence_after_sync();
+            uint32_t sv[64], dv[64];
+            ptx::tmem_ld64(tS, sv);   // this warpgroup's 64 columns of S and dP, then release both
+            ptx::tmem_ld64(tDP, dv);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(b.sd_free());
+            // KV: lane = key, column = query (lg and delta per column, from the
+            // stage); dQ pass: lane = query, column = key.  Masks: the causal
+            // diagonal tile, and in the dQ pass keys past N (padding queries
+            // have lg = +inf).
+            const uint32_t vec = sStage + (g % C::kStages) * C::kStageBytes + 2 * C::kTileBytes;
+            const int limit = KV ? kTile : p.N - si * kTile - 64 * h;   // dQ pass: columns >= limit past N
+            const bool diag = CAUSAL && si == rt;
+            const bool masked = diag || limit < 64;
+#pragma unroll
+            for (int i = 0; i < 64; i += 2) {
+                uint64_t nl = nlg, nd = ndl;
+                if (KV) {
+                    const float2 l2 = ptx::ld_shared_v2f32(vec + (uint32_t)(64 * h + i) * 4);
+                    const float2 d2 = ptx::ld_shared_v2f32(vec + kTile * 4 + (uint32_t)(64 * h + i) * 4);
+                    nl = ptx::f2_pack(-l2.x, -l2.y);
+                    nd = ptx::f2_pack(-d2.x, -d2.y);
+                }
+                float x0, x1;
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), qk2, nl),
+                               x0, x1);
+                float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                if (masked) {
+                    const int col = 64 * h + i;
+                    if (KV) {
+                        p0 = (diag && row > col) ? 0.f : p0;
+                        p1 = (diag && row > col + 1) ? 0.f : p1;
+                    } else {
+                        p0 = ((diag && col > row) || i >= limit) ? 0.f : p0;
+                        p1 = ((diag && col + 1 > row) || i + 1 >= limit) ? 0.f : p1;
+                    }
+                }
+                float d0, d1;
+                ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1),
+                                           ptx::f2_add(ptx::f2_pack(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), nd)),
+                               d0, d1);
+                sv[i] = __float_as_uint(p0);   // P, kept for KV's P^T
+                sv[i + 1] = __float_as_uint(p1);
+                dv[i] = __float_as_uint(d0);   // dS
+                dv[i + 1] = __float_as_uint(d1);
+            }
+            uint32_t pk[32];
+            if (KV) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    pk[i] = BF16 ? ptx::pack_bf16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]))
+                                 : ptx::pack_f16x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+                // the single P^T / dS^T buffers: the previous step's products must have read them
+                if (g > 0 && !warp_wait(b.pd_free(), (uint32_t)(g - 1) & 1u, c, kSiteBwdPdFree))
+                    return;
+                ptx::tc_fence_after_sync();
+                ptx::tmem_st32(tmem + C::kColP + lane_off + 32 * h, pk);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                pk[i] = BF16 ? ptx::pack_bf16x2(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]))
+                             : ptx::pack_f16x2(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]));
+            ptx::tmem_st32(tmem + C::kColDS + (KV ? 0u : 64u * (uint32_t)(g & 1)) + lane_off + 32 * h, pk);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(b.p_full());
+        }
+        // The tile's accumulators (see bwd_compute).
+        if (!warp_wait(b.acc_full(), (uint32_t)tiles & 1u, c, kSiteBwdAccFull))
+            return;
+        ptx::tc_fence_after_sync();
+        const int grow = rt * kTile + row;
+        if (KV) {
+            const uint32_t tA = tmem + (h ? C::kColAcc1 : C::kColAcc0) + lane_off;
+            char *dst = static_cast<char *>(h ? p.dA : p.dB) + ((size_t)bh * p.N + grow) * D * 2;
+            const float mul = h ? p.scale : 1.f;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tA + 32 * cc, v);
+                ptx::tmem_wait_ld();
+                if (grow < p.N)
+                    store_row32<BF16>(dst + cc * 64, v, mul);
+            }
+        } else {
+            char *dst = static_cast<char *>(p.dA) + ((size_t)bh * p.N + grow) * D * 2;
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+                const int col = h * (D / 2) + 32 * cc;
+                uint32_t v[32];
+                ptx::tmem_ld32(tmem + C::kColAcc0 + lane_off + col, v);
+                ptx::tmem_wait_ld();
+                if (grow < p.N)
+                    store_row32<BF16>(dst + col * 2, v, p.scale);
+            }
+        }
+        ptx::tc_fence_before_sync();
+        ptx::mbar_arrive(b.acc_free());
+        ++tiles;
+    }
+}
+
 // ------------------------------------------------------------------ kernels
 
 // KV = true:  tmR0 = K, tmR1 = V (resident), tmS0 = Q, tmS1 = dO (streamed)
@@ -505,6 +792,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(b.acc_full(), 1);
         ptx::mbar_init(b.acc_free(), kComputeThreads);
         ptx::mbar_init(b.drain(), 1);
+        ptx::mbar_init(b.sd_free(), kComputeThreads);
+        ptx::mbar_init(b.pd_free(), 1);
         *c.abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -523,12 +812,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc);
 
-    if (threadIdx.x < kComputeThreads)
-        bwd_compute<D, BF16, CAUSAL, KV>(p, tmem, sStage, b, c);
-    else if (warp == kLoadWarp)
-        bwd_load<D, KV>(&tmR0, &tmR1, &tmS0, &tmS1, p, CAUSAL, sRes, sStage, b, c);
-    else if (warp == kMmaWarp)
-        bwd_mma<D, BF16, KV>(p, CAUSAL, sRes, sStage, tmem, b, c);
+    if (threadIdx.x < kComputeThreads) {
+        ptx::regs_increase<kRegsCompute>();
+        if constexpr (kPipeline<D>)
+            bwd_compute_pipe<D, BF16, CAUSAL, KV>(p, tmem, sStage, b, c);
+        else
+            bwd_compute<D, BF16, CAUSAL, KV>(p, tmem, sStage, b, c);
+    } else {
+        ptx::regs_decrease<kRegsProducer>();
+        if (warp == kLoadWarp)
+            bwd_load<D, KV>(&tmR0, &tmR1, &tmS0, &tmS1, p, CAUSAL, sRes, sStage, b, c);
+        else if (warp == kMmaWarp)
+        {
+            if constexpr (kPipeline<D>)
+                bwd_mma_pipe<D, BF16, KV>(p, CAUSAL, sRes, sStage, tmem, b, c);
+            else
+                bwd_mma<D, BF16, KV>(p, CAUSAL, sRes, sStage, tmem, b, c);
+        }
+    }
 
     ptx::tc_fence_before_sync();
     __syncthreads();
