@@ -102,8 +102,8 @@ struct BCfg {
     static constexpr int kStageOff = 2 * kTileBytes;
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
     // full[kStages], empty[kStages], res_full, res_empty, sd_full, p_full, acc_full, acc_free, drain, sd_free,
-    // pd_free
-    static constexpr int kNumBars = 2 * kStages + 9;
+    // pd_free, p_full_odd
+    static constexpr int kNumBars = 2 * kStages + 10;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;           // TMEM address, abort flag
     static constexpr int kSmem = kMiscOff + 16 + 1024;                // + slack to align the base to 1024
     static_assert(kSmem <= 232448, "shared memory per CTA");
@@ -132,6 +132,11 @@ struct BBars {
     __device__ uint32_t drain() const { return at(6); }
     __device__ uint32_t sd_free() const { return at(7); }     // compute -> MMA: S and dP loaded (pipelined)
     __device__ uint32_t pd_free() const { return at(8); }     // MMA -> compute: P / dS buffers read (pipelined KV)
+    // p_full of step g in the pipelined dQ pass, which alternates two barriers:
+    // there the compute warps may finish step g + 1 before the MMA warp has
+    // waited for step g (nothing else holds them back), and one barrier two
+    // phases ahead of its waiter would read as not yet complete.
+    __device__ uint32_t p_full_dq(int g) const { return (g & 1) ? at(9) : at(3); }
 };
 
 // Work tile t -> (head, resident tile index), and the streamed tiles it
@@ -584,7 +589,9 @@ __device__ void bwd_mma_pipe(const Params &p, bool causal, uint32_t sRes, uint32
                 ok = false;
                 break;
             }
-            if (!warp_wait(b.p_full(), (uint32_t)g & 1u, c, kSiteBwdPFull)) {
+            const bool pok = KV ? warp_wait(b.p_full(), (uint32_t)g & 1u, c, kSiteBwdPFull)
+                                : warp_wait(b.p_full_dq(g), (uint32_t)(g >> 1) & 1u, c, kSiteBwdPFull);
+            if (!pok) {
                 ok = false;
                 break;
             }
@@ -720,7 +727,7 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
             ptx::tmem_st32(tmem + C::kColDS + (KV ? 0u : 64u * (uint32_t)(g & 1)) + lane_off + 32 * h, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(b.p_full());
+            ptx::mbar_arrive(KV ? b.p_full() : b.p_full_dq(g));
         }
         // The tile's accumulators (see bwd_compute).
         if (!warp_wait(b.acc_full(), (uint32_t)tiles & 1u, c, kSiteBwdAccFull))
@@ -794,6 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(b.drain(), 1);
         ptx::mbar_init(b.sd_free(), kComputeThreads);
         ptx::mbar_init(b.pd_free(), 1);
+        ptx::mbar_init(b.p_full_dq(1), kComputeThreads);
         *c.abort_flag = 0;
         ptx::fence_barrier_init();
     }
