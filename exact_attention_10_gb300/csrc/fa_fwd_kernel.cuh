@@ -105,6 +105,13 @@ constexpr int kPerTileBars = 7;
 constexpr int kMergeBufs = 4;            // merge staging buffers in flight
 constexpr int kMergeOBytes = 4096;       // partial O bytes per staging buffer
 constexpr int kMaxMergeParts = kSchedMaxParts;   // parts of one split tile, at most (the planner keeps to it)
+// (m, l) staging of a merge: parts x rows x 8 bytes -- 8 parts of 128 rows,
+// 16 of 64 or 32 of 32 (sched_ml_rows; the planner allows more than 8 parts
+// only for heads that short).
+constexpr int kMlBytes = kSchedMaxPartsTall * kBM * 8;
+static_assert(kSchedMaxParts * sched_ml_rows(kSchedMaxParts) * 8 <= kMlBytes &&
+                  (kSchedMaxParts / 2) * sched_ml_rows(kSchedMaxParts / 2) * 8 <= kMlBytes,
+              "merge staging holds the short-head parts");
 constexpr int kJobSlots = 2;             // merge jobs queued from the epilogue to the merge warp
 
 // A merge job, posted by the epilogue in shared memory: the Q tile's rows
@@ -154,12 +161,12 @@ struct Cfg {
     static constexpr int kHandOff = kBarOff + kNumBars * 8;            // float2 [2 tiles][128]
     static constexpr int kMiscOff = kHandOff + kQTiles * kBM * 8;
     // Merge staging: kMergeBufs buffers, each the partial O of kMergeRows rows
-    // of one part; the parts' (m, l) of the Q tile, float2 [kMaxMergeParts][128]
-    // (turned into merge weights in place); the job queue, kJobSlots MergeJobs.
+    // of one part; the parts' (m, l) of the Q tile, float2 [parts][128 or 64
+    // rows] (turned into merge weights in place); the job queue, kJobSlots MergeJobs.
     static constexpr int kMergeRows = kMergeOBytes / (D * 4);
     static constexpr int kMergeOff = (kMiscOff + 16 + 127) & ~127;
     static constexpr int kMlOff = kMergeOff + kMergeBufs * kMergeOBytes;
-    static constexpr int kJobOff = kMlOff + kMaxMergeParts * kBM * 8;
+    static constexpr int kJobOff = kMlOff + kMlBytes;
     // Shared memory of a launch (+ slack to align the base to 1024): the
     // whole-tile variant has no merge area.
     static constexpr int kSmemSplit = kJobOff + kJobSlots * (int)sizeof(MergeJob) + 1024;
@@ -827,6 +834,7 @@ __device__ void merge_role(const FwdParams &p, uint32_t sbuf, uint32_t sml, cons
         if (nparts == 0)
             return;   // stop
         const int nchunks = ((nrows + R - 1) / R) * nparts;
+        const int ml_rows = sched_ml_rows(nparts);   // staged rows per part
         const uint32_t first = streamed;
         int i_rb = 0, i_pi = 0, issued = 0;   // next chunk to stream (lane 0)
         auto issue_next = [&]() {
@@ -840,11 +848,18 @@ __device__ void merge_role(const FwdParams &p, uint32_t sbuf, uint32_t sml, cons
             }
             ++issued;
         };
+        if (nrows > ml_rows) {   // more parts than the staging holds for this many rows: the planner never does this
+            if (lane == 0)
+                record_timeout(c, kSiteMergeJob);
+            __syncwarp();
+            return;
+        }
         if (lane == 0) {
             ptx::fence_proxy_async_global();   // the parts' partials, made visible by the counter's acquire
-            ptx::mbar_arrive_expect_tx(b.ml_full(), (uint32_t)nparts * kBM * 8);
+            ptx::mbar_arrive_expect_tx(b.ml_full(), (uint32_t)(nparts * ml_rows * 8));
             for (int k = 0; k < nparts; ++k)
-                ptx::bulk_load(sml + k * kBM * 8, reinterpret_cast<const void *>(job.ml_addr[k]), kBM * 8, b.ml_full());
+                ptx::bulk_load(sml + k * ml_rows * 8, reinterpret_cast<const void *>(job.ml_addr[k]),
+                               (uint32_t)(ml_rows * 8), b.ml_full());
             while (issued < kMergeBufs && issued < nchunks)
                 issue_next();
         }
@@ -854,21 +869,21 @@ __device__ void merge_role(const FwdParams &p, uint32_t sbuf, uint32_t sml, cons
         ++ml_uses;
         if (ok) {
             // weights in place of m; a lane per row
-            for (int r = lane; r < kBM; r += 32) {
+            for (int r = lane; r < ml_rows; r += 32) {
                 float M = -INFINITY;
                 for (int k = 0; k < nparts; ++k)
-                    M = fmaxf(M, ptx::ld_shared_f32(sml + (k * kBM + r) * 8));
+                    M = fmaxf(M, ptx::ld_shared_f32(sml + (k * ml_rows + r) * 8));
                 const float Mu = (M == -INFINITY) ? 0.f : M;   // no key seen at all: every weight is 0
                 float L = 0.f;
                 for (int k = 0; k < nparts; ++k) {
-                    const uint32_t a = sml + (k * kBM + r) * 8;
+                    const uint32_t a = sml + (k * ml_rows + r) * 8;
                     const float e = ptx::ld_shared_f32(a + 4) * ptx::ex2(ptx::ld_shared_f32(a) - Mu);
                     ptx::st_shared_f32(a, e);
                     L += e;
                 }
                 const float inv_L = (L > 0.f) ? 1.f / L : 0.f;
                 for (int k = 0; k < nparts; ++k) {
-                    const uint32_t a = sml + (k * kBM + r) * 8;
+                    const uint32_t a = sml + (k * ml_rows + r) * 8;
                     ptx::st_shared_f32(a, ptx::ld_shared_f32(a) * inv_L);
                 }
                 if (r < nrows)
@@ -889,7 +904,7 @@ __device__ void merge_role(const FwdParams &p, uint32_t sbuf, uint32_t sml, cons
                     acc[q][0] = acc[q][1] = 0ull;
             }
             const uint32_t so = sbuf + buf * kMergeOBytes + (uint32_t)(row0 * D + col) * 4;
-            const uint32_t sw = sml + (uint32_t)(pi * kBM + rb * R + row0) * 8;
+            const uint32_t sw = sml + (uint32_t)(pi * ml_rows + rb * R + row0) * 8;
 #pragma unroll
             for (int q = 0; q < kPos; ++q) {
                 const float wt = ptx::ld_shared_f32(sw + q * kRowStep * 8);

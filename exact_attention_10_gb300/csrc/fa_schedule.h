@@ -44,7 +44,9 @@ constexpr int kSchedBN = 128;        // keys per step
 constexpr int kSchedCtaRows = 256;   // rows per CTA tile
 constexpr int kSchedMaxGrid = 160;   // CTAs of a balanced-schedule launch, at most
 constexpr long long kSchedMaxUnits = 0x3fffffffLL;   // units of a balanced schedule, at most (32-bit unit indices)
-constexpr int kSchedMaxParts = 8;                    // parts of one tile in a balanced schedule, at most
+constexpr int kSchedMaxParts = 32;      // parts of one tile in a balanced schedule: at most 32 for heads of
+constexpr int kSchedMaxPartsTall = 8;    // <= 32 query rows, 16 for <= 64, 8 for taller heads (the merge
+constexpr int kSchedShortRows = 64;      // warp stages (m, l) of 8 parts x 128 rows, 16 x 64 or 32 x 32)
 constexpr int kSchedUnbounded = 0x3fffffff;          // a band bound that never binds
 
 struct Schedule {
@@ -174,6 +176,21 @@ FA_HD int sched_steps_ct(const Schedule &s, int ct)
     int ks, ke;
     sched_band_steps(s, first, last, ks, ke);
     return ke - ks;
+}
+
+// Parts a tile of this schedule may be cut into: decoding-sized heads take
+// more (32 for at most 32 query rows, 16 for at most 64), so a few long heads
+// spread over more SMs; taller heads 8.  The merge warp's (m, l) staging is
+// the same size in every case (sched_ml_rows rows per part).
+FA_HD int sched_max_parts(const Schedule &s)
+{
+    return s.N <= kSchedShortRows / 2 ? kSchedMaxParts : (s.N <= kSchedShortRows ? kSchedMaxParts / 2 : kSchedMaxPartsTall);
+}
+
+// Rows of (m, l) the merge stages per part for a merge of `nparts` parts.
+FA_HD constexpr int sched_ml_rows(int nparts)
+{
+    return nparts > kSchedMaxParts / 2 ? kSchedShortRows / 2 : (nparts > kSchedMaxPartsTall ? kSchedShortRows : 128);
 }
 
 // Tile rows by length: the q-th longest and the q-th shortest (step counts
@@ -510,7 +527,7 @@ FA_HD int sched_part_slots(const Schedule &s, int t, int nw, int *slots, int max
 // the machine idle in its last wave for more than ~4% of the run and for at
 // least kSchedMinGain steps (a split tile costs its parts a partial write and
 // one of them a merge); its grid is kept small enough that no tile is cut
-// into more than kSchedMaxParts parts.  Parts have fixed costs (a partial
+// into more than sched_max_parts parts.  Parts have fixed costs (a partial
 // write, a merge, a pipeline start), so with many tiles the balanced schedule
 // is taken only where every CTA's range spans at least two tiles, and not
 // for causal attention, whose short tiles lose to those costs (measured).
@@ -585,8 +602,9 @@ inline Schedule sched_plan(int N, int Nkv, int BH, bool causal, int sms, int mod
     if (G > kSchedMaxGrid)
         G = kSchedMaxGrid;
     // Ranges of at least `need` units cut a tile of max_steps steps into at
-    // most (max_steps - 1) / need + 2 <= kSchedMaxParts parts.
-    const long long need = (max_steps - 1 + kSchedMaxParts - 3) / (kSchedMaxParts - 2);
+    // most (max_steps - 1) / need + 2 <= sched_max_parts parts.
+    const int mp = sched_max_parts(s);
+    const long long need = (max_steps - 1 + mp - 3) / (mp - 2);
     if (need > 0 && s.U / G < need)
         G = s.U / need;
     if (G < 1)

@@ -225,7 +225,7 @@ static int check_schedule(const Schedule &s, bool planned, int wl, int wr)
                     std::printf("merge slots mismatch tile %d w %d: expected %zu got %d\n", t, w, want.size(), n);
                     return 1;
                 }
-                if (planned && n > kSchedMaxParts) {
+                if (planned && n > sched_max_parts(s)) {
                     std::printf("tile %d w %d cut into %d parts\n", t, w, n);
                     return 1;
                 }

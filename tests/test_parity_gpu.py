@@ -334,3 +334,23 @@ def test_split_kv_decode_long_context(causal):
         lmax = float(np.abs(lse.cpu().double().numpy() - lse_ref).max())
         print(f"decode {schedule} causal={int(causal)}: max|dO|={emax:.3e} max|dLSE|={lmax:.3e}")
         assert emax <= TOL_O["bf16"] and lmax <= TOL_LSE
+
+
+@pytest.mark.parametrize("schedule", ["auto", "balanced"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,Nq,Nkv,D", [(1, 4, 2, 131072, 64), (1, 2, 33, 65536, 128), (2, 3, 64, 40000, 64)])
+def test_decode_many_parts(B, H, Nq, Nkv, D, causal, schedule):
+    """Few query rows against very long key sequences: the balanced schedule
+    cuts each head's key steps into up to 32 parts (heads of at most 32 rows),
+    16 (at most 64 rows) or 8, and the merge stages every part's row
+    statistics; compared in full with the oracle."""
+    q, k, v = _rect(B, H, Nq, Nkv, D, "bf16", seed=Nq + Nkv)
+    scale = D ** -0.5
+    dev = torch.device("cuda:0")
+    o, lse = fa.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale, schedule=schedule)
+    assert fa.sync_status(torch.cuda.current_stream(dev).cuda_stream) == 0
+    o_ref, lse_ref = oracle.forward_qkv(q, k, v, causal, scale)
+    emax = float(np.abs(o.cpu().double().numpy() - o_ref).max())
+    lmax = float(np.abs(lse.cpu().double().numpy() - lse_ref).max())
+    print(f"decode Nq={Nq} Nkv={Nkv} D={D} causal={int(causal)} {schedule}: max|dO|={emax:.3e} max|dLSE|={lmax:.3e}")
+    assert emax <= TOL_O["bf16"] and lmax <= TOL_LSE
