@@ -372,22 +372,31 @@ extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O
     return fa_fwd_ex(Q, K, V, O, LSE, B, H, N, D, causal, scale, dtype, FA_SCHEDULE_AUTO, stream);
 }
 
-extern "C" fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
-                            const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D, int causal,
-                            float scale, fa_dtype dtype, fa_stream_t stream)
+namespace {
+
+// Every backward entry point: N query rows against Nkv keys per head, masked
+// by the band [i' - left, i' + right], i' = i + Nkv - N (a negative bound:
+// unbounded; causal = (-1, 0), no mask = (-1, -1)).
+fa_status bwd_impl(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+                   void *dQ, void *dK, void *dV, int B, int H, int N, int Nkv, int D, int left, int right, float scale,
+                   fa_dtype dtype, fa_stream_t stream)
 {
+    int wl = left, wr = right;   // bounds that cannot bind are dropped: a band of no bounds runs unmasked
+    if (N >= 1 && Nkv >= 1)
+        fa::sched_band_normalize(N, Nkv, wl, wr);
+    const bool masked = wl < fa::kSchedUnbounded || wr < fa::kSchedUnbounded;
     // Arguments first: nothing below touches the device until they are sound.
     if (dtype != FA_BF16 && dtype != FA_FP16)
         return FA_ERR_INVALID_VALUE;
     if (D != 64 && D != 128)
         return FA_ERR_INVALID_VALUE;
-    if (B < 1 || H < 1 || N < 1 || (causal != 0 && causal != 1))
+    if (B < 1 || H < 1 || N < 1 || Nkv < 1)
         return FA_ERR_INVALID_VALUE;
     if (!std::isfinite(scale) || !(scale > 0.f))
         return FA_ERR_INVALID_VALUE;
     const long long BH = (long long)B * H;
     const long long Npad = ((long long)N + 127) / 128 * 128;
-    if (BH * Npad >= (1ll << 31))
+    if (BH * Npad >= (1ll << 31) || BH * Nkv >= (1ll << 31))
         return FA_ERR_INVALID_VALUE;
     if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV)
         return FA_ERR_INVALID_VALUE;
@@ -398,16 +407,17 @@ extern "C" fa_status fa_bwd(const void *Q, const void *K, const void *V, const v
                           reinterpret_cast<uintptr_t>(dV);
     if (any & 15u)
         return FA_ERR_MISALIGNED;
-    const size_t tbytes = (size_t)BH * N * D * 2, lbytes = (size_t)BH * N * sizeof(float);
+    const size_t qbytes = (size_t)BH * N * D * 2, kbytes = (size_t)BH * Nkv * D * 2, lbytes = (size_t)BH * N * 4;
     const void *ins[6] = {Q, K, V, O, dO, LSE};
-    const size_t in_bytes[6] = {tbytes, tbytes, tbytes, tbytes, tbytes, lbytes};
+    const size_t in_bytes[6] = {qbytes, kbytes, kbytes, qbytes, qbytes, lbytes};
     void *outs[3] = {dQ, dK, dV};
+    const size_t out_bytes[3] = {qbytes, kbytes, kbytes};
     for (int o = 0; o < 3; ++o) {   // outputs overlap no input and no other output
         for (int i = 0; i < 6; ++i)
-            if (ranges_overlap(outs[o], tbytes, ins[i], in_bytes[i]))
+            if (ranges_overlap(outs[o], out_bytes[o], ins[i], in_bytes[i]))
                 return FA_ERR_INVALID_VALUE;
         for (int o2 = o + 1; o2 < 3; ++o2)
-            if (ranges_overlap(outs[o], tbytes, outs[o2], tbytes))
+            if (ranges_overlap(outs[o], out_bytes[o], outs[o2], out_bytes[o2]))
                 return FA_ERR_INVALID_VALUE;
     }
 
@@ -428,8 +438,8 @@ extern "C" fa_status fa_bwd(const void *Q, const void *K, const void *V, const v
 
     const bool bf16 = dtype == FA_BF16;
     fa_launch::BwdLaunch a{};
-    if (!encode_map(&a.tq, Q, (int)BH, N, D, bf16) || !encode_map(&a.tk, K, (int)BH, N, D, bf16) ||
-        !encode_map(&a.tv, V, (int)BH, N, D, bf16) || !encode_map(&a.tdo, dO, (int)BH, N, D, bf16))
+    if (!encode_map(&a.tq, Q, (int)BH, N, D, bf16) || !encode_map(&a.tk, K, (int)BH, Nkv, D, bf16) ||
+        !encode_map(&a.tv, V, (int)BH, Nkv, D, bf16) || !encode_map(&a.tdo, dO, (int)BH, N, D, bf16))
         return FA_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float *ws = static_cast<float *>(bwd_workspace(dev, s, (size_t)2 * BH * Npad * sizeof(float)));
@@ -445,13 +455,35 @@ extern "C" fa_status fa_bwd(const void *Q, const void *K, const void *V, const v
     a.dl = ws + BH * Npad;
     a.BH = (int)BH;
     a.N = N;
+    a.Nkv = Nkv;
     a.Npad = (int)Npad;
     a.D = D;
     a.sms = di->sms;
     a.bf16 = bf16;
-    a.causal = causal != 0;
+    a.causal = masked;
+    a.wl = wl;
+    a.wr = wr;
     a.scale = scale;
     return fa_launch::launch_bwd(a, s, dev);
+}
+
+}  // namespace
+
+extern "C" fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                            const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D, int causal,
+                            float scale, fa_dtype dtype, fa_stream_t stream)
+{
+    if (causal != 0 && causal != 1)
+        return FA_ERR_INVALID_VALUE;
+    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, N, D, -1, causal ? 0 : -1, scale, dtype, stream);
+}
+
+extern "C" fa_status fa_bwd_band(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                                 const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nkv, int D,
+                                 int window_left, int window_right, float scale, fa_dtype dtype, fa_stream_t stream)
+{
+    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nkv, D, window_left, window_right, scale, dtype,
+                    stream);
 }
 
 extern "C" fa_status fa_sync_status(fa_stream_t stream)

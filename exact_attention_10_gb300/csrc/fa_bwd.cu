@@ -51,18 +51,26 @@ fa_status launch_all(const BwdLaunch &a, cudaStream_t s, int dev)
     p.lg = a.lg;
     p.dl = a.dl;
     p.N = a.N;
+    p.Nkv = a.Nkv;
     p.Npad = a.Npad;
     p.BH = a.BH;
-    p.nt = a.Npad / fa::bwd::kTile;
-    p.T = a.BH * p.nt;
+    p.nqt = a.Npad / fa::bwd::kTile;
+    p.nkt = (a.Nkv + fa::bwd::kTile - 1) / fa::bwd::kTile;
+    p.off = a.Nkv - a.N;
+    p.wl = a.wl;
+    p.wr = a.wr;
+    p.square_causal = (a.N == a.Nkv && a.wl >= fa::kSchedUnbounded && a.wr == 0) ? 1 : 0;
     p.qk2 = a.scale * 1.4426950408889634f;
     p.scale = a.scale;
-    const int grid = p.T < a.sms ? p.T : a.sms;
+    p.T = a.BH * p.nqt;
+    int grid = p.T < a.sms ? p.T : a.sms;
     p.dA = a.dQ;
     p.dB = nullptr;
     fa_status st = launch_pass<D, BF16, CAUSAL, false>(a.tq, a.tdo, a.tk, a.tv, p, grid, s, dev);
     if (st != FA_OK)
         return st;
+    p.T = a.BH * p.nkt;
+    grid = p.T < a.sms ? p.T : a.sms;
     p.dA = a.dK;
     p.dB = a.dV;
     return launch_pass<D, BF16, CAUSAL, true>(a.tk, a.tv, a.tq, a.tdo, p, grid, s, dev);

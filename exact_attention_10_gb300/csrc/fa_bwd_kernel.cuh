@@ -76,15 +76,20 @@ enum : uint32_t {
 };
 
 struct Params {
-    void *dA;          // KV: dK; dQ pass: dQ   ([B*H, N, D], the input type)
+    void *dA;          // KV: dK ([B*H, Nkv, D]); dQ pass: dQ ([B*H, N, D]); the input type
     void *dB;          // KV: dV; dQ pass: unused
     const float *lg;   // LSE * log2(e) per query row, [B*H][Npad]; +inf on padding rows and rows without keys
     const float *dl;   // delta = rowsum(dO o O) per query row, [B*H][Npad]
-    int N;             // rows per head (queries = keys)
+    int N;             // query rows per head
+    int Nkv;           // keys per head
     int Npad;          // N rounded up to a multiple of 128
     int BH;
-    int nt;            // 128-row tiles per head
-    int T;             // work tiles: BH * nt
+    int nqt;           // 128-row query tiles per head (Npad / 128)
+    int nkt;           // 128-key tiles per head
+    int T;             // work tiles of the pass: BH * nkt (KV) or BH * nqt (dQ pass)
+    int off;           // masked: query i sits at key position i + off (off = Nkv - N, bottom-right)
+    int wl, wr;        // masked: query i sees keys [i + off - wl, i + off + wr] (kSchedUnbounded: no bound)
+    int square_causal; // masked, N = Nkv, (unbounded, 0): tile rows go longest first
     float qk2;         // scale * log2(e)
     float scale;
 };
@@ -139,25 +144,110 @@ struct BBars {
     __device__ uint32_t p_full_dq(int g) const { return (g & 1) ? at(9) : at(3); }
 };
 
+// Streamed tiles of resident tile rt under a band mask, [s0, s0 + n): the
+// dK/dV pass's key tile sees the query tiles whose rows' bands reach one of
+// its keys, the dQ pass's query tile the key tiles its rows' bands reach.
+// An empty range still takes one (fully masked) step, so the tile's
+// gradients are written as zeros.
+template <bool KV>
+__device__ __forceinline__ void bwd_band_range(const Params &p, int rt, int &s0, int &n)
+{
+    const long long big = 1ll << 40;
+    const long long wl = p.wl >= kSchedUnbounded ? big : p.wl, wr = p.wr >= kSchedUnbounded ? big : p.wr;
+    const int ns = KV ? p.nqt : p.nkt, lim = KV ? p.N : p.Nkv;
+    long long lo, hi;
+    if (KV) {   // keys k0 .. k1; queries i with i + off - wl <= k1 and i + off + wr >= k0
+        const long long k0 = (long long)rt * kTile, k1 = min((long long)rt * kTile + kTile - 1, (long long)p.Nkv - 1);
+        lo = k0 - p.off - wr;
+        hi = k1 - p.off + wl;
+    } else {    // rows r0 .. r1 see keys r0 + off - wl .. r1 + off + wr
+        const long long r0 = (long long)rt * kTile, r1 = min((long long)rt * kTile + kTile - 1, (long long)p.N - 1);
+        lo = r0 + p.off - wl;
+        hi = r1 + p.off + wr;
+    }
+    lo = lo < 0 ? 0 : lo;
+    hi = hi > lim - 1 ? lim - 1 : hi;
+    if (lo > hi) {   // no row of the tile pair can see the other
+        s0 = (int)min(lo / kTile, (long long)ns - 1);
+        n = 1;
+    } else {
+        s0 = (int)(lo / kTile);
+        n = (int)(hi / kTile) + 1 - s0;
+    }
+}
+
 // Work tile t -> (head, resident tile index), and the streamed tiles it
-// visits, [s0, s0 + n).  Causal: the dK/dV pass's key tile kt sees query
-// tiles kt .. nt-1, the dQ pass's query tile qt sees key tiles 0 .. qt; tiles
-// go longest first, heads interleaved.  Unmasked: head-major.
+// visits, [s0, s0 + n).  Square causal: the dK/dV pass's key tile kt sees
+// query tiles kt .. nqt-1, the dQ pass's query tile qt sees key tiles 0 .. qt;
+// tiles go longest first, heads interleaved.  Otherwise head-major, with the
+// band's range when masked.
 template <bool KV>
 __device__ __forceinline__ void bwd_decode(const Params &p, bool causal, int t, int &bh, int &rt, int &s0, int &n)
 {
-    if (causal) {
+    if (causal && p.square_causal) {
         const int g = t / p.BH;
         bh = t - g * p.BH;
-        rt = KV ? g : p.nt - 1 - g;
+        rt = KV ? g : p.nqt - 1 - g;
         s0 = KV ? rt : 0;
-        n = KV ? p.nt - rt : rt + 1;
-    } else {
-        bh = t / p.nt;
-        rt = t - bh * p.nt;
-        s0 = 0;
-        n = p.nt;
+        n = KV ? p.nqt - rt : rt + 1;
+        return;
     }
+    const int nres = KV ? p.nkt : p.nqt;
+    bh = t / nres;
+    rt = t - bh * nres;
+    if (causal) {
+        bwd_band_range<KV>(p, rt, s0, n);
+    } else {
+        s0 = 0;
+        n = KV ? p.nqt : p.nkt;
+    }
+}
+
+// The band mask of one step, in terms of d = key - query: with (kt, qt) the
+// step's key and query tiles, d = 128 (kt - qt) + x where x = lane - column
+// (KV) or column - lane (dQ pass), and key j is visible from query i iff
+// e_lo <= x <= e_hi.  `whole` when every x in [-127, 127] is visible.
+struct StepMask {
+    int e_lo, e_hi;
+    bool whole;
+};
+
+// This thread's test for the step's mask, one unsigned compare per score:
+// column `col` is visible iff (uint)(a + sgn * col) < width, folding the band
+// (e_lo <= x <= e_hi with x = key - query = sgn * (col - row) ... ) and, in
+// the dQ pass, the keys past Nkv (col < limit) into `a` and `width`.
+struct LaneMask {
+    int a;
+    uint32_t width;
+};
+
+template <bool KV>
+__device__ __forceinline__ LaneMask bwd_lane_mask(const StepMask &m, int row, int limit)
+{
+    // KV: x = row - col, visible iff e_lo <= row - col <= e_hi, i.e. col in
+    //     [row - e_hi, row - e_lo]; dQ pass: x = col - row, col in
+    //     [row + e_lo, row + e_hi] and col < limit.
+    int lo = KV ? row - m.e_hi : row + m.e_lo;
+    int hi = KV ? row - m.e_lo : row + m.e_hi;
+    if (!KV && hi > limit - 1)
+        hi = limit - 1;
+    if (lo < 0)
+        lo = 0;
+    return LaneMask{-lo, hi >= lo ? (uint32_t)(hi - lo + 1) : 0u};
+}
+
+__device__ __forceinline__ StepMask bwd_step_mask(const Params &p, bool causal, int kt, int qt)
+{
+    StepMask m{-1024, 1024, true};
+    if (!causal)
+        return m;
+    const long long base = (long long)kTile * (kt - qt);
+    if (p.wl < kSchedUnbounded)
+        m.e_lo = (int)max(-1024ll, min(1024ll, (long long)p.off - p.wl - base));
+    if (p.wr < kSchedUnbounded)
+        m.e_hi = (int)max(-1024ll, min(1024ll, (long long)p.off + p.wr - base));
+    m.whole = m.e_lo <= -(kTile - 1) && m.e_hi >= kTile - 1;
+    return m;
 }
 
 // Work tiles of CTA c on a grid of G: serpentine rounds (c-th tile of even
@@ -391,12 +481,12 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
                 return;
             ptx::tc_fence_after_sync();
             const uint32_t vec = sStage + st * C::kStageBytes + 2 * C::kTileBytes;   // KV: lg[128], delta[128]
-            // Masks: the causal diagonal tile (key > query hidden) and, in the
-            // dQ pass, keys past N in the last key tile.  (Padding queries
-            // have lg = +inf, so their P is already 0.)
-            const bool diag = CAUSAL && si == rt;
-            const int key_limit = KV ? kTile : p.N - si * kTile;   // dQ pass: columns >= key_limit are past N
-            const bool masked = diag || key_limit < kTile;          // warp-uniform
+            // Masks: the band's edges (the causal diagonal) and, in the dQ
+            // pass, keys past Nkv in the last key tile.  (Padding queries and
+            // queries without keys have lg = +inf, so their P is already 0.)
+            const StepMask sm = bwd_step_mask(p, CAUSAL, KV ? rt : si, KV ? si : rt);
+            const int key_limit = KV ? kTile : p.Nkv - si * kTile;  // dQ pass: columns >= key_limit are past Nkv
+            const bool masked = !sm.whole || key_limit < kTile;     // warp-uniform
             const uint64_t qk2 = ptx::f2_pack(p.qk2, p.qk2);
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
@@ -427,12 +517,10 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
                         pr[i + e] = ptx::ex2(x[e]);
                 }
                 if (masked) {   // KV: lane = key, column = query; dQ pass: lane = query, column = key
+                    const LaneMask lm = bwd_lane_mask<KV>(sm, lane_row, key_limit);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = c0 + i;
-                        const bool hidden = KV ? (diag && lane_row > col) : ((diag && col > lane_row) || col >= key_limit);
-                        pr[i] = hidden ? 0.f : pr[i];
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        pr[i] = ((uint32_t)(lm.a + c0 + i) < lm.width) ? pr[i] : 0.f;
                 }
                 if (KV) {   // P^T, 16-bit pairs, over this chunk's first 16 columns
                     uint32_t pk[16];
@@ -478,14 +566,14 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
         const int grow = rt * kTile + lane_row;   // row within the head
         if (KV) {
             const uint32_t tA = tmem + (h ? C::kColAcc1 : C::kColAcc0) + lane_off;
-            char *dst = static_cast<char *>(h ? p.dA : p.dB) + ((size_t)bh * p.N + grow) * D * 2;
+            char *dst = static_cast<char *>(h ? p.dA : p.dB) + ((size_t)bh * p.Nkv + grow) * D * 2;
             const float mul = h ? p.scale : 1.f;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t v[32];
                 ptx::tmem_ld32(tA + 32 * cc, v);
                 ptx::tmem_wait_ld();
-                if (grow < p.N)
+                if (grow < p.Nkv)
                     store_row32<BF16>(dst + cc * 64, v, mul);
             }
         } else {
@@ -669,36 +757,44 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(b.sd_free());
             // KV: lane = key, column = query (lg and delta per column, from the
-            // stage); dQ pass: lane = query, column = key.  Masks: the causal
-            // diagonal tile, and in the dQ pass keys past N (padding queries
-            // have lg = +inf).
+            // stage); dQ pass: lane = query, column = key.  Masks: the band's
+            // edges (the causal diagonal), and in the dQ pass keys past Nkv
+            // (padding queries and queries without keys have lg = +inf).
             const uint32_t vec = sStage + (g % C::kStages) * C::kStageBytes + 2 * C::kTileBytes;
-            const int limit = KV ? kTile : p.N - si * kTile - 64 * h;   // dQ pass: columns >= limit past N
-            const bool diag = CAUSAL && si == rt;
-            const bool masked = diag || limit < 64;
+            const int limit = KV ? kTile : p.Nkv - si * kTile;   // dQ pass: columns >= limit past Nkv
+            const StepMask sm = bwd_step_mask(p, CAUSAL, KV ? rt : si, KV ? si : rt);
+            const bool masked = !sm.whole || limit < 64 * h + 64;
+            const LaneMask lm = bwd_lane_mask<KV>(sm, row, limit);
+            // Scaled scores x = S * s log2(e) - lg in place; masked steps then set
+            // hidden scores to -inf (exp2 gives 0) in a separate pass, so the
+            // main loop carries no mask code.
 #pragma unroll
             for (int i = 0; i < 64; i += 2) {
-                uint64_t nl = nlg, nd = ndl;
+                uint64_t nl = nlg;
                 if (KV) {
                     const float2 l2 = ptx::ld_shared_v2f32(vec + (uint32_t)(64 * h + i) * 4);
-                    const float2 d2 = ptx::ld_shared_v2f32(vec + kTile * 4 + (uint32_t)(64 * h + i) * 4);
                     nl = ptx::f2_pack(-l2.x, -l2.y);
-                    nd = ptx::f2_pack(-d2.x, -d2.y);
                 }
                 float x0, x1;
                 ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), qk2, nl),
                                x0, x1);
-                float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-                if (masked) {
-                    const int col = 64 * h + i;
-                    if (KV) {
-                        p0 = (diag && row > col) ? 0.f : p0;
-                        p1 = (diag && row > col + 1) ? 0.f : p1;
-                    } else {
-                        p0 = ((diag && col > row) || i >= limit) ? 0.f : p0;
-                        p1 = ((diag && col + 1 > row) || i + 1 >= limit) ? 0.f : p1;
-                    }
+                sv[i] = __float_as_uint(x0);
+                sv[i + 1] = __float_as_uint(x1);
+            }
+            if (masked) {
+                const uint32_t ninf = __float_as_uint(-INFINITY);
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    sv[i] = ((uint32_t)(lm.a + 64 * h + i) < lm.width) ? sv[i] : ninf;
+            }
+#pragma unroll
+            for (int i = 0; i < 64; i += 2) {
+                uint64_t nd = ndl;
+                if (KV) {
+                    const float2 d2 = ptx::ld_shared_v2f32(vec + kTile * 4 + (uint32_t)(64 * h + i) * 4);
+                    nd = ptx::f2_pack(-d2.x, -d2.y);
                 }
+                const float p0 = ptx::ex2(__uint_as_float(sv[i])), p1 = ptx::ex2(__uint_as_float(sv[i + 1]));
                 float d0, d1;
                 ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1),
                                            ptx::f2_add(ptx::f2_pack(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), nd)),
@@ -736,14 +832,14 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
         const int grow = rt * kTile + row;
         if (KV) {
             const uint32_t tA = tmem + (h ? C::kColAcc1 : C::kColAcc0) + lane_off;
-            char *dst = static_cast<char *>(h ? p.dA : p.dB) + ((size_t)bh * p.N + grow) * D * 2;
+            char *dst = static_cast<char *>(h ? p.dA : p.dB) + ((size_t)bh * p.Nkv + grow) * D * 2;
             const float mul = h ? p.scale : 1.f;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t v[32];
                 ptx::tmem_ld32(tA + 32 * cc, v);
                 ptx::tmem_wait_ld();
-                if (grow < p.N)
+                if (grow < p.Nkv)
                     store_row32<BF16>(dst + cc * 64, v, mul);
             }
         } else {

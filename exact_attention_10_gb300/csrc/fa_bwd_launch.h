@@ -10,13 +10,14 @@
 namespace fa_launch {
 
 struct BwdLaunch {
-    CUtensorMap tq, tk, tv, tdo;   // rank-3 maps over [B*H, N, D], 64 x 128 boxes, 128-byte swizzle
+    CUtensorMap tq, tk, tv, tdo;   // rank-3 maps over [B*H, rows, D], 64 x 128 boxes, 128-byte swizzle
     const void *O, *dO;            // [B*H, N, D], the input type
     const float *LSE;              // [B*H, N]
-    void *dQ, *dK, *dV;            // [B*H, N, D], the input type
+    void *dQ, *dK, *dV;            // dQ [B*H, N, D], dK and dV [B*H, Nkv, D], the input type
     float *lg, *dl;                // workspace: [B*H][Npad] each
-    int BH, N, Npad, D, sms;
-    bool bf16, causal;
+    int BH, N, Nkv, Npad, D, sms;   // N query rows, Nkv keys per head
+    bool bf16, causal;               // causal: masked by the band below
+    int wl, wr;                      // band: query i sees keys [i + Nkv - N - wl, i + Nkv - N + wr] (kSchedUnbounded: none)
     float scale;
 };
 

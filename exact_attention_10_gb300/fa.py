@@ -14,7 +14,7 @@ from .build import LIB_PATH
 FA_BF16, FA_FP16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_MISALIGNED", 3: "FA_ERR_UNSUPPORTED_DEVICE",
           4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT", 6: "FA_ERR_NO_ALLOC_LIMIT"}
-EXPORTS = ("fa_bwd", "fa_fwd", "fa_fwd_band", "fa_fwd_ex", "fa_fwd_noalloc", "fa_fwd_qkv", "fa_sync_status",
+EXPORTS = ("fa_bwd", "fa_bwd_band", "fa_fwd", "fa_fwd_band", "fa_fwd_ex", "fa_fwd_noalloc", "fa_fwd_qkv", "fa_sync_status",
            "fa_status_string")
 SCHEDULES = {"auto": 0, "whole_tiles": 1, "balanced": 2}
 
@@ -50,6 +50,8 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd_band.restype = c_int
     lib.fa_bwd.argtypes = [vp] * 9 + [c_int] * 5 + [ctypes.c_float, c_int, vp]
     lib.fa_bwd.restype = c_int
+    lib.fa_bwd_band.argtypes = [vp] * 9 + [c_int] * 7 + [ctypes.c_float, c_int, vp]
+    lib.fa_bwd_band.restype = c_int
     lib.fa_sync_status.argtypes = [vp]
     lib.fa_sync_status.restype = c_int
     lib.fa_status_string.argtypes = [c_int]
@@ -137,24 +139,27 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
 
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
-             stream=None):
-    """Attention backward (fa_bwd) on CUDA tensors: q, k, v, o, do [B, H, N, D]
-    and lse [B, H, N] as ``forward`` returned them; returns (dQ, dK, dV).
+             stream=None, window: tuple[int, int] | None = None):
+    """Attention backward on CUDA tensors: q, o, do [B, H, Nq, D], k, v
+    [B, H, Nkv, D] and lse [B, H, Nq] as ``forward`` returned them (same
+    causal / window); returns (dQ, dK, dV).  Square unmasked or causal calls
+    go to fa_bwd; a window, or Nq != Nkv (bottom-right causal), to fa_bwd_band.
 
     ``dq`` / ``dk`` / ``dv`` may be given to write into existing buffers.
     Raises FAError on any non-OK status.  Asynchronous on ``stream``
     (default: the current torch stream).
     """
     import torch
-    shape = q.shape
-    if q.dim() != 4 or any(x.shape != shape for x in (k, v, o, do)) or lse.shape != shape[:3]:
-        raise ValueError("q, k, v, o, do must be [B, H, N, D] and lse [B, H, N]")
+    if (q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or o.shape != q.shape or do.shape != q.shape
+            or lse.shape != q.shape[:3] or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]):
+        raise ValueError("q, o, do must be [B, H, Nq, D], k, v [B, H, Nkv, D] and lse [B, H, Nq]")
     if not all(x.is_contiguous() for x in (q, k, v, o, do, lse)):
         raise ValueError("inputs must be contiguous")
     code = _dtype_code(q)
     if any(x.dtype != q.dtype for x in (k, v, o, do)) or lse.dtype != torch.float32:
         raise TypeError("q, k, v, o, do must share a dtype; lse must be float32")
-    B, H, N, D = shape
+    B, H, N, D = q.shape
+    Nkv = k.shape[2]
     if scale is None:
         scale = D ** -0.5
     dq = torch.empty_like(q) if dq is None else dq
@@ -163,9 +168,13 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     st = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    rc = load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D, int(bool(causal)), float(scale), code,
-                       st)
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+            dk.data_ptr(), dv.data_ptr())
+    if window is None and Nkv == N:
+        rc = load().fa_bwd(*ptrs, B, H, N, D, int(bool(causal)), float(scale), code, st)
+    else:
+        left, right = window if window is not None else (-1, 0 if causal else -1)
+        rc = load().fa_bwd_band(*ptrs, B, H, N, Nkv, D, int(left), int(right), float(scale), code, st)
     if rc != 0:
         raise FAError(rc, "fa_bwd")
     return dq, dk, dv

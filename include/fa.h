@@ -246,6 +246,22 @@ FA_API fa_status fa_bwd(const void *Q, const void *K, const void *V, const void 
                         float scale, fa_dtype dtype, fa_stream_t stream);
 
 /*
+ * fa_bwd_band -- fa_bwd for Nq queries against Nkv keys under the band mask
+ * of fa_fwd_band (window_left, window_right; a negative bound is unbounded;
+ * causal = (-1, 0), no mask = (-1, -1)), from that call's O and LSE.
+ *
+ * Q, O, dO, dQ : contiguous [B, H, Nq, D];  K, V, dK, dV : contiguous
+ * [B, H, Nkv, D];  LSE : [B, H, Nq] float32.  A query that sees no key
+ * (LSE = -inf) contributes nothing and gets dQ = 0; a key that no query sees
+ * gets dK = dV = 0.  Each key tile visits only the query tiles whose bands
+ * reach it, and each query tile only the key tiles its rows' bands reach.
+ * Other arguments as for fa_bwd; B*H*Nkv must stay below 2^31 as well.
+ */
+FA_API fa_status fa_bwd_band(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                             const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nkv, int D,
+                             int window_left, int window_right, float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
  * fa_sync_status -- synchronise `stream`, then return and clear the device
  * status word of the current device: FA_OK, FA_ERR_DEVICE_TIMEOUT if a kernel
  * gave up on a wait since the last call, or FA_ERR_CUDA if the synchronise

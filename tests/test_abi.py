@@ -177,3 +177,17 @@ def test_bwd_invalid_arguments_rejected(lib):
     if not torch.cuda.is_available():
         assert call() == UNSUPPORTED
         assert call(causal=1, D=128, dtype=1) == UNSUPPORTED
+
+
+def test_bwd_band_arguments(lib):
+    """fa_bwd_band validates its sizes like fa_bwd; any window bound is valid."""
+    import ctypes
+    a = [A + i * 0x1000000 for i in range(9)]
+    for nq, nkv in ((0, 16), (16, 0), (-1, 16)):
+        rc = lib.fa_bwd_band(*a, 1, 2, nq, nkv, 64, 3, 0, ctypes.c_float(0.125), 0, None)
+        assert rc == INVALID, (nq, nkv, rc)
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        for window in ((-1, -1), (-1, 0), (0, 0), (5, -7)):
+            rc = lib.fa_bwd_band(*a, 1, 2, 16, 300, 64, window[0], window[1], ctypes.c_float(0.125), 0, None)
+            assert rc == UNSUPPORTED, (window, rc)

@@ -131,3 +131,46 @@ def test_backward_long_sequence(causal):
     grads = _gpu_grads(q, k, v, do, causal, scale)
     refs = oracle.backward(q, k, v, do, causal, scale)
     _check(grads, refs, "bf16", f"N4096 D128 causal={int(causal)}")
+
+
+BAND = [  # (B, H, Nq, Nkv, D, dtype, (left, right))
+    (1, 2, 1000, 1000, 64, "bf16", (255, 0)),     # causal sliding window
+    (1, 2, 777, 777, 128, "fp16", (100, 100)),    # two-sided, narrower than a tile
+    (1, 2, 300, 2000, 64, "bf16", (511, 0)),      # the last 300 positions of a longer sequence
+    (1, 2, 513, 200, 128, "bf16", (50, 10)),      # more queries than keys: rows without keys, keys without queries
+    (2, 2, 600, 600, 64, "bf16", (-1, 0)),        # causal through the band entry point
+    (1, 3, 129, 1000, 128, "bf16", (-1, 0)),      # Nq != Nkv, bottom-right causal
+    (1, 2, 1500, 1500, 64, "fp16", (300, -1)),    # bounded on the left only
+    (1, 2, 1000, 1000, 128, "bf16", (-1, -1)),    # no mask through the band entry point
+    (1, 2, 2048, 2048, 64, "bf16", (0, 0)),       # the diagonal alone
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nkv,D,dtype,window", BAND)
+def test_backward_band_matches_oracle(B, H, Nq, Nkv, D, dtype, window):
+    """fa_bwd_band against the oracle's band gradients, from the forward's own
+    O and LSE under the same window."""
+    q = make_custom(B, H, Nq, D, dtype, seed=Nq)[0]
+    _, k, v = make_custom(B, H, Nkv, D, dtype, seed=Nkv + 1)
+    do = make_custom(B, H, Nq, D, dtype, seed=Nq + 7)[0]
+    scale = D ** -0.5
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, scale=scale, window=window)
+    grads = fa.backward(qd, kd, vd, o, dod, lse, scale=scale, window=window)
+    rc = fa.sync_status(torch.cuda.current_stream(dev).cuda_stream)
+    assert rc == 0, fa.status_string(rc)
+    refs = oracle.backward_band(q, k, v, do, window[0], window[1], scale)
+    _check([g.cpu() for g in grads], refs, dtype, f"Nq{Nq} Nkv{Nkv} D{D} {dtype} window={window}")
+    # Rows the band leaves empty are exactly zero: queries that see no key
+    # (dQ) and keys that no query sees (dK, dV).
+    ii = np.arange(Nq)[:, None] + (Nkv - Nq)
+    jj = np.arange(Nkv)[None, :]
+    vis = np.ones((Nq, Nkv), dtype=bool)
+    if window[0] >= 0:
+        vis &= jj >= ii - window[0]
+    if window[1] >= 0:
+        vis &= jj <= ii + window[1]
+    for g, empty in zip(grads, (~vis.any(axis=1), ~vis.any(axis=0), ~vis.any(axis=0))):
+        got = g.cpu()
+        assert (got[:, :, empty] == 0).all()
