@@ -9,7 +9,9 @@ call is bracketed by CUDA events on the stream it is launched on, and L2 is
 flushed (a 256 MiB write) between calls, outside the events.
 
 Other keys: ``e2e`` (same metric through the C ABI with pinned host buffers,
-host->device and device->host copies inside the timed region), ``roofline``
+host->device and device->host copies of every step inside the timed region,
+pipelined so one step's calls overlap its neighbours' copies), ``backward``
+(fa_bwd on the same workload, per call), ``roofline``
 (the non-causal kernel against the measured bf16 tensor peak), ``clocks``
 (nvidia-smi samples taken during the timed region), ``cpu_baseline`` (the fp64
 CPU oracle on a bounded sample, timed on this host's cores).
@@ -314,34 +316,73 @@ def main(argv=None):
     value = job_tflops(world, args.steps, F[False] + F[True], total_ms)
     clk = clocks.finish()
 
-    # end to end through the C ABI: pinned host inputs in, O and LSE back out, every step
+    # End to end through the C ABI: every step copies its inputs in from pinned
+    # host memory, makes both calls, and copies both O and LSE back out.  The
+    # steps are pipelined over two sets of device buffers and three streams
+    # (copies in, calls, copies out), so step i's calls overlap step i+1's
+    # input copies and step i-1's output copies; every copy of every timed step
+    # is inside the timed region.
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     qp, kp, vp = (x.pin_memory() for x in (q_h, k_h, v_h))
-    op = torch.empty(q_h.shape, dtype=q_h.dtype).pin_memory()
-    lp = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    outs_h = {c: (torch.empty(q_h.shape, dtype=q_h.dtype).pin_memory(),
+                  torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()) for c in modes}
     h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp))
-    d2h = len(modes) * (op.numel() * op.element_size() + lp.numel() * lp.element_size())
+    d2h = sum(op_.numel() * op_.element_size() + lp_.numel() * lp_.element_size() for op_, lp_ in outs_h.values())
+    sets = [{"in": (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)),
+             "out": {c: (torch.empty_like(o), torch.empty_like(lse)) for c in modes}} for _ in range(2)]
+    s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = [{name: torch.cuda.Event() for name in ("in", "run", "out")} for _ in range(2)]
+    used = [False, False]
 
-    def e2e_step():
-        q.copy_(qp, non_blocking=True)
-        k.copy_(kp, non_blocking=True)
-        v.copy_(vp, non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        bq, bk, bv = sets[b]["in"]
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(ev[b]["run"])      # the calls of step i-2 have read this set's inputs
+            bq.copy_(qp, non_blocking=True)
+            bk.copy_(kp, non_blocking=True)
+            bv.copy_(vp, non_blocking=True)
+            ev[b]["in"].record(s_in)
+        s_run.wait_event(ev[b]["in"])
+        if used[b]:
+            s_run.wait_event(ev[b]["out"])         # step i-2's outputs have been copied out
         for c in modes:
-            call(c)
-            op.copy_(o, non_blocking=True)
-            lp.copy_(lse, non_blocking=True)
+            bo, bl = sets[b]["out"][c]
+            rc = fa.fwd_raw(bq.data_ptr(), bk.data_ptr(), bv.data_ptr(), bo.data_ptr(), bl.data_ptr(), w.B, w.H,
+                            w.N, w.D, int(c), w.scale, code, s_run.cuda_stream)
+            if rc != 0:
+                raise fa.FAError(rc, "fa_fwd")
+        ev[b]["run"].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev[b]["run"])
+            for c in modes:
+                bo, bl = sets[b]["out"][c]
+                outs_h[c][0].copy_(bo, non_blocking=True)
+                outs_h[c][1].copy_(bl, non_blocking=True)
+            ev[b]["out"].record(s_out)
+        used[b] = True
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(4):
+        e2e_step(i)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(s_out)   # after the last step's output copies
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     e2e_value = job_tflops(world, e2e_steps, F[False] + F[True], e2e_ms)
+    rc = fa.sync_status(s_run.cuda_stream)
+    if rc != 0:
+        raise fa.FAError(rc, "e2e")
+    # the last step's results, as read back, match the device-timed calls' outputs
+    for c in modes:
+        call(c)
+        torch.cuda.synchronize(dev)
+        if not (torch.equal(outs_h[c][0], o.cpu()) and torch.equal(outs_h[c][1], lse.cpu())):
+            raise RuntimeError("end-to-end results differ from the device-timed calls")
 
     # backward (fa_bwd) on the same workload, from this forward's O and LSE and
     # a seeded upstream gradient; timed per call like the forward, outside the
@@ -399,7 +440,9 @@ def main(argv=None):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "modes": mode_info, "roofline": roofline,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
+                    "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+                    "pipelined": "step i's calls overlap step i+1's input copies and step i-1's output copies "
+                                 "(two device buffer sets, three streams)"},
             "clocks": clk, "gpu_launches": args.steps * len(modes), "wall_s_timed_region": wall}
     if bwd_info is not None:
         line["backward"] = bwd_info
