@@ -1063,13 +1063,15 @@ __device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl 
                 }
                 if (valid)
                     p.LSE[(size_t)bh * p.N + row] = (st.x + log2f(st.y)) * kLn2;
-            } else {
+            } else {   // a part of a split tile: the partial result of the valid rows (the merge reads no other)
                 float *prow = p.part_o + ((size_t)pt.slot * kCtaRows + w * kBM + t) * D;
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     uint32_t o[32];
-                    ptx::tmem_ld32(tO + q * 32, o);
+                    ptx::tmem_ld32(tO + q * 32, o);   // (warp-collective: every lane loads)
                     ptx::tmem_wait_ld();
+                    if (!valid)
+                        continue;
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         float x0, x1, x2, x3;
@@ -1081,7 +1083,8 @@ __device__ void epilogue_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl 
                                           __float_as_uint(x2), __float_as_uint(x3));
                     }
                 }
-                p.part_ml[(size_t)pt.slot * kCtaRows + w * kBM + t] = st;
+                if (valid)
+                    p.part_ml[(size_t)pt.slot * kCtaRows + w * kBM + t] = st;
                 published |= 1u << w;
             }
             ptx::tc_fence_before_sync();

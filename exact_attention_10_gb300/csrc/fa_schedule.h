@@ -533,7 +533,8 @@ FA_HD int sched_part_slots(const Schedule &s, int t, int nw, int *slots, int max
 // for causal attention, whose short tiles lose to those costs (measured).
 // With few long tiles -- decoding a few queries against many keys -- whole
 // tiles would leave most SMs idle, and the balanced schedule (split-KV) is
-// taken whenever it at least halves the makespan.
+// taken whenever it at least halves the makespan; for heads of at most 64
+// query rows, whose merges are cheap, whenever it saves more than 10 %.
 constexpr int kSchedMinGain = 4;
 
 // mode: 0 = as above, 1 = round-robin, 2 = balanced wherever it can be built.
@@ -613,7 +614,10 @@ inline Schedule sched_plan(int N, int Nkv, int BH, bool causal, int sms, int mod
     const bool many_tiles = !causal && balanced >= 2LL * max_steps && rr * 100 > balanced * 104 &&
                             rr - balanced >= kSchedMinGain;
     const bool few_long_tiles = 2LL * s.T <= sms && max_steps >= 32 && rr >= 2 * balanced;
-    const bool pays = many_tiles || few_long_tiles;
+    // decoding-sized heads (at most 64 query rows) merge cheaply: balance
+    // whenever it shortens the makespan by more than 10 %
+    const bool short_heads = N <= kSchedShortRows && rr * 100 > balanced * 110;
+    const bool pays = many_tiles || few_long_tiles || short_heads;
     if (mode == 2 || pays) {
         s.split = 1;
         s.G = (int)G;
