@@ -105,29 +105,55 @@ struct BCfg {
     static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;   // a multiple of 1024
     static constexpr int kResOff = 0;                                 // the resident pair of tiles
     static constexpr int kStageOff = 2 * kTileBytes;
-    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-    // full[kStages], empty[kStages], res_full, res_empty, sd_full, p_full, acc_full, acc_free, drain, sd_free,
-    // pd_free, p_full_odd
-    static constexpr int kNumBars = 2 * kStages + 10;
+    // The dQ pass at D = 128 streams K and V through separate rings, 3 slots
+    // of K and 2 of V, instead of 2 stages of both: V is done with once dP is
+    // computed, K only after the step's dQ product, and the third K slot lets
+    // the next steps' tiles load while it runs.  (Both rings: 224 KB with the
+    // resident Q and dO.)
+    static constexpr bool kSplitRing = !KV && D == 128;
+    static constexpr int kRing0 = kSplitRing ? 3 : kStages;   // slots of streamed tile 0 (KV: Q; dQ pass: K)
+    static constexpr int kRing1 = kSplitRing ? 2 : kStages;   // slots of streamed tile 1 (KV: dO; dQ pass: V)
+    static constexpr int kRing1Off = kStageOff + kRing0 * kTileBytes;   // split rings: tile 1's ring
+    static constexpr int kBarOff = kSplitRing ? kRing1Off + kRing1 * kTileBytes : kStageOff + kStages * kStageBytes;
+    // full/empty per slot (unified stages, or ring 0 then ring 1), then res_full, res_empty,
+    // sd_full, p_full, acc_full, acc_free, drain, sd_free, pd_free, p_full_odd
+    static constexpr int kRingBars = kSplitRing ? 2 * (kRing0 + kRing1) : 2 * kStages;
+    static constexpr int kNumBars = kRingBars + 10;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;           // TMEM address, abort flag
     static constexpr int kSmem = kMiscOff + 16 + 1024;                // + slack to align the base to 1024
     static_assert(kSmem <= 232448, "shared memory per CTA");
     static_assert(kStageBytes % 1024 == 0, "stages keep the tiles' 1024-byte swizzle alignment");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
-    // Pipelined passes (D = 64): dQ pass: two 64-column dS buffers after dQ (dS of
-    // step g in buffer g % 2); KV pass: one P^T and one dS^T buffer after dV, dK.
+    // Pipelined passes: dQ pass: two 64-column dS buffers after dQ (dS of step g
+    // in buffer g % 2); KV pass (D = 64): one P^T and one dS^T buffer after dV, dK.
     static constexpr uint32_t kColDS = KV ? 256 + 2 * D + 64 : 256 + D;
     static constexpr uint32_t kColP = 256 + 2 * D;
-    static_assert(D != 64 || (KV ? kColDS + 64 : kColDS + 128) <= kTmemCols, "pipelined buffers fit TMEM");
+    static_assert((KV && D == 128) || (KV ? kColDS + 64 : kColDS + 128) <= kTmemCols, "pipelined buffers fit TMEM");
+    // Shared-memory address of streamed tile 0 / 1 of global step g.
+    __device__ static uint32_t slot0(uint32_t sStage, int g)
+    {
+        return kSplitRing ? sStage + (uint32_t)((g % kRing0) * kTileBytes) : sStage + (uint32_t)((g % kStages) * kStageBytes);
+    }
+    __device__ static uint32_t slot1(uint32_t sStage, int g)
+    {
+        return kSplitRing ? sStage + (uint32_t)(kRing1Off - kStageOff + (g % kRing1) * kTileBytes)
+                          : slot0(sStage, g) + (uint32_t)kTileBytes;
+    }
 };
 
 template <int D, bool KV>
 struct BBars {
     uint32_t base;
-    __device__ uint32_t full(int s) const { return base + 8u * s; }
-    __device__ uint32_t empty(int s) const { return base + 8u * (BCfg<D, KV>::kStages + s); }
-    __device__ uint32_t at(int k) const { return base + 8u * (2 * BCfg<D, KV>::kStages + k); }
+    using C = BCfg<D, KV>;
+    __device__ uint32_t full(int s) const { return base + 8u * s; }                    // slot s of ring 0 / stage s
+    __device__ uint32_t empty(int s) const { return base + 8u * (C::kRing0 + s); }
+    __device__ uint32_t full1(int s) const { return C::kSplitRing ? base + 8u * (2 * C::kRing0 + s) : full(s); }
+    __device__ uint32_t empty1(int s) const
+    {
+        return C::kSplitRing ? base + 8u * (2 * C::kRing0 + C::kRing1 + s) : empty(s);
+    }
+    __device__ uint32_t at(int k) const { return base + 8u * (C::kRingBars + k); }
     __device__ uint32_t res_full() const { return at(0); }    // TMA -> MMA: resident tiles landed
     __device__ uint32_t res_empty() const { return at(1); }   // MMA -> TMA: the tile's last MMAs done
     __device__ uint32_t sd_full() const { return at(2); }     // MMA -> compute: S and dP of a step ready
@@ -302,13 +328,32 @@ __device__ void bwd_load(const CUtensorMap *tmR0, const CUtensorMap *tmR1, const
         __syncwarp();
         ++tiles;
         for (int j = 0; j < n; ++j, ++step) {
+            const int row = (s0 + j) * kTile;
+            if (C::kSplitRing) {   // K into ring 0, V into ring 1, each on its own barriers
+                const int k0 = step % C::kRing0, k1 = step % C::kRing1;
+                if (!warp_wait(b.empty(k0), ((uint32_t)(step / C::kRing0) & 1u) ^ 1u, c, kSiteBwdSlotEmpty) ||
+                    !warp_wait(b.empty1(k1), ((uint32_t)(step / C::kRing1) & 1u) ^ 1u, c, kSiteBwdSlotEmpty)) {
+                    ok = false;
+                    break;
+                }
+                if (ptx::elect_one()) {
+                    const uint32_t d0 = C::slot0(sStage, step), d1 = C::slot1(sStage, step);
+                    ptx::mbar_arrive_expect_tx(b.full(k0), C::kTileBytes);
+                    ptx::mbar_arrive_expect_tx(b.full1(k1), C::kTileBytes);
+                    for (int x = 0; x < C::kBoxes; ++x) {
+                        ptx::tma_load_3d(d0 + x * C::kBoxBytes, tmS0, b.full(k0), x * 64, row, bh);
+                        ptx::tma_load_3d(d1 + x * C::kBoxBytes, tmS1, b.full1(k1), x * 64, row, bh);
+                    }
+                }
+                __syncwarp();
+                continue;
+            }
             const int st = step % C::kStages;
             const uint32_t use = (uint32_t)(step / C::kStages);
             if (!warp_wait(b.empty(st), (use & 1u) ^ 1u, c, kSiteBwdSlotEmpty)) {
                 ok = false;
                 break;
             }
-            const int row = (s0 + j) * kTile;
             if (ptx::elect_one()) {
                 const uint32_t dst = sStage + st * C::kStageBytes;
                 ptx::mbar_arrive_expect_tx(b.full(st), C::kStageBytes);
@@ -327,9 +372,13 @@ __device__ void bwd_load(const CUtensorMap *tmR0, const CUtensorMap *tmR1, const
     }
     // Tail: every copy issued has landed (time-bounded), so no asynchronous
     // write targets this CTA's shared memory after exit.
-    for (int s = 0; s < C::kStages && s < step; ++s) {
-        const int last = step - 1 - ((step - 1 - s) % C::kStages);
-        wait_landed(b.full(s), (uint32_t)(last / C::kStages) & 1u, c, kSiteBwdTail);
+    for (int s = 0; s < C::kRing0 && s < step; ++s) {
+        const int last = step - 1 - ((step - 1 - s) % C::kRing0);
+        wait_landed(b.full(s), (uint32_t)(last / C::kRing0) & 1u, c, kSiteBwdTail);
+    }
+    for (int s = 0; C::kSplitRing && s < C::kRing1 && s < step; ++s) {
+        const int last = step - 1 - ((step - 1 - s) % C::kRing1);
+        wait_landed(b.full1(s), (uint32_t)(last / C::kRing1) & 1u, c, kSiteBwdTail);
     }
     if (tiles > 0)
         wait_landed(b.res_full(), (uint32_t)(tiles - 1) & 1u, c, kSiteBwdTail);
@@ -604,8 +653,8 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
 // 840 TFLOP/s at N = 16384), and the KV pass has no TMEM left for separate
 // P^T / dS^T buffers at D = 128; so D = 128 keeps the serialized step
 // (S and dP, compute, accumulating products).
-template <int D>
-constexpr bool kPipeline = (D == 64);
+template <int D, bool KV>
+constexpr bool kPipeline = (D == 64) || (!KV && D == 128);
 
 // The dQ pass overlaps the compute warps with the tensor core: as soon as the
 // compute warps have loaded S_g and dP_g into registers (sd_free), the next
@@ -631,14 +680,14 @@ __device__ void bwd_mma_pipe(const Params &p, bool causal, uint32_t sRes, uint32
     // S_g = R0 S0_g^T and dP_g = R1 S1_g^T into their columns (the previous
     // step's S and dP must have been loaded by the compute warps).
     auto issue_sd = [&](int gs) -> bool {
-        const int st = gs % C::kStages;
         if (gs > 0 && !warp_wait(b.sd_free(), (uint32_t)(gs - 1) & 1u, c, kSiteBwdSdFree))
             return false;
-        if (!warp_wait(b.full(st), (uint32_t)(gs / C::kStages) & 1u, c, kSiteBwdSlotFull))
+        if (!warp_wait(b.full(gs % C::kRing0), (uint32_t)(gs / C::kRing0) & 1u, c, kSiteBwdSlotFull))
+            return false;
+        if (C::kSplitRing && !warp_wait(b.full1(gs % C::kRing1), (uint32_t)(gs / C::kRing1) & 1u, c, kSiteBwdSlotFull))
             return false;
         ptx::tc_fence_after_sync();
-        const uint32_t sa = sStage + st * C::kStageBytes;
-        const uint32_t s0_lo = desc_lo(sa, 16), s1_lo = desc_lo(sa + C::kTileBytes, 16);
+        const uint32_t s0_lo = desc_lo(C::slot0(sStage, gs), 16), s1_lo = desc_lo(C::slot1(sStage, gs), 16);
         if (ptx::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -651,6 +700,8 @@ __device__ void bwd_mma_pipe(const Params &p, bool causal, uint32_t sRes, uint32
                 ptx::mma_ss(tDP, desc_from_lo(r1_lo + off), desc_from_lo(s1_lo + off), kIdescSS, kk > 0 ? 1u : 0u);
             }
             ptx::mma_commit(b.sd_full());
+            if (C::kSplitRing)
+                ptx::mma_commit(b.empty1(gs % C::kRing1));   // V's slot is free once dP is computed
         }
         __syncwarp();
         return true;
@@ -684,14 +735,13 @@ __device__ void bwd_mma_pipe(const Params &p, bool causal, uint32_t sRes, uint32
                 break;
             }
             ptx::tc_fence_after_sync();
-            const int st = g % C::kStages;
+            const int st = g % C::kRing0;
             // KV:  dV += P^T_g dO_g, dK += dS^T_g Q_g;  dQ pass: dQ += dS_g K_g.
             // The A operand comes from a TMEM buffer (8 columns per 16 rows of the
             // streamed tile), the B operand is the streamed tile read MN-major
             // (16 rows = 2 KB per k-step).
-            const uint32_t sa = sStage + st * C::kStageBytes;
-            const uint32_t m0_lo = desc_lo(sa + (KV ? C::kTileBytes : 0), C::kBoxBytes);   // KV: dO; dQ: K
-            const uint32_t m1_lo = desc_lo(sa, C::kBoxBytes);                               // KV: Q
+            const uint32_t m0_lo = desc_lo(KV ? C::slot1(sStage, g) : C::slot0(sStage, g), C::kBoxBytes);   // KV: dO; dQ: K
+            const uint32_t m1_lo = desc_lo(C::slot0(sStage, g), C::kBoxBytes);                               // KV: Q
             const uint32_t tA0 = tmem + (KV ? C::kColP : C::kColDS + 64u * (uint32_t)(g & 1));
             const uint32_t tA1 = tmem + C::kColDS;
             if (ptx::elect_one()) {
@@ -884,9 +934,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < C::kRing0; ++s) {
             ptx::mbar_init(b.full(s), 1);
             ptx::mbar_init(b.empty(s), 1);
+        }
+        for (int s = 0; C::kSplitRing && s < C::kRing1; ++s) {
+            ptx::mbar_init(b.full1(s), 1);
+            ptx::mbar_init(b.empty1(s), 1);
         }
         ptx::mbar_init(b.res_full(), 1);
         ptx::mbar_init(b.res_empty(), 1);
@@ -918,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x < kComputeThreads) {
         ptx::regs_increase<kRegsCompute>();
-        if constexpr (kPipeline<D>)
+        if constexpr (kPipeline<D, KV>)
             bwd_compute_pipe<D, BF16, CAUSAL, KV>(p, tmem, sStage, b, c);
         else
             bwd_compute<D, BF16, CAUSAL, KV>(p, tmem, sStage, b, c);
@@ -928,7 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bwd_load<D, KV>(&tmR0, &tmR1, &tmS0, &tmS1, p, CAUSAL, sRes, sStage, b, c);
         else if (warp == kMmaWarp)
         {
-            if constexpr (kPipeline<D>)
+            if constexpr (kPipeline<D, KV>)
                 bwd_mma_pipe<D, BF16, KV>(p, CAUSAL, sRes, sStage, tmem, b, c);
             else
                 bwd_mma<D, BF16, KV>(p, CAUSAL, sRes, sStage, tmem, b, c);
