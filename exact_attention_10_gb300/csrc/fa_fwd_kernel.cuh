@@ -150,6 +150,12 @@ struct Cfg {
     static constexpr int kTileBytes = kBM * D * 2;     // one [128, D] 16-bit tile
     static constexpr int kStages = (D == 64) ? 4 : 2;  // K/V ring depth; a stage holds K_j and V_j
     static constexpr int kStageBytes = 2 * kTileBytes;
+    // At D = 128 (two stages), in the separate-P order of heads of one Q
+    // tile, a stage's K and V land and are released on barriers of their
+    // own: K once the step's S MMA read it, V once its P.V did, and the
+    // producer loads K one step ahead of V.  (The two-tile interleaved order
+    // keeps whole stages: two tiles' work per step already hides the loads.)
+    static constexpr bool kSplitKV = (D == 128);
     static constexpr int kQBufs = (D == 64) ? 2 : 1;   // Q buffers: the next CTA tile's Q loads early
     static constexpr int kQBufBytes = kQTiles * kTileBytes;
     static constexpr int kQOff = 0;
@@ -167,16 +173,28 @@ struct Cfg {
     static constexpr int kMergeOff = (kMiscOff + 16 + 127) & ~127;
     static constexpr int kMlOff = kMergeOff + kMergeBufs * kMergeOBytes;
     static constexpr int kJobOff = kMlOff + kMlBytes;
-    // Shared memory of a launch (+ slack to align the base to 1024): the
-    // whole-tile variant has no merge area.
-    static constexpr int kSmemSplit = kJobOff + kJobSlots * (int)sizeof(MergeJob) + 1024;
-    static constexpr int kSmemWhole = kMiscOff + 16 + 1024;
+    // The split ring's V barriers, v_full[kStages] and v_empty[kStages], come
+    // after everything else (the merge area, which whole-tile launches do not
+    // have): moving the other barriers by their 32 bytes measured 4.6 %
+    // slower on long causal calls at D = 128.
+    static constexpr int kVBarBytes = kSplitKV ? 16 * kStages : 0;
+    __host__ __device__ static constexpr int vbar_off(bool split)
+    {
+        return split ? ((kJobOff + kJobSlots * (int)sizeof(MergeJob) + 7) & ~7) : kMiscOff + 16;
+    }
+    // Shared memory of a launch (+ slack to align the base to 1024).
+    static constexpr int kSmemSplit = vbar_off(true) + kVBarBytes + 1024;
+    static constexpr int kSmemWhole = vbar_off(false) + kVBarBytes + 1024;
     __host__ __device__ static constexpr int smem_bytes(bool split) { return split ? kSmemSplit : kSmemWhole; }
     static_assert(kSmemSplit <= 232448 && kSmemWhole <= kSmemSplit, "shared memory per CTA");
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t col_s(int w) { return w ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t col_o(int w) { return w ? 256u + D : 256u; }
     __host__ __device__ static constexpr uint32_t col_p(int w) { return kSeparateP ? (w ? 448u : 384u) : col_s(w); }
+    // At D = 128 a launch whose heads have at most 128 query rows (decoding)
+    // leaves Q tile 1 idle, so P_0 takes tile 1's S columns and the steps run
+    // in the separate-P order of D = 64.
+    __host__ __device__ static constexpr uint32_t col_p_one_tile() { return col_s(1); }
 };
 
 struct FwdParams {
@@ -191,6 +209,21 @@ struct FwdParams {
     float2 *part_ml;     // balanced schedule: partial (m, l) per row, [2 * grid slots][256]
     int *counters;       // balanced schedule: finished parts per (tile, Q tile), zero between launches
 };
+
+// Separate-P order (S_{j+1} issued while the softmax of step j runs): always
+// at D = 64; at D = 128 when no CTA tile has a second Q tile.
+template <int D>
+__device__ __forceinline__ bool separate_p(const FwdParams &p)
+{
+    return Cfg<D>::kSeparateP || p.N <= kBM;
+}
+
+// K and V of a stage on separate barriers (D = 128, separate-P order).
+template <int D>
+__device__ __forceinline__ bool split_kv(const FwdParams &p)
+{
+    return Cfg<D>::kSplitKV && p.N <= kBM;
+}
 
 // Shared-memory matrix descriptor (tcgen05), 128-byte swizzle, 8-row groups
 // 1024 bytes apart (stride byte offset), `lbo` = leading byte offset.
@@ -232,6 +265,9 @@ static __device__ __noinline__ void record_timeout(Ctl c, uint32_t site)
 // hardware.)  kSuspendNs is the hint for waits bounded by time alone.
 constexpr uint32_t kSuspendNs = 20000;
 
+// INLINE: record a timeout without a call, for waits that hold many live
+// registers (a call there makes the caller save them around it, as spills).
+template <bool INLINE = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Ctl c, uint32_t site)
 {
     if (ptx::mbar_try_wait(bar, parity))
@@ -244,7 +280,12 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Ctl 
             if (*c.abort_flag)
                 return false;
             if (ptx::global_timer_ns() - t0 > kWaitLimitNs) {
-                record_timeout(c, site);
+                if (INLINE) {
+                    *c.abort_flag = 1;
+                    atomicCAS(&g_status_word, 0u, 1u | (site << 8));
+                } else {
+                    record_timeout(c, site);
+                }
                 return false;
             }
         }
@@ -252,17 +293,23 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Ctl 
 }
 
 // Bounded wait by a whole warp; the outcome is warp-uniform.
+template <bool INLINE = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c, uint32_t site)
 {
-    const bool ok = wait_bounded(bar, parity, c, site);
+    const bool ok = wait_bounded<INLINE>(bar, parity, c, site);
     return __all_sync(0xffffffffu, ok);
 }
 
 template <int D>
 struct Bars {
     uint32_t base;
-    __device__ uint32_t full(int s) const { return base + 8u * s; }                          // TMA -> MMA: stage s landed
-    __device__ uint32_t empty(int s) const { return base + 8u * (Cfg<D>::kStages + s); }     // MMA -> TMA: stage s read
+    uint32_t vbase;   // the split ring's V barriers
+    // TMA -> MMA: stage s landed (K_j alone when K and V are split)
+    __device__ uint32_t full(int s) const { return base + 8u * s; }
+    // MMA -> TMA: stage s read (K_j alone when split)
+    __device__ uint32_t empty(int s) const { return base + 8u * (Cfg<D>::kStages + s); }
+    __device__ uint32_t v_full(int s) const { return vbase + 8u * s; }                          // split: V_j landed
+    __device__ uint32_t v_empty(int s) const { return vbase + 8u * (Cfg<D>::kStages + s); }     // split: V_j read
     __device__ uint32_t q_full(int qb) const { return base + 8u * (2 * Cfg<D>::kStages + qb); }
     __device__ uint32_t q_empty(int qb) const { return base + 8u * (2 * Cfg<D>::kStages + Cfg<D>::kQBufs + qb); }
     __device__ uint32_t per_tile(int w, int k) const
@@ -270,7 +317,7 @@ struct Bars {
         return base + 8u * (2 * Cfg<D>::kStages + 2 * Cfg<D>::kQBufs + kPerTileBars * w + k);
     }
     __device__ uint32_t s_full(int w) const { return per_tile(w, 0); }     // MMA -> softmax: S_w ready
-    __device__ uint32_t s_free(int w) const { return per_tile(w, 1); }     // softmax -> MMA: S_w loaded (D = 64)
+    __device__ uint32_t s_free(int w) const { return per_tile(w, 1); }     // softmax -> MMA: S_w loaded (separate-P order)
     __device__ uint32_t p_full(int w) const { return per_tile(w, 2); }     // softmax -> MMA: P_w written, O_w rescaled
     __device__ uint32_t o_done(int w) const { return per_tile(w, 3); }     // MMA -> softmax, epilogue: P.V done
     __device__ uint32_t st_ready(int w) const { return per_tile(w, 4); }   // softmax -> epilogue: final (m, l) written
@@ -287,21 +334,44 @@ struct Bars {
 
 // TMA producer, run by a whole warp; one elected lane issues the copies.
 // Per CTA tile: both Q tiles into the Q buffer, then for each step j the
-// pair K_j, V_j into the next stage of the ring.
-template <int D, int MASK, bool SPLIT>
+// pair K_j, V_j into the next stage of the ring.  With K and V split, the
+// copies go K_0, K_1, V_0, K_2, V_1, ... (V_j after K_{j+1} within a part),
+// each half waiting only for its own half of the stage.
+// SKV: K and V of a stage on separate barriers (split_kv).
+template <int D, int MASK, bool SPLIT, bool SKV>
 __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
                           const FwdParams &p, uint32_t sQ, uint32_t sStage, Bars<D> b, Ctl c)
 {
     using C = Cfg<D>;
-    int step = 0;   // K/V stages filled so far
+    int step = 0;   // K/V stages filled so far (K halves when split)
     int it = 0;     // parts started by this CTA (one Q load each)
+    int nv = 0;     // split: V halves filled so far; V of step nv is pending while nv < step
+    int pv_bh = 0, pv_row = 0;   // ... its head and first key
     bool ok = true;
+    auto load_v = [&]() -> bool {
+        const int st = nv % C::kStages;
+        const uint32_t use = (uint32_t)(nv / C::kStages);
+        if (!warp_wait(b.v_empty(st), (use & 1u) ^ 1u, c, kSiteLoadSlotEmpty))
+            return false;
+        if (ptx::elect_one()) {
+            const uint32_t dst = sStage + st * C::kStageBytes + C::kTileBytes;
+            ptx::mbar_arrive_expect_tx(b.v_full(st), C::kTileBytes);
+            for (int x = 0; x < C::kBoxes; ++x)
+                ptx::tma_load_3d(dst + x * C::kBoxBytes, tmV, b.v_full(st), x * 64, pv_row, pv_bh);
+        }
+        __syncwarp();
+        ++nv;
+        return true;
+    };
     PartIter parts;
     parts.init_t<SPLIT>(p.sch, blockIdx.x);
     Part pt;
     while (ok && parts.next_t<SPLIT, MASK == kMaskBand>(p.sch, pt)) {
         int bh, ct;
         sched_decode_t<SPLIT, MASK == kMaskBand>(p.sch, pt.tile, bh, ct);
+        // The previous part's last V before the Q buffer is waited for: the
+        // MMA warp frees that buffer only after the part's last P.V.
+        if (SKV && nv < step && !load_v()) { ok = false; break; }
         const int qb = it % C::kQBufs;
         const uint32_t quse = (uint32_t)(it / C::kQBufs);
         if (!warp_wait(b.q_empty(qb), (quse & 1u) ^ 1u, c, kSiteLoadQEmpty)) { ok = false; break; }
@@ -322,16 +392,24 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
             if (!warp_wait(b.empty(st), (use & 1u) ^ 1u, c, kSiteLoadSlotEmpty)) { ok = false; break; }
             if (ptx::elect_one()) {
                 const uint32_t dst = sStage + st * C::kStageBytes;
-                ptx::mbar_arrive_expect_tx(b.full(st), C::kStageBytes);
+                ptx::mbar_arrive_expect_tx(b.full(st), SKV ? C::kTileBytes : C::kStageBytes);
                 for (int x = 0; x < C::kBoxes; ++x)
                     ptx::tma_load_3d(dst + x * C::kBoxBytes, tmK, b.full(st), x * 64, (ks + j) * kBN, bh);
-                for (int x = 0; x < C::kBoxes; ++x)
-                    ptx::tma_load_3d(dst + C::kTileBytes + x * C::kBoxBytes, tmV, b.full(st), x * 64, (ks + j) * kBN,
-                                     bh);
+                if (!SKV)
+                    for (int x = 0; x < C::kBoxes; ++x)
+                        ptx::tma_load_3d(dst + C::kTileBytes + x * C::kBoxBytes, tmV, b.full(st), x * 64,
+                                         (ks + j) * kBN, bh);
             }
             __syncwarp();
+            if (SKV) {   // V of the previous step, then this step's V becomes the pending one
+                if (nv < step && !load_v()) { ++step; ok = false; break; }
+                pv_bh = bh;
+                pv_row = (ks + j) * kBN;
+            }
         }
     }
+    if (SKV && ok && nv < step)   // the last step's V
+        load_v();
     // Tail: every copy issued has landed and (unless aborting) every stage and
     // the Q buffer have been released by the MMA warp, so no asynchronous
     // write or arrive targets this CTA's shared memory after exit.
@@ -341,6 +419,13 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
         warp_wait(b.full(s), use & 1u, c, kSiteTail);
         if (!*c.abort_flag)
             warp_wait(b.empty(s), use & 1u, c, kSiteTail);
+    }
+    for (int s = 0; SKV && s < C::kStages && s < nv; ++s) {
+        const int last = nv - 1 - ((nv - 1 - s) % C::kStages);
+        const uint32_t use = (uint32_t)(last / C::kStages);
+        warp_wait(b.v_full(s), use & 1u, c, kSiteTail);
+        if (!*c.abort_flag)
+            warp_wait(b.v_empty(s), use & 1u, c, kSiteTail);
     }
     for (int qb = 0; qb < C::kQBufs && qb < it; ++qb) {
         const int last = it - 1 - ((it - 1 - qb) % C::kQBufs);   // last CTA tile that used Q buffer qb
@@ -377,7 +462,7 @@ __device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo)
 // as tcgen05.commit tracks the MMAs of the lane that issued them) issues the
 // tcgen05.mma and tcgen05.commit instructions.  Tile-level ping-pong between
 // the two softmax warpgroups falls out of the two independent MMA streams.
-template <int D, bool BF16>
+template <int D, bool BF16, bool SEP>
 struct MmaIssuer {
     using C = Cfg<D>;
     static constexpr uint32_t kIdescQK = instr_desc_f16(BF16, kBM, kBN, false);   // S = Q K^T, both K-major
@@ -401,8 +486,19 @@ struct MmaIssuer {
         return true;
     }
 
-    // Release a stage once this warp's MMAs reading it have completed (the
-    // empty barrier expects one such arrival from each MMA warp).
+    // Split K and V: wait for V of `step` (K is what stage_wait waits for).
+    __device__ bool v_wait(int step) const
+    {
+        const int st = step % C::kStages;
+        if (!warp_wait(b.v_full(st), (uint32_t)(step / C::kStages) & 1u, c, kSiteMmaSlotFull))
+            return false;
+        ptx::tc_fence_after_sync();
+        return true;
+    }
+
+    // Release a stage (its K half when split) once this warp's MMAs reading
+    // it have completed (the empty barrier expects one such arrival from
+    // each MMA warp).
     __device__ void release(int st) const
     {
         if (ptx::elect_one())
@@ -410,11 +506,19 @@ struct MmaIssuer {
         __syncwarp();
     }
 
+    // Split K and V: release the V half of a stage.
+    __device__ void release_v(int st) const
+    {
+        if (ptx::elect_one())
+            ptx::mma_commit(b.v_empty(st));
+        __syncwarp();
+    }
+
     // S_w = Q_w K^T over D/16 k-steps: K-major operands advance 32 bytes per
     // step inside a 128-byte swizzle row and 16 KB per 64-column box.
     __device__ bool issue_s(int st)
     {
-        if (C::kSeparateP && n_s > 0) {   // the softmax has loaded the previous S_w
+        if (SEP && n_s > 0) {   // the softmax has loaded the previous S_w
             if (!warp_wait(b.s_free(w), (n_s - 1) & 1u, c, kSiteMmaSFree))
                 return false;
             ptx::tc_fence_after_sync();
@@ -458,41 +562,39 @@ struct MmaIssuer {
         return true;
     }
 
-    // One CTA tile: steps 0..n-1 of the K/V stream, of which Q tile w uses the
-    // first nw.  Every stage is released by this warp, used or not.
+    // One CTA tile in the separate-P order: S_w of step j+1 as soon as the
+    // softmax has loaded S_w(j), then P.V of step j.  Steps 0..n-1 of the K/V
+    // stream, of which Q tile w uses the first nw; every stage is waited for
+    // and released by this warp, used or not.  (At D = 128 this order runs
+    // only for heads of one Q tile, whose stages are split into K and V.)
     __device__ bool tile(int step0, int n, int nw)
     {
         int st;
-        if (C::kSeparateP) {
-            // D = 64 order: S_w of step j+1 as soon as the softmax has loaded S_w(j),
-            // then P.V of step j.
-            if (!stage_wait(step0, st))
-                return false;
-            if (nw > 0 && !issue_s(st))
-                return false;
-            for (int j = 0; j < n; ++j) {
-                int st_next = st;
-                if (j + 1 < n) {
-                    if (!stage_wait(step0 + j + 1, st_next))
-                        return false;
-                    if (j + 1 < nw && !issue_s(st_next))
-                        return false;
-                }
-                if (j < nw && !issue_pv(st, j > 0))
+        if (!stage_wait(step0, st))
+            return false;
+        if (nw > 0 && !issue_s(st))
+            return false;
+        if (C::kSplitKV)
+            release(st);   // K_0 read
+        for (int j = 0; j < n; ++j) {
+            int st_next = st;
+            if (j + 1 < n) {
+                if (!stage_wait(step0 + j + 1, st_next))
                     return false;
-                release(st);
-                st = st_next;
+                if (j + 1 < nw && !issue_s(st_next))
+                    return false;
+                if (C::kSplitKV)
+                    release(st_next);   // K_{j+1} read
             }
-        } else {
-            // D = 128 order: S_w(j), then P.V_w(j) once P_w(j) overwrote S_w(j) in TMEM;
-            // S_w(j+1) follows in issue order.
-            for (int j = 0; j < n; ++j) {
-                if (!stage_wait(step0 + j, st))
-                    return false;
-                if (j < nw && (!issue_s(st) || !issue_pv(st, j > 0)))
-                    return false;
+            if (C::kSplitKV && !v_wait(step0 + j))
+                return false;
+            if (j < nw && !issue_pv(st, j > 0))
+                return false;
+            if (C::kSplitKV)
+                release_v(st);   // V_j read
+            else
                 release(st);
-            }
+            st = st_next;
         }
         return true;
     }
@@ -502,7 +604,8 @@ struct MmaIssuer {
 // so each softmax warpgroup works while the tensor core runs the other
 // tile's MMAs, and P_w(j) overwrites S_w(j) in TMEM before S_w(j+1) is issued.
 template <int D, bool BF16>
-__device__ bool tile_interleaved(MmaIssuer<D, BF16> &m0, MmaIssuer<D, BF16> &m1, int step0, int n, int n0, int n1)
+__device__ bool tile_interleaved(MmaIssuer<D, BF16, false> &m0, MmaIssuer<D, BF16, false> &m1, int step0, int n, int n0,
+                                 int n1)
 {
     int st, prev = -1;
     for (int j = 0; j < n; ++j) {
@@ -527,12 +630,14 @@ __device__ bool tile_interleaved(MmaIssuer<D, BF16> &m0, MmaIssuer<D, BF16> &m1,
     return true;
 }
 
-template <int D, bool BF16, int MASK, bool SPLIT>
+// SEP: separate-P order (always at D = 64; at D = 128 for heads of one Q
+// tile, P_0 in tile 1's S columns), else the two-tile interleaved order.
+template <int D, bool BF16, int MASK, bool SPLIT, bool SEP>
 __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage, uint32_t tmem, Bars<D> b, Ctl c)
 {
     using C = Cfg<D>;
     auto make = [&](int q) {
-        return MmaIssuer<D, BF16>{q,
+        return MmaIssuer<D, BF16, SEP>{q,
                                   desc_lo(sQ + q * C::kTileBytes, 16),
                                   desc_lo(sStage, 16),
                                   desc_lo(sStage + C::kTileBytes, C::kBoxBytes),
@@ -543,8 +648,10 @@ __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage
                                   c,
                                   0u, 0u, 0u, 0u};
     };
-    MmaIssuer<D, BF16> m = make(w);                 // this warp's tile (D = 64) or tile 0 (D = 128)
-    MmaIssuer<D, BF16> m1 = make(1);                // tile 1 when one warp serves both
+    MmaIssuer<D, BF16, SEP> m = make(w);            // this warp's tile (D = 64) or tile 0 (D = 128)
+    MmaIssuer<D, BF16, SEP> m1 = make(1);           // tile 1 when one warp serves both
+    if (!C::kSeparateP && SEP)                      // D = 128, heads of one Q tile
+        m.tP = tmem + C::col_p_one_tile();
     int step = 0, it = 0;
     PartIter parts;
     parts.init_t<SPLIT>(p.sch, blockIdx.x);
@@ -560,7 +667,11 @@ __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage
         ptx::tc_fence_after_sync();
         m.q_cur = m.q_lo + (uint32_t)(qb * (C::kQBufBytes >> 4));
         m1.q_cur = m1.q_lo + (uint32_t)(qb * (C::kQBufBytes >> 4));
-        const bool ok = (C::kMmaWarps == 2) ? m.tile(step, n, w ? n1 : n0) : tile_interleaved(m, m1, step, n, n0, n1);
+        bool ok;
+        if constexpr (SEP)
+            ok = m.tile(step, n, w ? n1 : n0);
+        else
+            ok = tile_interleaved(m, m1, step, n, n0, n1);
         if (!ok)
             break;
         step += n;
@@ -578,7 +689,10 @@ __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage
 
 // ------------------------------------------------------------------ softmax
 
-template <int D, bool BF16, int MASK, bool SPLIT>
+// SEP as in mma_role.  At D = 128 its waits record a timeout inline: they
+// hold S, P or O rescale registers, which a call made the balanced variant
+// spill (1.3 % slower); at D = 64 the inline form measured 1.4 % slower.
+template <int D, bool BF16, int MASK, bool SPLIT, bool SEP>
 __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c, float2 *handoff)
 {
     using C = Cfg<D>;
@@ -587,7 +701,8 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
     const int t = threadIdx.x % 128;              // row within the Q tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(t & ~31) << 16;
     const uint32_t tS = tmem + C::col_s(w) + lane_off;
-    const uint32_t tP = tmem + C::col_p(w) + lane_off;
+    constexpr bool sep = SEP;                        // P_w apart from S_w: S_w is released once loaded
+    const uint32_t tP = tmem + ((SEP && !C::kSeparateP) ? C::col_p_one_tile() : C::col_p(w)) + lane_off;   // (w = 0)
     const uint32_t tO = tmem + C::col_o(w) + lane_off;
     const uint64_t qk2 = ptx::f2_pack(p.qk_scale, p.qk_scale);
     uint32_t s_phase = 0, o_phase = 0, n_st = 0;
@@ -622,7 +737,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
 
         for (int jr = 0; jr < np; ++jr) {
             const int j = pt.kb + jr;   // K/V step within the tile
-            if (!warp_wait(b.s_full(w), s_phase & 1u, c, kSiteSoftSFull))
+            if (!warp_wait<D == 128>(b.s_full(w), s_phase & 1u, c, kSiteSoftSFull))
                 return;
             ++s_phase;
             ptx::tc_fence_after_sync();
@@ -631,7 +746,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             ptx::tmem_ld64(tS, r[0]);   // the whole row of S_w in two instructions
             ptx::tmem_ld64(tS + 64, r[1]);
             ptx::tmem_wait_ld();
-            if (C::kSeparateP) {   // S_w may now be overwritten by the next step's MMA
+            if (sep) {   // S_w may now be overwritten by the next step's MMA
                 ptx::tc_fence_before_sync();
                 ptx::mbar_arrive(b.s_free(w));
             }
@@ -695,12 +810,12 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
                 acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
                 pk[i] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
             }
-            if (C::kSeparateP && jr > 0) {   // P.V of the previous step done: P_w may be overwritten, O_w is final
-                if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
+            if (sep && jr > 0) {   // P.V of the previous step done: P_w may be overwritten, O_w is final
+                if (!warp_wait<D == 128>(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
                     return;
                 ++o_phase;
                 ptx::tc_fence_after_sync();
-            }   // (D = 128: S_w(j) is issued after P.V_w(j-1), so s_full already implies it)
+            }   // (otherwise S_w(j) is issued after P.V_w(j-1), so s_full already implies it)
             ptx::tmem_st64(tP, pk);
             const uint64_t a2 = ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3]));
             float a_lo, a_hi;
@@ -735,13 +850,13 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(b.p_full(w));
         }
-        if (C::kSeparateP) {   // account for the last P.V of this tile
-            if (!warp_wait(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
+        if (sep) {   // account for the last P.V of this tile
+            if (!warp_wait<D == 128>(b.o_done(w), o_phase & 1u, c, kSiteSoftODone))
                 return;
             ++o_phase;
         }
         // Final row statistics for the epilogue warps (slot reused only once read).
-        if (n_st > 0 && !warp_wait(b.st_free(w), (n_st - 1) & 1u, c, kSiteSoftStFree))
+        if (n_st > 0 && !warp_wait<D == 128>(b.st_free(w), (n_st - 1) & 1u, c, kSiteSoftStFree))
             return;
         handoff[w * kBM + t] = make_float2(m, l);
         ++n_st;
@@ -1153,7 +1268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *base_ptr = smem_raw + (base - raw);
     const uint32_t sQ = base + C::kQOff;
     const uint32_t sStage = base + C::kStageOff;
-    Bars<D> b{base + C::kBarOff};
+    Bars<D> b{base + C::kBarOff, base + (uint32_t)C::vbar_off(SPLIT)};
     float2 *handoff = reinterpret_cast<float2 *>(base_ptr + C::kHandOff);
     uint32_t *misc = reinterpret_cast<uint32_t *>(base_ptr + C::kMiscOff);
     Ctl c{reinterpret_cast<volatile int *>(misc + 1)};
@@ -1166,6 +1281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(b.full(s), 1);
             ptx::mbar_init(b.empty(s), C::kMmaWarps);
+            if (C::kSplitKV) {
+                ptx::mbar_init(b.v_full(s), 1);
+                ptx::mbar_init(b.v_empty(s), C::kMmaWarps);
+            }
         }
         for (int qb = 0; qb < C::kQBufs; ++qb) {
             ptx::mbar_init(b.q_full(qb), 1);
@@ -1208,16 +1327,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (wg < kEpilogueWarpgroup) {
         ptx::regs_increase<kRegsSoftmax>();
-        softmax_role<D, BF16, MASK, SPLIT>(p, tmem, b, c, handoff);
+        if constexpr (C::kSeparateP)
+            softmax_role<D, BF16, MASK, SPLIT, true>(p, tmem, b, c, handoff);
+        else if (separate_p<D>(p))
+            softmax_role<D, BF16, MASK, SPLIT, true>(p, tmem, b, c, handoff);
+        else
+            softmax_role<D, BF16, MASK, SPLIT, false>(p, tmem, b, c, handoff);
     } else if (wg == kEpilogueWarpgroup) {
         ptx::regs_decrease<kRegsEpilogue>();
         epilogue_role<D, BF16, MASK, SPLIT>(p, tmem, b, c, base + C::kHandOff, base + C::kMiscOff + 8, base + C::kJobOff);
     } else {
         ptx::regs_decrease<kRegsProducer>();
-        if (warp == kLoadWarp)
-            load_role<D, MASK, SPLIT>(&tmQ, &tmK, &tmV, p, sQ, sStage, b, c);
-        else if (warp < kMmaWarp + C::kMmaWarps)
-            mma_role<D, BF16, MASK, SPLIT>(warp - kMmaWarp, p, sQ, sStage, tmem, b, c);
+        if (warp == kLoadWarp) {
+            if constexpr (!C::kSplitKV)
+                load_role<D, MASK, SPLIT, false>(&tmQ, &tmK, &tmV, p, sQ, sStage, b, c);
+            else if (split_kv<D>(p))
+                load_role<D, MASK, SPLIT, true>(&tmQ, &tmK, &tmV, p, sQ, sStage, b, c);
+            else
+                load_role<D, MASK, SPLIT, false>(&tmQ, &tmK, &tmV, p, sQ, sStage, b, c);
+        }
+        else if (warp < kMmaWarp + C::kMmaWarps) {
+            if constexpr (C::kSeparateP)
+                mma_role<D, BF16, MASK, SPLIT, true>(warp - kMmaWarp, p, sQ, sStage, tmem, b, c);
+            else if (separate_p<D>(p))
+                mma_role<D, BF16, MASK, SPLIT, true>(warp - kMmaWarp, p, sQ, sStage, tmem, b, c);
+            else
+                mma_role<D, BF16, MASK, SPLIT, false>(warp - kMmaWarp, p, sQ, sStage, tmem, b, c);
+        }
         else if (SPLIT && warp == kMergeWarp)
             merge_role<D, BF16>(p, base + C::kMergeOff, base + C::kMlOff,
                                 reinterpret_cast<const MergeJob *>(base_ptr + C::kJobOff), b, c);

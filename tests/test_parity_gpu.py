@@ -354,3 +354,23 @@ def test_decode_many_parts(B, H, Nq, Nkv, D, causal, schedule):
     lmax = float(np.abs(lse.cpu().double().numpy() - lse_ref).max())
     print(f"decode Nq={Nq} Nkv={Nkv} D={D} causal={int(causal)} {schedule}: max|dO|={emax:.3e} max|dLSE|={lmax:.3e}")
     assert emax <= TOL_O["bf16"] and lmax <= TOL_LSE
+
+
+@pytest.mark.parametrize("schedule", ["whole_tiles", "balanced"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nkv,dtype", [(1, 700, "bf16"), (77, 1300, "fp16"), (128, 900, "bf16")])
+def test_one_tile_heads_many_per_cta(Nq, Nkv, dtype, causal, schedule):
+    """D = 128 heads of at most 128 query rows run the separate-P order with
+    K and V released separately; 160 heads over the SMs give CTAs several
+    such tiles (whole tiles) or parts (balanced) in a row, so the producer's
+    hand-over of the last V between them is exercised.  Compared in full."""
+    q, k, v = _rect(2, 80, Nq, Nkv, 128, dtype, seed=Nq * 7 + Nkv)
+    scale = 128 ** -0.5
+    dev = torch.device("cuda:0")
+    o, lse = fa.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale, schedule=schedule)
+    assert fa.sync_status(torch.cuda.current_stream(dev).cuda_stream) == 0
+    o_ref, lse_ref = oracle.forward_qkv(q, k, v, causal, scale)
+    emax = float(np.abs(o.cpu().double().numpy() - o_ref).max())
+    lmax = float(np.abs(lse.cpu().double().numpy() - lse_ref).max())
+    print(f"one-tile heads Nq={Nq} Nkv={Nkv} {dtype} causal={int(causal)} {schedule}: max|dO|={emax:.3e} max|dLSE|={lmax:.3e}")
+    assert emax <= TOL_O[dtype] and lmax <= TOL_LSE
