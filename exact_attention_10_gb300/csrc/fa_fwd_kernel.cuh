@@ -33,7 +33,10 @@
 //            S_j: the softmax releases S_w as soon as it has loaded it.
 //   D = 128: no room for separate P: P_w overwrites columns [0,64) of S_w,
 //            and S_w of step j+1 is issued after the MMA that reads P_w(j)
-//            (tcgen05 MMAs from one thread execute in issue order).
+//            (tcgen05 MMAs from one thread execute in issue order).  When
+//            every head has at most 128 query rows (decoding), Q tile 1 is
+//            idle: P_0 goes to S1's columns and the steps run in the D = 64
+//            order, with each stage's K and V released separately.
 // P feeds the P.V MMA as its TMEM A operand.
 //
 // MMA issue order per K/V step j, per Q tile w (each tile has its own issuing
