@@ -1,33 +1,61 @@
-"""The forward kernel's mbarrier protocol for heads of one Q tile at D = 128
-(separate-P order, K and V of a stage released separately), modelled on the
-CPU.
+"""The forward kernel's mbarrier protocol, modelled on the CPU for each of
+its three step orders:
 
-Each role of a CTA -- the TMA producer, the MMA issuer, the softmax
-warpgroup of Q tile 0 and the epilogue -- is a coroutine that follows the
+* D = 64: one MMA-issuing warp per Q tile, a ring of four whole K/V stages,
+  two Q buffers, P apart from S (S_{j+1} issued once the softmax has loaded
+  S_j);
+* D = 128, two Q tiles: one MMA warp interleaving both tiles
+  (S0_j, P.V1_{j-1}, S1_j, P.V0_j), two whole stages, one Q buffer, P written
+  over S;
+* D = 128, heads of one Q tile: the D = 64 order with P in the idle tile's S
+  columns, and each stage's K and V landing and released on barriers of their
+  own, the producer loading K one step ahead of V.
+
+Each role of a CTA -- the TMA producer, the MMA issuer(s), the softmax
+warpgroup of each Q tile and the epilogue -- is a coroutine that follows the
 kernel's own sequence of waits, arrivals and commits
 (exact_attention_10_gb300/csrc/fa_fwd_kernel.cuh: load_role, MmaIssuer::tile,
-softmax_role, epilogue_role).  Barriers keep phase counts exactly as
-mbarriers do: a parity wait on phase k returns once k has completed, and a
-waiter that finds its barrier two phases past k would mistake the parity
-(the bug class of a lost phase), which the model reports.  TMA copies and
+tile_interleaved, mma_role, softmax_role, epilogue_role).  Barriers keep
+phase counts exactly as mbarriers do: a parity wait on phase k returns once
+k has completed, and a waiter that finds its barrier two phases past k would
+mistake the parity (a lost phase), which the model reports.  TMA copies and
 tcgen05 commits arrive as soon as they are issued; the hardware may delay
-them, which only removes interleavings, never adds a dependency.
+them, which only removes interleavings, never adds a dependency.  The model
+checks liveness and phase accounting, not the data hazards that the issue
+order of the tensor core's operations guards.
 
-Random interleavings over CTAs holding one or several parts of varying
-length must all finish.  Two pins: the producer order this kernel first
-had, which held a part's last V until after the next part's Q load although
-the MMA warp frees the single Q buffer only after that V is read, must
-deadlock once a CTA holds two parts; and a softmax that skips the wait for
-its part's last P.V must be reported as a lost phase.
+A CTA holds a sequence of parts, each a run of n key steps of one CTA tile
+of which Q tile w computes the first n_w (a causal or band tile's shorter
+tile may have none).  Random interleavings over many part sequences must all
+finish.  Two pins: the producer order the one-tile kernel first had, which
+held a part's last V until after the next part's Q load although the MMA
+warp frees the single Q buffer only after that V is read, must deadlock once
+a CTA holds two parts; and a softmax that skips the wait for its part's last
+P.V must be reported as a lost phase.
 """
 from __future__ import annotations
 
 import random
+from dataclasses import dataclass
 
 import pytest
 
-STAGES = 2     # K/V ring depth at D = 128
-Q_BUFS = 1     # Q buffers at D = 128
+
+@dataclass(frozen=True)
+class Order:
+    stages: int      # K/V ring depth
+    q_bufs: int      # Q buffers
+    mma_warps: int   # MMA-issuing warps (one per Q tile, or one for both)
+    sep: bool        # P apart from S
+    split_kv: bool   # K and V of a stage on separate barriers
+    tiles: int       # Q tiles with work
+
+
+ORDERS = {
+    "d64": Order(stages=4, q_bufs=2, mma_warps=2, sep=True, split_kv=False, tiles=2),
+    "d128": Order(stages=2, q_bufs=1, mma_warps=1, sep=False, split_kv=False, tiles=2),
+    "d128_one_tile": Order(stages=2, q_bufs=1, mma_warps=1, sep=True, split_kv=True, tiles=1),
+}
 
 
 class Barrier:
@@ -52,122 +80,184 @@ def wait(bar: Barrier, k: int):
 
 
 class CTA:
-    def __init__(self):
-        b = Barrier
-        self.full = [b(f"full{s}") for s in range(STAGES)]        # K landed
-        self.empty = [b(f"empty{s}") for s in range(STAGES)]      # K read
-        self.v_full = [b(f"v_full{s}") for s in range(STAGES)]    # V landed
-        self.v_empty = [b(f"v_empty{s}") for s in range(STAGES)]  # V read
-        self.q_full = [b(f"q_full{q}") for q in range(Q_BUFS)]
-        self.q_empty = [b(f"q_empty{q}") for q in range(Q_BUFS)]
-        self.s_full, self.s_free, self.p_full = b("s_full"), b("s_free"), b("p_full")
-        self.o_done, self.st_ready, self.st_free, self.o_free = b("o_done"), b("st_ready"), b("st_free"), b("o_free")
+    def __init__(self, o: Order):
+        b, m = Barrier, o.mma_warps
+        self.full = [b(f"full{s}") for s in range(o.stages)]              # stage (or K) landed
+        self.empty = [b(f"empty{s}", m) for s in range(o.stages)]         # stage (or K) read by every MMA warp
+        self.v_full = [b(f"v_full{s}") for s in range(o.stages)]          # split: V landed
+        self.v_empty = [b(f"v_empty{s}", m) for s in range(o.stages)]     # split: V read
+        self.q_full = [b(f"q_full{q}") for q in range(o.q_bufs)]
+        self.q_empty = [b(f"q_empty{q}", m) for q in range(o.q_bufs)]
+        # per Q tile (a warpgroup's 128 arrivals count as one here)
+        self.s_full = [b(f"s_full{w}") for w in range(2)]
+        self.s_free = [b(f"s_free{w}") for w in range(2)]
+        self.p_full = [b(f"p_full{w}") for w in range(2)]
+        self.o_done = [b(f"o_done{w}") for w in range(2)]
+        self.st_ready = [b(f"st_ready{w}") for w in range(2)]
+        self.st_free = [b(f"st_free{w}") for w in range(2)]
+        self.o_free = [b(f"o_free{w}") for w in range(2)]
 
 
-def loader(c: CTA, parts, flush_before_q: bool = True):
+def loader(c: CTA, o: Order, parts, flush_before_q: bool = True):
     step = it = nv = 0
 
     def load_v():
         nonlocal nv
-        st, use = nv % STAGES, nv // STAGES
+        st, use = nv % o.stages, nv // o.stages
         yield wait(c.v_empty[st], use - 1)
         c.v_full[st].arrive()
         nv += 1
 
-    for n in parts:
-        if flush_before_q and nv < step:   # the previous part's last V
+    for n, _, _ in parts:
+        if o.split_kv and flush_before_q and nv < step:   # the previous part's last V
             yield from load_v()
-        qb, quse = it % Q_BUFS, it // Q_BUFS
+        qb, quse = it % o.q_bufs, it // o.q_bufs
         yield wait(c.q_empty[qb], quse - 1)
         c.q_full[qb].arrive()
         it += 1
         for _ in range(n):
-            st, use = step % STAGES, step // STAGES
+            st, use = step % o.stages, step // o.stages
             yield wait(c.empty[st], use - 1)
-            c.full[st].arrive()              # K of this step
-            if nv < step:
+            c.full[st].arrive()              # K (and V, unless split) of this step
+            if o.split_kv and nv < step:
                 yield from load_v()          # V of the previous step
             step += 1
-    if nv < step:
+    if o.split_kv and nv < step:
         yield from load_v()                  # the last step's V
 
 
-def mma(c: CTA, parts):
-    step = it = n_s = n_pv = n_t = 0
+class Issuer:
+    """MMA issue state of one Q tile (MmaIssuer)."""
 
-    def issue_s():
-        nonlocal n_s
-        if n_s > 0:
-            yield wait(c.s_free, n_s - 1)
-        c.s_full.arrive()                    # commit after S
-        n_s += 1
+    def __init__(self, c: CTA, o: Order, w: int):
+        self.c, self.o, self.w = c, o, w
+        self.n_s = self.n_pv = self.n_t = 0
 
-    def issue_pv(accumulate: bool):
-        nonlocal n_t, n_pv
-        if not accumulate:
-            if n_t > 0:
-                yield wait(c.o_free, n_t - 1)
-            n_t += 1
-        yield wait(c.p_full, n_pv)
-        c.o_done.arrive()
-        n_pv += 1
+    def issue_s(self):
+        if self.o.sep and self.n_s > 0:
+            yield wait(self.c.s_free[self.w], self.n_s - 1)
+        self.c.s_full[self.w].arrive()       # commit after S
+        self.n_s += 1
 
-    for n in parts:
-        qb = it % Q_BUFS
-        yield wait(c.q_full[qb], it // Q_BUFS)
-        yield wait(c.full[step % STAGES], step // STAGES)
-        yield from issue_s()
-        c.empty[step % STAGES].arrive()      # K_0 read
-        for j in range(n):
-            if j + 1 < n:
-                g = step + j + 1
-                yield wait(c.full[g % STAGES], g // STAGES)
-                yield from issue_s()
-                c.empty[g % STAGES].arrive()
-            g = step + j
-            yield wait(c.v_full[g % STAGES], g // STAGES)
-            yield from issue_pv(j > 0)
-            c.v_empty[g % STAGES].arrive()
+    def issue_pv(self, accumulate: bool):
+        if not accumulate:                   # the part's first P.V overwrites O: the epilogue has read it
+            if self.n_t > 0:
+                yield wait(self.c.o_free[self.w], self.n_t - 1)
+            self.n_t += 1
+        yield wait(self.c.p_full[self.w], self.n_pv)
+        self.c.o_done[self.w].arrive()
+        self.n_pv += 1
+
+
+def tile_sep(m: Issuer, step0: int, n: int, nw: int):
+    """MmaIssuer::tile, the separate-P order."""
+    c, o = m.c, m.o
+    yield wait(c.full[step0 % o.stages], step0 // o.stages)
+    if nw > 0:
+        yield from m.issue_s()
+    if o.split_kv:
+        c.empty[step0 % o.stages].arrive()
+    for j in range(n):
+        if j + 1 < n:
+            g = step0 + j + 1
+            yield wait(c.full[g % o.stages], g // o.stages)
+            if j + 1 < nw:
+                yield from m.issue_s()
+            if o.split_kv:
+                c.empty[g % o.stages].arrive()
+        g = step0 + j
+        if o.split_kv:
+            yield wait(c.v_full[g % o.stages], g // o.stages)
+        if j < nw:
+            yield from m.issue_pv(j > 0)
+        (c.v_empty if o.split_kv else c.empty)[g % o.stages].arrive()
+
+
+def tile_interleaved(m0: Issuer, m1: Issuer, step0: int, n: int, n0: int, n1: int):
+    c, o = m0.c, m0.o
+    prev = None
+    for j in range(n):
+        g = step0 + j
+        yield wait(c.full[g % o.stages], g // o.stages)
+        if j < n0:
+            yield from m0.issue_s()
+        if j >= 1:
+            if j - 1 < n1:
+                yield from m1.issue_pv(j - 1 > 0)
+            c.empty[prev].arrive()           # K_{j-1} and V_{j-1} read
+        if j < n1:
+            yield from m1.issue_s()
+        if j < n0:
+            yield from m0.issue_pv(j > 0)
+        prev = g % o.stages
+    if n - 1 < n1:
+        yield from m1.issue_pv(n - 1 > 0)
+    c.empty[prev].arrive()
+
+
+def mma(c: CTA, o: Order, parts, w: int):
+    """mma_role of warp w (w = 0 issues both tiles when one warp serves both)."""
+    m, m1 = Issuer(c, o, w), Issuer(c, o, 1)
+    step = it = 0
+    for n, n0, n1 in parts:
+        qb = it % o.q_bufs
+        yield wait(c.q_full[qb], it // o.q_bufs)
+        if o.sep:
+            yield from tile_sep(m, step, n, n1 if w else n0)
+        else:
+            yield from tile_interleaved(m, m1, step, n, n0, n1)
         step += n
         c.q_empty[qb].arrive()
         it += 1
 
 
-def softmax(c: CTA, parts, last_pv_wait: bool = True):
+def softmax(c: CTA, o: Order, parts, w: int, last_pv_wait: bool = True):
     s_phase = o_phase = n_st = 0
-    for n in parts:
-        for jr in range(n):
-            yield wait(c.s_full, s_phase)
+    for part in parts:
+        np_ = part[1 + w]
+        if np_ == 0:
+            continue
+        for jr in range(np_):
+            yield wait(c.s_full[w], s_phase)
             s_phase += 1
-            c.s_free.arrive()
-            if jr > 0:
-                yield wait(c.o_done, o_phase)
+            if o.sep:
+                c.s_free[w].arrive()
+            if o.sep and jr > 0:
+                yield wait(c.o_done[w], o_phase)
                 o_phase += 1
-            c.p_full.arrive()
-        if last_pv_wait:
-            yield wait(c.o_done, o_phase)    # the part's last P.V
+            c.p_full[w].arrive()
+        if o.sep and last_pv_wait:
+            yield wait(c.o_done[w], o_phase)  # the part's last P.V
             o_phase += 1
         if n_st > 0:
-            yield wait(c.st_free, n_st - 1)
+            yield wait(c.st_free[w], n_st - 1)
         n_st += 1
-        c.st_ready.arrive()
+        c.st_ready[w].arrive()
 
 
-def epilogue(c: CTA, parts):
-    taken = pv = 0
-    for n in parts:
-        yield wait(c.st_ready, taken)
-        taken += 1
-        c.st_free.arrive()
-        pv += n
-        yield wait(c.o_done, pv - 1)
-        c.o_free.arrive()
+def epilogue(c: CTA, o: Order, parts):
+    taken, pv = [0, 0], [0, 0]
+    for part in parts:
+        for w in range(o.tiles):
+            np_ = part[1 + w]
+            if np_ == 0:
+                continue
+            yield wait(c.st_ready[w], taken[w])
+            taken[w] += 1
+            c.st_free[w].arrive()
+            pv[w] += np_
+            yield wait(c.o_done[w], pv[w] - 1)
+            c.o_free[w].arrive()
 
 
-def run(parts, seed: int, flush_before_q: bool = True, last_pv_wait: bool = True) -> str:
+def run(order: str, parts, seed: int, flush_before_q: bool = True, last_pv_wait: bool = True) -> str:
     """'done', 'deadlock' or 'aliased' for one random interleaving."""
-    c = CTA()
-    roles = [loader(c, parts, flush_before_q), mma(c, parts), softmax(c, parts, last_pv_wait), epilogue(c, parts)]
+    o = ORDERS[order]
+    c = CTA(o)
+    roles = [loader(c, o, parts, flush_before_q)]
+    roles += [mma(c, o, parts, w) for w in range(o.mma_warps)]
+    roles += [softmax(c, o, parts, w, last_pv_wait) for w in range(o.tiles)]
+    roles.append(epilogue(c, o, parts))
     blocked = [None] * len(roles)
     live = set(range(len(roles)))
     rng = random.Random(seed)
@@ -197,33 +287,64 @@ def run(parts, seed: int, flush_before_q: bool = True, last_pv_wait: bool = True
     return "done"
 
 
-PART_SETS = [(1,), (2,), (5,), (1, 1), (1, 4), (3, 2), (4, 1, 3), (1, 1, 1, 1), (7, 1), (2, 6, 1, 3)]
+def one_tile_parts(lengths):
+    return [(n, n, 0) for n in lengths]
 
 
-@pytest.mark.parametrize("parts", PART_SETS)
-def test_one_tile_protocol_always_completes(parts):
+def random_parts(rng: random.Random, tiles: int):
+    """A CTA's parts: 1-4 runs of 1-7 steps; with two tiles, one of them
+    (either) may stop early, down to no steps at all."""
+    parts = []
+    for _ in range(rng.randint(1, 4)):
+        n = rng.randint(1, 7)
+        if tiles == 1:
+            parts.append((n, n, 0))
+        elif rng.random() < 0.5:
+            parts.append((n, rng.randint(0, n), n))   # causal-like: tile 0 shorter
+        else:
+            parts.append((n, n, rng.randint(0, n)))   # band-like: tile 1 shorter
+    return parts
+
+
+ONE_TILE_SETS = [(1,), (2,), (5,), (1, 1), (1, 4), (3, 2), (4, 1, 3), (1, 1, 1, 1), (7, 1), (2, 6, 1, 3)]
+
+
+@pytest.mark.parametrize("lengths", ONE_TILE_SETS)
+def test_one_tile_order_always_completes(lengths):
     for seed in range(300):
-        assert run(parts, seed) == "done", (parts, seed)
+        assert run("d128_one_tile", one_tile_parts(lengths), seed) == "done", (lengths, seed)
 
 
-@pytest.mark.parametrize("parts", [(1, 1), (3, 2), (4, 1, 3)])
-def test_holding_the_last_v_past_the_next_q_load_deadlocks(parts):
-    """The pin: without the flush before the next part's Q load the model
-    finds the deadlock the kernel hit (a bounded wait expired), in every
+@pytest.mark.parametrize("order", ["d64", "d128", "d128_one_tile"])
+def test_every_order_completes_on_random_part_sequences(order):
+    rng = random.Random(sum(map(ord, order)))
+    for _ in range(150):
+        parts = random_parts(rng, ORDERS[order].tiles)
+        for seed in range(20):
+            assert run(order, parts, seed) == "done", (order, parts, seed)
+
+
+@pytest.mark.parametrize("lengths", [(1, 1), (3, 2), (4, 1, 3)])
+def test_holding_the_last_v_past_the_next_q_load_deadlocks(lengths):
+    """The first pin: without the flush before the next part's Q load the
+    model finds the deadlock the kernel hit (a bounded wait expired), in every
     interleaving of a CTA with two or more parts."""
-    assert all(run(parts, seed, flush_before_q=False) == "deadlock" for seed in range(50))
+    parts = one_tile_parts(lengths)
+    assert all(run("d128_one_tile", parts, seed, flush_before_q=False) == "deadlock" for seed in range(50))
 
 
 def test_single_part_needs_no_flush():
     """One part per CTA never reaches the hand-over, so the old order passed
     there, as it did on the GPU for every test with one part per CTA."""
     for seed in range(100):
-        assert run((5,), seed, flush_before_q=False) == "done"
+        assert run("d128_one_tile", one_tile_parts((5,)), seed, flush_before_q=False) == "done"
 
 
-def test_a_lost_phase_is_reported():
+@pytest.mark.parametrize("order", ["d64", "d128_one_tile"])
+def test_a_lost_phase_is_reported(order):
     """The second pin: a softmax that skips the wait for its part's last P.V
-    lets its count of o_done phases fall behind, so a later parity wait
-    can see a phase two past the one it means; the model must flag it."""
-    outcomes = {run((3, 2, 4), seed, last_pv_wait=False) for seed in range(200)}
+    lets its count of o_done phases fall behind, so a later parity wait can
+    see a phase two past the one it means; the model must flag it."""
+    parts = [(3, 3, 3), (2, 2, 2), (4, 4, 4)] if ORDERS[order].tiles == 2 else one_tile_parts((3, 2, 4))
+    outcomes = {run(order, parts, seed, last_pv_wait=False) for seed in range(200)}
     assert "aliased" in outcomes, outcomes
