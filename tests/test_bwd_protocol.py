@@ -1,0 +1,250 @@
+"""The backward kernel's mbarrier protocol, modelled on the CPU for its four
+passes (exact_attention_10_gb300/csrc/fa_bwd_kernel.cuh: bwd_load, bwd_mma,
+bwd_compute, bwd_mma_pipe, bwd_compute_pipe):
+
+* D = 64, dQ and dK/dV passes: pipelined (S_{g+1} and dP_{g+1} issued once the
+  compute warps have loaded S_g and dP_g), three stages of both streamed tiles;
+* D = 128, dQ pass: pipelined, K and V in separate rings of three and two
+  slots, V's slot freed once dP is computed;
+* D = 128, dK/dV pass: not pipelined (P^T and dS^T overwrite S and dP, and the
+  next S follows the products in issue order), two stages.
+
+The producer, the MMA warp and the two compute warpgroups (column halves) are
+coroutines following the kernel's waits, arrivals and commits; barriers keep
+exact phase counts, and a waiter that finds its barrier two phases past the
+one it means (a lost phase: its parity would read as not yet complete) is
+reported.  Copies and commits arrive when issued.  Random interleavings over
+CTAs holding one or several resident tiles of varying length must finish.
+
+The pin: in the pipelined dQ pass nothing holds the compute warps back from
+finishing step g + 1 before the MMA warp waits for step g, so one p_full
+barrier can run two phases ahead of its waiter; the kernel alternates two
+barriers there, and the model must flag the single-barrier form.
+"""
+from __future__ import annotations
+
+import random
+from dataclasses import dataclass
+
+import pytest
+
+
+@dataclass(frozen=True)
+class Pass:
+    pipeline: bool
+    kv: bool          # dK/dV pass (else dQ)
+    split: bool       # K and V in separate rings (D = 128 dQ pass)
+    ring0: int        # stages, or slots of ring 0
+    ring1: int        # slots of ring 1 (split)
+
+
+PASSES = {
+    "d64_dq": Pass(pipeline=True, kv=False, split=False, ring0=3, ring1=3),
+    "d64_kv": Pass(pipeline=True, kv=True, split=False, ring0=3, ring1=3),
+    "d128_dq": Pass(pipeline=True, kv=False, split=True, ring0=3, ring1=2),
+    "d128_kv": Pass(pipeline=False, kv=True, split=False, ring0=2, ring1=2),
+}
+COMPUTE = 2   # compute warpgroups, each arriving once per barrier phase
+
+
+class Barrier:
+    def __init__(self, name: str, count: int = 1):
+        self.name, self.count, self.phase, self.pending = name, count, 0, 0
+
+    def arrive(self):
+        self.pending += 1
+        if self.pending == self.count:
+            self.pending = 0
+            self.phase += 1
+
+
+class Aliased(Exception):
+    pass
+
+
+def wait(bar: Barrier, k: int):
+    return ("wait", bar, k)
+
+
+class CTA:
+    def __init__(self, q: Pass, alternate_p_full: bool):
+        b = Barrier
+        self.full = [b(f"full{s}") for s in range(q.ring0)]
+        self.empty = [b(f"empty{s}") for s in range(q.ring0)]
+        self.full1 = [b(f"full1_{s}") for s in range(q.ring1)]
+        self.empty1 = [b(f"empty1_{s}") for s in range(q.ring1)]
+        self.res_full, self.res_empty, self.sd_full = b("res_full"), b("res_empty"), b("sd_full")
+        self.p_full, self.p_full_odd = b("p_full", COMPUTE), b("p_full_odd", COMPUTE)
+        self.acc_full, self.acc_free = b("acc_full"), b("acc_free", COMPUTE)
+        self.sd_free, self.pd_free = b("sd_free", COMPUTE), b("pd_free")
+        self.alternate = alternate_p_full
+
+    def p_full_dq(self, g: int):
+        """The barrier and phase that carry step g's P / dS in the pipelined dQ pass."""
+        if self.alternate:
+            return (self.p_full_odd if g & 1 else self.p_full), g >> 1
+        return self.p_full, g
+
+
+def loader(c: CTA, q: Pass, tiles):
+    step = t = 0
+    for n in tiles:
+        if t > 0:
+            yield wait(c.res_empty, t - 1)
+        c.res_full.arrive()
+        t += 1
+        for _ in range(n):
+            k0 = step % q.ring0
+            yield wait(c.empty[k0], step // q.ring0 - 1)
+            if q.split:
+                k1 = step % q.ring1
+                yield wait(c.empty1[k1], step // q.ring1 - 1)
+                c.full1[k1].arrive()
+            c.full[k0].arrive()
+            step += 1
+
+
+def mma_pipe(c: CTA, q: Pass, tiles):
+    g = done = 0
+
+    def issue_sd(gs):
+        if gs > 0:
+            yield wait(c.sd_free, gs - 1)
+        yield wait(c.full[gs % q.ring0], gs // q.ring0)
+        if q.split:
+            yield wait(c.full1[gs % q.ring1], gs // q.ring1)
+        c.sd_full.arrive()
+        if q.split:
+            c.empty1[gs % q.ring1].arrive()   # V's slot is free once dP is computed
+
+    for n in tiles:
+        yield wait(c.res_full, done)
+        yield from issue_sd(g)
+        for j in range(n):
+            if j + 1 < n:
+                yield from issue_sd(g + 1)
+            if j == 0 and done > 0:
+                yield wait(c.acc_free, done - 1)
+            if q.kv:
+                yield wait(c.p_full, g)
+            else:
+                yield wait(*c.p_full_dq(g))
+            if q.kv:
+                c.pd_free.arrive()
+            c.empty[g % q.ring0].arrive()
+            if j == n - 1:
+                c.acc_full.arrive()
+                c.res_empty.arrive()
+            g += 1
+        done += 1
+
+
+def compute_pipe(c: CTA, q: Pass, tiles, pd_wait: bool = True):
+    g = done = 0
+    for n in tiles:
+        for _ in range(n):
+            yield wait(c.sd_full, g)
+            c.sd_free.arrive()
+            if q.kv and pd_wait and g > 0:
+                yield wait(c.pd_free, g - 1)
+            if q.kv:
+                c.p_full.arrive()
+            else:
+                c.p_full_dq(g)[0].arrive()
+            g += 1
+        yield wait(c.acc_full, done)
+        c.acc_free.arrive()
+        done += 1
+
+
+def mma_serial(c: CTA, q: Pass, tiles):
+    step = done = n_p = 0
+    for n in tiles:
+        yield wait(c.res_full, done)
+        for j in range(n):
+            yield wait(c.full[step % q.ring0], step // q.ring0)
+            c.sd_full.arrive()
+            if j == 0 and done > 0:
+                yield wait(c.acc_free, done - 1)
+            yield wait(c.p_full, n_p)
+            n_p += 1
+            c.empty[step % q.ring0].arrive()
+            if j == n - 1:
+                c.acc_full.arrive()
+                c.res_empty.arrive()
+            step += 1
+        done += 1
+
+
+def compute_serial(c: CTA, q: Pass, tiles):
+    step = done = 0
+    for n in tiles:
+        for _ in range(n):
+            yield wait(c.sd_full, step)
+            c.p_full.arrive()
+            step += 1
+        yield wait(c.acc_full, done)
+        c.acc_free.arrive()
+        done += 1
+
+
+def run(name: str, tiles, seed: int, alternate_p_full: bool = True, pd_wait: bool = True) -> str:
+    q = PASSES[name]
+    c = CTA(q, alternate_p_full)
+    roles = [loader(c, q, tiles)]
+    if q.pipeline:
+        roles += [mma_pipe(c, q, tiles)] + [compute_pipe(c, q, tiles, pd_wait) for _ in range(COMPUTE)]
+    else:
+        roles += [mma_serial(c, q, tiles)] + [compute_serial(c, q, tiles) for _ in range(COMPUTE)]
+    blocked = [None] * len(roles)
+    live = set(range(len(roles)))
+    rng = random.Random(seed)
+
+    def ready(i):
+        w = blocked[i]
+        if w is None:
+            return True
+        _, bar, k = w
+        if bar.phase > k + 1:
+            raise Aliased(f"{bar.name}: phase {bar.phase} while waiting for {k}")
+        return bar.phase >= k + 1
+
+    try:
+        while live:
+            runnable = [i for i in live if ready(i)]
+            if not runnable:
+                return "deadlock"
+            i = rng.choice(runnable)
+            try:
+                blocked[i] = next(roles[i])
+            except StopIteration:
+                live.discard(i)
+                blocked[i] = None
+    except Aliased:
+        return "aliased"
+    return "done"
+
+
+@pytest.mark.parametrize("name", sorted(PASSES))
+def test_every_pass_completes_on_random_tile_sequences(name):
+    rng = random.Random(sum(map(ord, name)))
+    for _ in range(150):
+        tiles = [rng.randint(1, 6) for _ in range(rng.randint(1, 4))]
+        for seed in range(20):
+            assert run(name, tiles, seed) == "done", (name, tiles, seed)
+
+
+@pytest.mark.parametrize("name", ["d64_dq", "d128_dq"])
+def test_single_p_full_barrier_in_the_pipelined_dq_pass_is_flagged(name):
+    """The pin: with one p_full barrier the compute warps can complete two of
+    its phases before the MMA warp waits for the first."""
+    outcomes = {run(name, [5, 3], seed, alternate_p_full=False) for seed in range(200)}
+    assert "aliased" in outcomes, outcomes
+
+
+def test_pipelined_kv_pass_needs_the_pd_free_wait():
+    """In the pipelined dK/dV pass the single P^T / dS^T buffers are what hold
+    the compute warps to one step ahead; without their wait on pd_free the
+    same lost phase appears."""
+    outcomes = {run("d64_kv", [5, 3], seed, pd_wait=False) for seed in range(200)}
+    assert "aliased" in outcomes, outcomes
