@@ -114,6 +114,20 @@ def test_band_decode_long_windowed_context():
         _compare(o, lse, o_ref, lse_ref, "bf16", f"decode window=8192 {schedule}")
 
 
+@pytest.mark.parametrize("schedule", ["whole_tiles", "balanced"])
+@pytest.mark.parametrize("Nq,Nkv,window,dtype", [(16, 2000, (500, 0), "bf16"), (77, 1500, (300, 40), "fp16")])
+def test_band_one_tile_heads_many_per_cta(Nq, Nkv, window, dtype, schedule):
+    """D = 128 heads of at most 128 query rows under a band run the one-tile
+    order (K and V released separately); 160 heads give CTAs several such
+    tiles (whole tiles) or parts (balanced), so the producer hands a part's
+    last V over from a band's first key step on.  Compared in full."""
+    q, k, v = _inputs(2, 80, Nq, Nkv, 128, dtype, seed=Nq * 5 + Nkv)
+    scale = 128 ** -0.5
+    o, lse = _band(q, k, v, window, scale, schedule)
+    o_ref, lse_ref = oracle.forward_band(q, k, v, window[0], window[1], scale)
+    _compare(o, lse, o_ref, lse_ref, dtype, f"one-tile band Nq={Nq} Nkv={Nkv} window={window} {dtype} {schedule}")
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_band_reduces_to_the_plain_masks(D):
     """The band (-1, 0) is fa_fwd_qkv's causal mask and (-1, -1) no mask: same
