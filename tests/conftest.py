@@ -1,4 +1,7 @@
+import json
 import os
+import shutil
+import subprocess
 import sys
 
 import pytest
@@ -17,3 +20,17 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle._load()
+
+
+@pytest.fixture(scope="session")
+def kernel_constants(tmp_path_factory):
+    """The kernels' pipeline constants (tests/kernel_constants.cu, compiled with
+    nvcc for the host), which the CPU models of their protocols must match."""
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path_factory.mktemp("kernel_constants") / "kernel_constants")
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17", "-O1",
+                    "-I", os.path.join(ROOT, "include"), "-I", os.path.join(ROOT, "exact_attention_10_gb300", "csrc"),
+                    os.path.join(ROOT, "tests", "kernel_constants.cu"), "-o", exe], check=True, capture_output=True)
+    return json.loads(subprocess.run([exe], check=True, capture_output=True, text=True).stdout)

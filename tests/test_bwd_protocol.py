@@ -248,3 +248,13 @@ def test_pipelined_kv_pass_needs_the_pd_free_wait():
     same lost phase appears."""
     outcomes = {run("d64_kv", [5, 3], seed, pd_wait=False) for seed in range(200)}
     assert "aliased" in outcomes, outcomes
+
+
+def test_model_matches_the_kernel_constants(kernel_constants):
+    """The passes above use the kernel's own pipelining choice, ring layout
+    and slot counts."""
+    for name, q in PASSES.items():
+        k = kernel_constants[name]
+        assert (q.pipeline, q.split, q.ring0) == (bool(k["pipeline"]), bool(k["split"]), k["ring0"]), name
+        if q.split:
+            assert q.ring1 == k["ring1"], name

@@ -348,3 +348,18 @@ def test_a_lost_phase_is_reported(order):
     parts = [(3, 3, 3), (2, 2, 2), (4, 4, 4)] if ORDERS[order].tiles == 2 else one_tile_parts((3, 2, 4))
     outcomes = {run(order, parts, seed, last_pv_wait=False) for seed in range(200)}
     assert "aliased" in outcomes, outcomes
+
+
+def test_model_matches_the_kernel_constants(kernel_constants):
+    """The orders above use the kernel's own ring depths, Q buffers and issue
+    structure: D = 64 and the two-tile D = 128 order as compiled, the
+    one-tile order as the D = 128 kernel runs it (separate P, K and V split)."""
+    k64, k128 = kernel_constants["fwd64"], kernel_constants["fwd128"]
+    assert kernel_constants["q_tiles"] == 2
+    d64, d128, one = ORDERS["d64"], ORDERS["d128"], ORDERS["d128_one_tile"]
+    assert (d64.stages, d64.q_bufs, d64.mma_warps, d64.sep, d64.split_kv) == \
+        (k64["stages"], k64["q_bufs"], k64["mma_warps"], bool(k64["sep"]), bool(k64["split_kv"]))
+    assert (d128.stages, d128.q_bufs, d128.mma_warps, d128.sep) == \
+        (k128["stages"], k128["q_bufs"], k128["mma_warps"], bool(k128["sep"]))
+    assert (one.stages, one.q_bufs, one.mma_warps, one.split_kv) == \
+        (k128["stages"], k128["q_bufs"], k128["mma_warps"], bool(k128["split_kv"]))
