@@ -11,7 +11,9 @@ flushed (a 256 MiB write) between calls, outside the events.
 Other keys: ``e2e`` (same metric through the C ABI with pinned host buffers,
 host->device and device->host copies of every step inside the timed region,
 pipelined so one step's calls overlap its neighbours' copies), ``backward``
-(fa_bwd on the same workload, per call), ``roofline``
+(fa_bwd on the same workload, per call), ``decode`` (split-KV decoding of a
+few queries against long key sequences, per call, as K/V bandwidth against
+the measured HBM copy rate), ``roofline``
 (the non-causal kernel against the measured bf16 tensor peak), ``clocks``
 (nvidia-smi samples taken during the timed region), ``cpu_baseline`` (the fp64
 CPU oracle on a bounded sample, timed on this host's cores).
@@ -48,6 +50,46 @@ def _peaks():
         return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), float(d["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+# Split-KV decode shapes timed beside the headline (B, H, query rows, keys, D):
+# a few queries against long key sequences, bf16, automatic schedule.
+DECODE_SHAPES = ((1, 32, 4, 32768, 128), (8, 32, 1, 8192, 128))
+
+
+def decode_timings(steps: int, dev, stream, flush, hbm_gbs: float) -> dict:
+    """Mean time of `steps` fa_fwd_qkv calls per decode shape (CUDA events on
+    the launching stream, L2 flushed before each call) and the K/V bandwidth
+    it implies, against the measured HBM copy rate."""
+    import torch
+    from exact_attention_10_gb300 import fa
+    out = {"dtype": "bf16", "schedule": "auto", "l2": "flushed between calls", "steps": steps, "shapes": []}
+    for B, H, Nq, Nkv, D in DECODE_SHAPES:
+        g = torch.Generator(device=dev).manual_seed(Nq * 131 + Nkv)
+        q = torch.randn(B, H, Nq, D, device=dev, generator=g).to(torch.bfloat16)
+        k = torch.randn(B, H, Nkv, D, device=dev, generator=g).to(torch.bfloat16)
+        v = torch.randn(B, H, Nkv, D, device=dev, generator=g).to(torch.bfloat16)
+        o, lse = torch.empty_like(q), torch.empty(B, H, Nq, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            fa.forward(q, k, v, scale=D ** -0.5, out=o, lse=lse)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            fa.forward(q, k, v, scale=D ** -0.5, out=o, lse=lse)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        rc = fa.sync_status(stream.cuda_stream)
+        if rc != 0:
+            raise fa.FAError(rc, "decode")
+        ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
+        kv = 2 * B * H * Nkv * D * 2
+        out["shapes"].append({"B": B, "H": H, "Nq": Nq, "Nkv": Nkv, "D": D, "us_mean": ms * 1e3,
+                              "kv_bytes": kv, "kv_gbs": kv / (ms * 1e-3) / 1e9,
+                              "frac_of_measured_hbm": kv / (ms * 1e-3) / 1e9 / hbm_gbs})
+        del q, k, v, o, lse
+    return out
 
 
 def _dist_env():
@@ -238,6 +280,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--bwd-steps", type=int, default=50, help="timed backward calls per mask (0: skip)")
+    ap.add_argument("--decode-steps", type=int, default=30, help="timed split-KV decode calls per shape (0: skip)")
     args = ap.parse_args(argv)
 
     from exact_attention_10_gb300.inputs import WORKLOADS
@@ -446,6 +489,13 @@ def main(argv=None):
             "clocks": clk, "gpu_launches": args.steps * len(modes), "wall_s_timed_region": wall}
     if bwd_info is not None:
         line["backward"] = bwd_info
+    if args.decode_steps > 0:
+        # outside the timed region; a failure here is reported in the object
+        # and leaves the line's own measurements as they are
+        try:
+            line["decode"] = decode_timings(args.decode_steps, dev, stream, flush, _peaks()[2])
+        except Exception as e:
+            line["decode"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0 and not args.no_cpu_baseline:
         v_cpu, desc, cores, spent = cpu_oracle_sample(w, args.cpu_budget)
         line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
