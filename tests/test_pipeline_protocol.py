@@ -32,6 +32,10 @@ held a part's last V until after the next part's Q load although the MMA
 warp frees the single Q buffer only after that V is read, must deadlock once
 a CTA holds two parts; and a softmax that skips the wait for its part's last
 P.V must be reported as a lost phase.
+
+The balanced variant's merge path (the epilogue's job queue to the merge warp
+and the merge warp's ring of copy buffers) is modelled the same way at the
+end of this file.
 """
 from __future__ import annotations
 
@@ -363,3 +367,98 @@ def test_model_matches_the_kernel_constants(kernel_constants):
         (k128["stages"], k128["q_bufs"], k128["mma_warps"], bool(k128["sep"]))
     assert (one.stages, one.q_bufs, one.mma_warps, one.split_kv) == \
         (k128["stages"], k128["q_bufs"], k128["mma_warps"], bool(k128["split_kv"]))
+
+
+# ---------------------------------------------------------------- merge queue
+# The balanced variant's merge path (epilogue_role's post, merge_role): the
+# epilogue hands merge jobs to the merge warp through kJobSlots = 2 slots
+# (job_full / job_empty); the merge warp brings each job's (m, l) in with one
+# bulk copy (ml_full) and streams its chunks of partial O through
+# kMergeBufs = 4 buffers (merge_full), issuing the next chunk into a buffer as
+# soon as it has read it and numbering chunks across jobs, so a buffer's
+# phase is its chunk count so far; a job with no parts tells it to stop.
+JOB_SLOTS, MERGE_BUFS = 2, 4
+
+
+def merge_run(jobs, seed: int, carry_count: bool = True) -> str:
+    job_full = [Barrier(f"job_full{j}") for j in range(JOB_SLOTS)]
+    job_empty = [Barrier(f"job_empty{j}") for j in range(JOB_SLOTS)]
+    merge_full = [Barrier(f"merge_full{i}") for i in range(MERGE_BUFS)]
+    ml_full = Barrier("ml_full")
+    posted = []
+
+    def epilogue_posts():
+        for n, nchunks in enumerate(list(jobs) + [0]):   # the last job (no parts) stops the merge warp
+            j = n % JOB_SLOTS
+            yield wait(job_empty[j], n // JOB_SLOTS - 1)
+            posted.append(nchunks)
+            job_full[j].arrive()
+
+    def merge_warp():
+        n_jobs = streamed = ml_uses = 0
+        while True:
+            j = n_jobs % JOB_SLOTS
+            yield wait(job_full[j], n_jobs // JOB_SLOTS)
+            nchunks = posted[n_jobs]
+            if nchunks == 0:
+                return
+            first = streamed if carry_count else 0
+            issued = 0
+            ml_full.arrive()                          # the (m, l) copy lands
+            while issued < MERGE_BUFS and issued < nchunks:
+                merge_full[(first + issued) % MERGE_BUFS].arrive()
+                issued += 1
+            yield wait(ml_full, ml_uses)
+            ml_uses += 1
+            for k in range(nchunks):
+                g = first + k
+                yield wait(merge_full[g % MERGE_BUFS], g // MERGE_BUFS)
+                if issued < nchunks:                  # the next chunk into the buffer just read
+                    merge_full[(first + issued) % MERGE_BUFS].arrive()
+                    issued += 1
+            streamed = first + issued
+            job_empty[j].arrive()
+            n_jobs += 1
+
+    roles = [epilogue_posts(), merge_warp()]
+    blocked = [None, None]
+    live = {0, 1}
+    rng = random.Random(seed)
+    try:
+        while live:
+            runnable = []
+            for i in live:
+                w = blocked[i]
+                if w is not None:
+                    _, bar, k = w
+                    if bar.phase > k + 1:
+                        raise Aliased(bar.name)
+                    if bar.phase < k + 1:
+                        continue
+                runnable.append(i)
+            if not runnable:
+                return "deadlock"
+            i = rng.choice(runnable)
+            try:
+                blocked[i] = next(roles[i])
+            except StopIteration:
+                live.discard(i)
+                blocked[i] = None
+    except Aliased:
+        return "aliased"
+    return "done"
+
+
+def test_merge_queue_completes():
+    rng = random.Random(7)
+    for _ in range(200):
+        jobs = [rng.randint(1, 19) for _ in range(rng.randint(1, 6))]   # chunks per job: parts x row blocks
+        for seed in range(10):
+            assert merge_run(jobs, seed) == "done", (jobs, seed)
+
+
+def test_merge_buffers_need_the_count_carried_across_jobs():
+    """The pin: restarting the chunk count at each job would wait on a
+    buffer's phase from an earlier job, which the model flags."""
+    outcomes = {merge_run([3, 5, 2], seed, carry_count=False) for seed in range(50)}
+    assert "aliased" in outcomes, outcomes
