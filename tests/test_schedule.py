@@ -66,6 +66,15 @@ for N, Nkv, wl, wr in ((32768, 32768, 4096, 0), (8192, 8192, 255, 0), (1, 131072
     for BH in (1, 3, 32):
         PLAN_CASES.append((N, Nkv, BH, 1, 152, wl, wr))
 
+# the decode shapes bench.py times beside the headline, and the one-tile heads
+# the GPU parity tests spread over more CTA tiles than SMs
+for N, Nkv, BH in ((4, 32768, 32), (1, 8192, 256), (1, 32768, 32), (4, 131072, 8), (128, 32768, 32), (16, 2000, 160),
+                   (77, 1500, 160), (1, 700, 160), (128, 900, 160)):
+    for causal in (0, 1):
+        PLAN_CASES.append((N, Nkv, BH, causal, 152, -1, 0))
+for N, Nkv, BH, wl, wr in ((16, 2000, 160, 500, 0), (77, 1500, 160, 300, 40), (4, 131072, 8, 8191, 0)):
+    PLAN_CASES.append((N, Nkv, BH, 1, 152, wl, wr))
+
 
 def test_schedule_planner(checker):
     """Every schedule the planner picks covers all work once, and a balanced
