@@ -39,10 +39,13 @@
 //            order, with each stage's K and V released separately.
 // P feeds the P.V MMA as its TMEM A operand.
 //
-// MMA issue order per K/V step j, per Q tile w (each tile has its own issuing
-// warp, so the two streams interleave on the tensor core by themselves):
-//   D = 64:  S_w(j+1) as soon as the softmax has loaded S_w(j), then O_w += P_w(j) V_j
-//   D = 128: S_w(j), then O_w += P_w(j) V_j once P_w(j) has overwritten S_w(j)
+// MMA issue order per K/V step j, per Q tile w:
+//   D = 64:  S_w(j+1) as soon as the softmax has loaded S_w(j), then O_w += P_w(j) V_j;
+//            each tile has its own issuing warp, so the two streams interleave
+//            on the tensor core by themselves
+//   D = 128: one warp issues S0(j), O1 += P1(j-1) V_{j-1}, S1(j), O0 += P0(j) V_j,
+//            each P.V once P_w has overwritten S_w; heads of one Q tile run
+//            the D = 64 order instead
 // so each softmax warpgroup's work overlaps the other tile's MMAs.
 //
 // Softmax follows the exp2 form ("How to profile and optimise kernels", exp2):
