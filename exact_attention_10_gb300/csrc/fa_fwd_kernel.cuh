@@ -20,7 +20,9 @@
 //   warpgroup 1  the same for Q tile 1
 //   warpgroup 2  epilogue for both Q tiles: O = acc / l and LSE, written once per tile
 //   warpgroup 3  warp 12: TMA producer (Q tiles, then K_j and V_j into a stage ring)
-//                warps 13, 14: tcgen05 MMA issuers for Q tiles 0 and 1 (warp 13 owns TMEM)
+//                warps 13, 14: tcgen05 MMA issuers for Q tiles 0 and 1 at D = 64;
+//                warp 13 alone issues for both at D = 128 (warp 13 owns TMEM)
+//                warp 15: merge warp of the balanced variants
 // Registers are rebalanced with setmaxnreg: the softmax warpgroups hold a
 // 128-score row per thread, the other two need little.  The producer warps
 // run as whole warps with one elected lane issuing, so their control state is
