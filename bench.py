@@ -8,7 +8,10 @@ all ranks divided by the summed device time of the calls, in TFLOP/s; each
 call is bracketed by CUDA events on the stream it is launched on, and L2 is
 flushed (a 256 MiB write) between calls, outside the events.
 
-Other keys: ``e2e`` (same metric through the C ABI with pinned host buffers,
+Other keys: ``configs`` (every workload of the task -- the five shapes, each
+mask it is run with -- timed per call the same way: mean and median ms,
+TFLOP/s and the fraction of the measured bf16 tensor peak), ``e2e`` (same
+metric through the C ABI with pinned host buffers,
 host->device and device->host copies of every step inside the timed region,
 pipelined so one step's calls overlap its neighbours' copies), ``backward``
 (fa_bwd on the same workload, per call), ``decode`` (split-KV decoding of a
@@ -89,6 +92,58 @@ def decode_timings(steps: int, dev, stream, flush, hbm_gbs: float) -> dict:
                               "kv_bytes": kv, "kv_gbs": kv / (ms * 1e-3) / 1e9,
                               "frac_of_measured_hbm": kv / (ms * 1e-3) / 1e9 / hbm_gbs})
         del q, k, v, o, lse
+    return out
+
+
+# The task's workloads, in order, each with the masks it is run with; the
+# long-context one is causal at N = 32768 and non-causal at N = 16384.
+CONFIG_WORKLOADS = ("tiny_n256", "b4h16_n1024", "b2h16_n4096", "ragged_n3000_d128_fp16", "long_n32768_d128",
+                    "long_n16384_d128")
+
+
+def config_timings(steps: int, dev, stream, flush, peak: float) -> dict:
+    """Per-call timings of every task workload and mask (fa_fwd, automatic
+    schedule; CUDA events on the launching stream, L2 flushed before each
+    call, after 3 untimed calls), with the pages' FLOP count (4*B*H*N^2*D,
+    half causal) and the exact causal count beside it."""
+    import torch
+    from exact_attention_10_gb300 import fa
+    from exact_attention_10_gb300.accounting import flops, flops_causal_exact
+    from exact_attention_10_gb300.inputs import WORKLOADS, make_qkv
+    out = {"schedule": "auto", "l2": "flushed between calls", "steps": steps, "inputs": "make_qkv(seed=0)",
+           "peak_tflops": peak, "workloads": {}}
+    for name in CONFIG_WORKLOADS:
+        w = WORKLOADS[name]
+        q, k, v = (x.to(dev) for x in make_qkv(w, seed=0))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        entry = {"shape": w.describe()}
+        for causal in w.masks:
+            for _ in range(3):
+                fa.forward(q, k, v, causal=causal, scale=w.scale, out=o, lse=lse)
+            starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            for i in range(steps):
+                flush.zero_()
+                starts[i].record(stream)
+                fa.forward(q, k, v, causal=causal, scale=w.scale, out=o, lse=lse)
+                ends[i].record(stream)
+            torch.cuda.synchronize(dev)
+            rc = fa.sync_status(stream.cuda_stream)
+            if rc != 0:
+                raise fa.FAError(rc, name)
+            ts = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+            avg = statistics.mean(ts)
+            fl = flops(w.B, w.H, w.N, w.D, causal)
+            tf = fl / (avg * 1e-3) / 1e12
+            rec = {"ms_mean": avg, "ms_median": statistics.median(ts), "tflops": tf,
+                   "frac_of_measured_peak": tf / peak, "flops_per_call": fl}
+            if causal:
+                rec["tflops_exact_causal_count"] = flops_causal_exact(w.B, w.H, w.N, w.D) / (avg * 1e-3) / 1e12
+            entry["causal" if causal else "noncausal"] = rec
+        out["workloads"][name] = entry
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
     return out
 
 
@@ -281,6 +336,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--bwd-steps", type=int, default=50, help="timed backward calls per mask (0: skip)")
     ap.add_argument("--decode-steps", type=int, default=30, help="timed split-KV decode calls per shape (0: skip)")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed calls per task workload and mask (0: skip)")
     args = ap.parse_args(argv)
 
     from exact_attention_10_gb300.inputs import WORKLOADS
@@ -489,6 +545,9 @@ def main(argv=None):
             "clocks": clk, "gpu_launches": args.steps * len(modes), "wall_s_timed_region": wall}
     if bwd_info is not None:
         line["backward"] = bwd_info
+    if args.config_steps > 0:
+        # every task workload, outside the headline's timed region
+        line["configs"] = config_timings(args.config_steps, dev, stream, flush, peak)
     if args.decode_steps > 0:
         # outside the timed region; a failure here is reported in the object
         # and leaves the line's own measurements as they are

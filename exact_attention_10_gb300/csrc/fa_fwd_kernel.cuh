@@ -137,6 +137,11 @@ struct MergeJob {
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
+// Guarded lazy rescale (softmax_role): a new row max may leave the reference
+// max in place when it exceeds it by at most kLazyMax (log2 units) and the
+// row's sum is at least kLazyWeight times the new maximum's probability.
+constexpr float kLazyMax = 8.f;
+constexpr float kLazyWeight = 16.f;
 
 // Wait sites recorded in the status word.
 enum : uint32_t {
@@ -792,14 +797,28 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
                     mx[k] = ptx::fmax3(mx[k], s[i + 2 * k], s[i + 2 * k + 1]);
             const float tile_max = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]), ptx::fmax3(mx[3], mx[4], mx[5]),
                                               fmaxf(mx[6], mx[7])) * p.qk_scale;
-            // The running max changes only when this tile holds a larger score
-            // (always on the first visible tile, where m = -inf); otherwise
-            // alpha = 1 and nothing is rescaled.  (A stale max within a
-            // threshold would save rescales but is not used: with it a row's
-            // dominant probability is no longer exactly 1, and its 16-bit
-            // rounding lands on outputs dominated by one key -- measured
-            // 1.7e-2 in bf16 with Q and K amplified 4x.)
-            const bool move = tile_max > m;
+            // The reference max m moves only when this tile holds a larger
+            // score (always on the first visible tile, where m = -inf);
+            // otherwise alpha = 1 and nothing is rescaled.  Any reference
+            // gives the same exact result (the recurrence divides by l
+            // relative to the same m), so a larger score may also leave m
+            // where it is (a guarded lazy rescale):
+            //  * the new score exceeds m by at most kLazyMax (log2 units),
+            //    so every probability stays at most 2^kLazyMax, and
+            //  * the row's sum so far is at least kLazyWeight times that
+            //    score's probability, so no single key carries more than
+            //    1/kLazyWeight of the row's weight.
+            // The second condition guards the precision: the largest
+            // probability is then no longer exactly 1, so its 16-bit
+            // rounding (relative 2^-8 in bf16) reaches the output, but
+            // weighted by at most 1/kLazyWeight.  Rows dominated by one key
+            // (large logits) never meet it and rescale exactly.  Most steps
+            // of long rows meet both, and a warp none of whose rows moved
+            // skips the rescale of O.
+            const bool up = tile_max > m;
+            const float dlt = tile_max - m;   // (+inf on the first visible tile)
+            const bool lazy = up && dlt <= kLazyMax && l >= kLazyWeight * ptx::ex2(dlt);
+            const bool move = up && !lazy;
             const float m_new = move ? tile_max : m;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;   // no visible key yet: shift 0
             const float alpha = move ? ptx::ex2(m - m_use) : 1.f;     // 0 on the first tile (m = -inf)

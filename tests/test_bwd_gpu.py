@@ -3,9 +3,9 @@
 The CUDA path takes O and LSE from the library's own forward (as a training
 step would) and an upstream gradient dO; the oracle differentiates the exact
 attention of the same Q, K, V.  Errors are measured normwise per gradient,
-||g - g_ref|| / ||g_ref||, plus the largest element error relative to the
-largest reference element, against bounds derived from the rounding the
-path performs (see BOUNDS).  Cases cover D = 64 and 128, bf16 and fp16,
+||g - g_ref|| / ||g_ref||, and row by row: each row's largest element error
+against that row's own largest reference element plus the gradient's RMS
+(see BOUNDS).  Cases cover D = 64 and 128, bf16 and fp16,
 causal and not, one and several 128-row tiles, ragged lengths, N = 1, and a
 4096-row sequence compared in full.
 """
@@ -27,10 +27,24 @@ pytestmark = pytest.mark.gpu
 # roundoff u (2^-8 bf16, 2^-11 fp16), each rounding contributes at most u/2
 # relative to the terms it touches, and four of them stack on dK and dQ (O via
 # delta, dS, the output, and P inside dS's factor), so the normwise error is
-# bounded by about 2u; the bounds below allow 4u normwise and 16u on the
-# largest element relative to the largest reference element.
+# bounded by about 2u.
+#
+# The bounds are set from the errors measured on a GB300 over the cases below
+# (both dtypes, D = 64 and 128, causal and not, N from 128 to 4096), with a
+# stated margin:
+#   normwise: measured at most 0.67u on every gradient; bound 1.5u (2.2x).
+#   per row r of a gradient (a query row of dQ, a key row of dK and dV):
+#     max_d |g - g_ref|  <=  12u * (max_d |g_ref[r]| + rms(g_ref)).
+#   A row's error scales with its own magnitude, and rows whose exact
+#   gradient is (nearly) zero -- causal row 0 of dQ, where P = 1 and dS = 0,
+#   and the first few causal rows -- keep an error from the fp32 cancellation
+#   in dP - delta, set by the gradient's overall scale, hence the RMS term.
+#   Measured at most 7.6u (dQ of the first causal rows: row 1 of a head, in
+#   bf16); bound 12u (1.6x).
+# A wrong term on any row of ordinary magnitude shows as an error of the
+# order of that row itself, hundreds of u.
 U = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}
-BOUNDS = {dt: {"norm": 4 * u, "max": 16 * u} for dt, u in U.items()}
+BOUNDS = {dt: {"norm": 1.5 * u, "row": 12 * u} for dt, u in U.items()}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -56,22 +70,38 @@ def _gpu_grads(q, k, v, do, causal, scale):
     return dq.cpu(), dk.cpu(), dv.cpu()
 
 
-def _errors(g, ref):
+def _rms(x):
+    return float(np.sqrt(np.mean(np.square(x)))) if x.size else 0.0
+
+
+def _errors(g, ref, floor):
+    """(normwise error, worst per-row error ratio, its row): the row ratio is
+    max_d |g - g_ref| / (max_d |g_ref[r]| + floor) over rows r, floor being
+    the gradient's RMS.  (The normwise error of an identically zero reference
+    is taken against the floor.)"""
     gd = g.double().numpy().reshape(ref.shape)
     assert np.isfinite(gd).all()
     nref = float(np.linalg.norm(ref))
-    norm = float(np.linalg.norm(gd - ref)) / nref if nref > 0 else float(np.linalg.norm(gd))
-    mref = float(np.abs(ref).max())
-    mx = float(np.abs(gd - ref).max()) / mref if mref > 0 else float(np.abs(gd).max())
-    return norm, mx
+    norm = float(np.linalg.norm(gd - ref)) / (nref if nref > 0 else floor * np.sqrt(ref.size))
+    D = ref.shape[-1]
+    err = np.abs(gd - ref).reshape(-1, D).max(axis=1)
+    scale = np.abs(ref).reshape(-1, D).max(axis=1) + floor
+    ratio = err / scale
+    worst = int(ratio.argmax())
+    return norm, float(ratio[worst]), worst
 
 
 def _check(grads, refs, dtype, label):
+    u = U[dtype]
+    # A gradient whose exact value is zero everywhere (one visible key per
+    # query: P = 1, dS = 0, so dQ = dK = 0) keeps only the fp32 cancellation
+    # residue of dP - delta; its floor is the RMS of all three gradients.
+    rms_all = _rms(np.concatenate([r.reshape(-1) for r in refs]))
     for name, g, ref in zip(("dQ", "dK", "dV"), grads, refs):
-        norm, mx = _errors(g, ref)
-        print(f"{label} {name}: normwise {norm:.2e}  max/max|ref| {mx:.2e}")
-        assert norm <= BOUNDS[dtype]["norm"], (label, name, norm)
-        assert mx <= BOUNDS[dtype]["max"], (label, name, mx)
+        norm, row, where = _errors(g, ref, _rms(ref) or rms_all)
+        print(f"{label} {name}: normwise {norm / u:.2f}u  worst row {row / u:.2f}u (flattened row {where})")
+        assert norm <= BOUNDS[dtype]["norm"], (label, name, norm / u)
+        assert row <= BOUNDS[dtype]["row"], (label, name, row / u, where)
 
 
 CASES = [  # (B, H, N, D, dtype)
