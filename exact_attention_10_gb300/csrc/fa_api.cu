@@ -237,9 +237,9 @@ fa_status launch_whole(int D, bool bf16, bool causal, const CUtensorMap &q, cons
                   : launch_mask<fa::kMaskNone, false>(D, bf16, q, k, v, p, grid, s, dev);
 }
 
-bool take_status_word_whole(unsigned int *word)
+bool take_status_word_whole(cudaStream_t s, unsigned int *word)
 {
-    return take_status_word_here(word);
+    return fa::take_status_word_on(s, word);
 }
 
 }  // namespace fa_launch
@@ -314,7 +314,11 @@ fa_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *
     p.Nkv = Nkv;
     p.off = causal ? Nkv - N : 0;
     p.qk_scale = scale * 1.4426950408889634f;   // scale * log2(e)
-    p.sch = fa::sched_plan(N, Nkv, (int)BH, causal != 0, di->sms, (int)schedule, wl, wr);
+    // A call that may not allocate takes whole tiles where the automatic
+    // plan would need more than its static workspace.
+    p.sch = no_alloc ? fa::sched_plan_limited(N, Nkv, (int)BH, causal != 0, di->sms, (int)schedule, wl, wr, D,
+                                              FA_NOALLOC_WORKSPACE_BYTES)
+                     : fa::sched_plan(N, Nkv, (int)BH, causal != 0, di->sms, (int)schedule, wl, wr);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (p.sch.split) {
         const fa_status ws =
@@ -492,9 +496,10 @@ extern "C" fa_status fa_sync_status(fa_stream_t stream)
         cudaGetLastError();
         return FA_ERR_CUDA;
     }
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     unsigned int w_whole = 0, w_split = 0, w_band = 0, w_bwd = 0;
-    if (!fa_launch::take_status_word_whole(&w_whole) || !fa_launch::take_status_word_split(&w_split) ||
-        !fa_launch::take_status_word_band(&w_band) || !fa_launch::take_status_word_bwd(&w_bwd))
+    if (!fa_launch::take_status_word_whole(s, &w_whole) || !fa_launch::take_status_word_split(s, &w_split) ||
+        !fa_launch::take_status_word_band(s, &w_band) || !fa_launch::take_status_word_bwd(s, &w_bwd))
         return FA_ERR_CUDA;
     if ((w_whole | w_split | w_band | w_bwd) != 0) {
         // an aborted launch may have left split-tile counters non-zero

@@ -11,9 +11,9 @@ fa_status launch_band(int D, bool bf16, bool split, const CUtensorMap &q, const 
                  : launch_mask<fa::kMaskBand, false>(D, bf16, q, k, v, p, grid, s, dev);
 }
 
-bool take_status_word_band(unsigned int *word)
+bool take_status_word_band(cudaStream_t s, unsigned int *word)
 {
-    return take_status_word_here(word);
+    return fa::take_status_word_on(s, word);
 }
 
 }  // namespace fa_launch

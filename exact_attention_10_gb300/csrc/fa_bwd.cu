@@ -90,21 +90,9 @@ fa_status launch_bwd(const BwdLaunch &a, cudaStream_t s, int dev)
     return a.causal ? launch_all<128, false, true>(a, s, dev) : launch_all<128, false, false>(a, s, dev);
 }
 
-bool take_status_word_bwd(unsigned int *word)
+bool take_status_word_bwd(cudaStream_t s, unsigned int *word)
 {
-    *word = 0;
-    if (cudaMemcpyFromSymbol(word, fa::g_status_word, sizeof *word) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    if (*word != 0) {
-        const unsigned int zero = 0;
-        if (cudaMemcpyToSymbol(fa::g_status_word, &zero, sizeof zero) != cudaSuccess) {
-            cudaGetLastError();
-            return false;
-        }
-    }
-    return true;
+    return fa::take_status_word_on(s, word);
 }
 
 }  // namespace fa_launch

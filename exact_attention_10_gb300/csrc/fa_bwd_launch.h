@@ -23,6 +23,6 @@ struct BwdLaunch {
 
 // Enqueue the pre-pass, the dQ pass and the dK/dV pass on `s`.
 fa_status launch_bwd(const BwdLaunch &a, cudaStream_t s, int dev);
-bool take_status_word_bwd(unsigned int *word);
+bool take_status_word_bwd(cudaStream_t s, unsigned int *word);
 
 }  // namespace fa_launch

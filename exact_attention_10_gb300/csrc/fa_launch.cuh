@@ -64,25 +64,6 @@ fa_status launch_mask(int D, bool bf16, const CUtensorMap &q, const CUtensorMap 
                 : launch_variant<128, false, MASK, SPLIT>(q, k, v, p, grid, s, dev);
 }
 
-// Read and clear this translation unit's device status word (current
-// device) into *word; false if the copy failed.
-inline bool take_status_word_here(unsigned int *word)
-{
-    *word = 0;
-    if (cudaMemcpyFromSymbol(word, fa::g_status_word, sizeof *word) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    if (*word != 0) {
-        const unsigned int zero = 0;
-        if (cudaMemcpyToSymbol(fa::g_status_word, &zero, sizeof zero) != cudaSuccess) {
-            cudaGetLastError();
-            return false;
-        }
-    }
-    return true;
-}
-
 }  // namespace
 
 // Defined in fa_api.cu, fa_split.cu and fa_band.cu respectively; `causal`
@@ -93,9 +74,9 @@ fa_status launch_split(int D, bool bf16, bool causal, const CUtensorMap &q, cons
                        const CUtensorMap &v, const fa::FwdParams &p, int grid, cudaStream_t s, int dev);
 fa_status launch_band(int D, bool bf16, bool split, const CUtensorMap &q, const CUtensorMap &k,
                       const CUtensorMap &v, const fa::FwdParams &p, int grid, cudaStream_t s, int dev);
-bool take_status_word_whole(unsigned int *word);
-bool take_status_word_split(unsigned int *word);
-bool take_status_word_band(unsigned int *word);
+bool take_status_word_whole(cudaStream_t s, unsigned int *word);
+bool take_status_word_split(cudaStream_t s, unsigned int *word);
+bool take_status_word_band(cudaStream_t s, unsigned int *word);
 
 // The static workspace of fa_fwd_noalloc (fa_split.cu): points p's partial
 // buffers into it for schedule `sc` and head size D, and clears the counters
@@ -110,7 +91,7 @@ inline size_t workspace_bytes(const fa::Schedule &sc, int D, size_t *o_bytes, si
     *o_bytes = slots * fa::kCtaRows * D * sizeof(float);
     *ml_bytes = slots * fa::kCtaRows * sizeof(float2);
     *cnt_bytes = (size_t)2 * sc.T * sizeof(int);
-    return *o_bytes + *ml_bytes + *cnt_bytes;
+    return *o_bytes + *ml_bytes + *cnt_bytes;   // (= fa::sched_workspace_bytes of a balanced schedule)
 }
 
 }  // namespace fa_launch

@@ -627,4 +627,29 @@ inline Schedule sched_plan(int N, int Nkv, int BH, bool causal, int sms, int mod
     return s;
 }
 
+// Workspace bytes of a balanced schedule at head size D: a partial O
+// ([256 rows][D] fp32) and (m, l) per row for two slots per CTA, then two
+// int counters per CTA tile (one per Q tile).  Whole tiles need none.
+inline unsigned long long sched_workspace_bytes(const Schedule &s, int D)
+{
+    if (!s.split)
+        return 0ull;
+    const unsigned long long slots = 2ull * (unsigned long long)s.G;
+    return slots * 256ull * (unsigned long long)D * 4ull + slots * 256ull * 8ull + 2ull * (unsigned long long)s.T * 4ull;
+}
+
+// The plan of a call that may not allocate (a fixed workspace of `limit`
+// bytes): the planner's choice for `mode`, except that an automatic choice
+// of the balanced schedule whose workspace exceeds the limit falls back to
+// whole tiles, which need none.  An explicit request is kept as it is (the
+// caller reports the limit).
+inline Schedule sched_plan_limited(int N, int Nkv, int BH, bool causal, int sms, int mode, int wl, int wr, int D,
+                                   unsigned long long limit)
+{
+    Schedule s = sched_plan(N, Nkv, BH, causal, sms, mode, wl, wr);
+    if (mode == 0 && s.split && sched_workspace_bytes(s, D) > limit)
+        s = sched_plan(N, Nkv, BH, causal, sms, 1, wl, wr);
+    return s;
+}
+
 }  // namespace fa

@@ -13,9 +13,9 @@ fa_status launch_split(int D, bool bf16, bool causal, const CUtensorMap &q, cons
                   : launch_mask<fa::kMaskNone, true>(D, bf16, q, k, v, p, grid, s, dev);
 }
 
-bool take_status_word_split(unsigned int *word)
+bool take_status_word_split(cudaStream_t s, unsigned int *word)
 {
-    return take_status_word_here(word);
+    return fa::take_status_word_on(s, word);
 }
 
 namespace {

@@ -194,10 +194,13 @@ FA_API fa_status fa_fwd_band(const void *Q, const void *K, const void *V, void *
  * clears the partial-result counters (which must start at zero) with an
  * asynchronous memset on `stream`.
  *
- * Limit: a call whose schedule (as fa_fwd_ex would choose it) needs more
- * workspace than the array holds returns FA_ERR_NO_ALLOC_LIMIT before
- * anything is enqueued.  The partial-result slots always fit; the counters
- * take 8 bytes per 256 query rows per head, so B*H*ceil(N/256) may reach
+ * Limit: with FA_SCHEDULE_AUTO, where the automatic plan would split tiles
+ * into more partial results than the array holds, the call runs whole tiles
+ * instead, which need no workspace.  A call with FA_SCHEDULE_BALANCED whose
+ * schedule needs more workspace than the array holds returns
+ * FA_ERR_NO_ALLOC_LIMIT before anything is enqueued.  The partial-result
+ * slots always fit; the counters take 8 bytes per 256 query rows per head,
+ * so B*H*ceil(N/256) may reach
  * 966,656 -- e.g. B*H = 256 at N = 965,000.  Whole-tile calls need no
  * workspace and have no limit.
  *
@@ -266,6 +269,18 @@ FA_API fa_status fa_bwd_band(const void *Q, const void *K, const void *V, const 
  * status word of the current device: FA_OK, FA_ERR_DEVICE_TIMEOUT if a kernel
  * gave up on a wait since the last call, or FA_ERR_CUDA if the synchronise
  * itself failed.
+ *
+ * The word is read and cleared in one atomic exchange by a one-thread kernel
+ * on `stream`, so a timeout recorded meanwhile is never lost.  There is one
+ * word per device, shared by all streams: a timeout from a kernel on another
+ * stream is reported by whichever call reads the word first, and a timeout
+ * from a kernel on another stream that has not finished yet is reported only
+ * by a later call.  To attribute a timeout to a stream, synchronise the
+ * others first.
+ *
+ * Device resets: the library keeps, per device, a lazily created workspace,
+ * the status word and the static workspace's address.  A call that follows
+ * cudaDeviceReset() on that device in the same process is not supported.
  */
 FA_API fa_status fa_sync_status(fa_stream_t stream);
 

@@ -235,8 +235,53 @@ static int check_schedule(const Schedule &s, bool planned, int wl, int wr)
     return 0;
 }
 
+// sched_plan_limited with a workspace limit of `limit` bytes: an automatic
+// balanced plan that needs more falls back to whole tiles (no workspace);
+// one that fits, a whole-tile plan and an explicit balanced request are kept
+// as sched_plan makes them.  *fell_back counts the fallbacks seen.
+static int check_limited(int N, int Nkv, int BH, int causal, int sms, int wl, int wr, int D,
+                         unsigned long long limit, int *fell_back)
+{
+    const Schedule a = sched_plan(N, Nkv, BH, causal != 0, sms, 0, wl, wr);
+    const Schedule l = sched_plan_limited(N, Nkv, BH, causal != 0, sms, 0, wl, wr, D, limit);
+    const bool over = a.split && sched_workspace_bytes(a, D) > limit;
+    if (over) {
+        ++*fell_back;
+        const Schedule w = sched_plan(N, Nkv, BH, causal != 0, sms, 1, wl, wr);
+        if (l.split || sched_workspace_bytes(l, D) != 0 || l.G != w.G || l.T != w.T || l.U != w.U)
+            return 1;
+    } else if (l.split != a.split || l.G != a.G || l.T != a.T || l.U != a.U) {
+        return 1;
+    }
+    for (int mode = 1; mode <= 2; ++mode) {   // explicit requests are never changed
+        const Schedule e = sched_plan(N, Nkv, BH, causal != 0, sms, mode, wl, wr);
+        const Schedule el = sched_plan_limited(N, Nkv, BH, causal != 0, sms, mode, wl, wr, D, limit);
+        if (e.split != el.split || e.G != el.G || e.U != el.U)
+            return 1;
+    }
+    return check_schedule(l, true, wl, wr);
+}
+
 int main(int argc, char **argv)
 {
+    // "limit L" then "N Nkv BH causal sms wl wr D" cases: the no-allocation planner
+    if (argc > 2 && std::string(argv[1]) == "limit") {
+        const unsigned long long limit = std::strtoull(argv[2], nullptr, 10);
+        int failures = 0, cases = 0, fell_back = 0;
+        for (int i = 3; i + 8 <= argc; i += 8) {
+            int v[8];
+            for (int k = 0; k < 8; ++k)
+                v[k] = std::atoi(argv[i + k]);
+            const int wl = v[5] < 0 ? kSchedUnbounded : v[5], wr = v[6] < 0 ? kSchedUnbounded : v[6];
+            ++cases;
+            if (check_limited(v[0], v[1], v[2], v[3], v[4], wl, wr, v[7], limit, &fell_back)) {
+                std::printf("FAILED limit N=%d Nkv=%d BH=%d causal=%d sms=%d D=%d\n", v[0], v[1], v[2], v[3], v[4], v[7]);
+                ++failures;
+            }
+        }
+        std::printf("%d cases, %d failures, %d fallbacks\n", cases, failures, fell_back);
+        return failures ? 1 : 0;
+    }
     // "N Nkv BH causal G split wl wr" cases, repeated; or "plan" then "N Nkv BH causal sms wl wr" cases
     // (wl, wr < 0: unbounded)
     int failures = 0, cases = 0;

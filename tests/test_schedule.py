@@ -90,3 +90,24 @@ def test_schedule_exhaustive(checker):
     res = subprocess.run([checker, *args], capture_output=True, text=True, timeout=600)
     assert res.returncode == 0, res.stdout[-2000:]
     assert f"{len(CASES)} cases, 0 failures" in res.stdout
+
+
+def test_no_alloc_planner_falls_back_to_whole_tiles(checker):
+    """fa_fwd_noalloc's planner (sched_plan_limited): where the automatic
+    plan would split tiles into more partial results than the static
+    workspace holds, it runs whole tiles, which need none; otherwise, and for
+    explicit requests, it plans exactly as fa_fwd_ex does.  The automatic
+    plan never needs more than the real 48 MiB limit on these shapes, so the
+    fallback is exercised with small limits as well."""
+    cases = [(4096, 4096, 32, 0, 152, -1, 0, 64), (4096, 4096, 32, 1, 152, -1, 0, 64),
+             (4, 32768, 32, 0, 152, -1, 0, 128), (1, 8192, 256, 0, 152, -1, 0, 128),
+             (4, 131072, 8, 1, 152, -1, 0, 128), (3000, 3000, 16, 0, 152, -1, 0, 128),
+             (16384, 16384, 32, 0, 152, -1, 0, 128), (8192, 8192, 3, 1, 152, 1000, -1, 64),
+             (1024, 1024, 64, 0, 152, -1, 0, 64)]
+    for limit, expect_fallbacks in ((48 << 20, False), (1 << 20, True), (0, True)):
+        args = ["limit", str(limit)] + [str(x) for case in cases for x in case]
+        res = subprocess.run([checker, *args], capture_output=True, text=True, timeout=600)
+        assert res.returncode == 0, res.stdout[-2000:]
+        assert f"{len(cases)} cases, 0 failures" in res.stdout, res.stdout
+        fallbacks = int(res.stdout.split(",")[-1].split()[0])
+        assert (fallbacks > 0) == expect_fallbacks, (limit, res.stdout)

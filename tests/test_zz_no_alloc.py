@@ -93,3 +93,10 @@ def test_rejects_a_call_beyond_its_workspace(lib):
     assert _call(lib.fa_fwd_ex, q, q, q, ref, ref_lse, False, WHOLE, 0.125) == 0
     torch.cuda.synchronize()
     assert torch.equal(o, ref) and torch.equal(lse, ref_lse)
+    # the automatic schedule never fails on the limit: where its plan would
+    # not fit it runs whole tiles (its planner is checked on the CPU in
+    # tests/test_schedule.py with smaller limits)
+    o.fill_(7.0)
+    assert _call(lib.fa_fwd_noalloc, q, q, q, o, lse, False, AUTO, 0.125) == 0
+    assert lib.fa_sync_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+    assert torch.equal(o, ref) and torch.equal(lse, ref_lse)
