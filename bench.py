@@ -108,7 +108,7 @@ def config_timings(steps: int, dev, stream, flush, peak: float) -> dict:
     half causal) and the exact causal count beside it."""
     import torch
     from exact_attention_10_gb300 import fa
-    from exact_attention_10_gb300.accounting import flops, flops_causal_exact
+    from exact_attention_10_gb300.accounting import flops, flops_causal_exact, fused_bytes
     from exact_attention_10_gb300.inputs import WORKLOADS, make_qkv
     out = {"schedule": "auto", "l2": "flushed between calls", "steps": steps, "inputs": "make_qkv(seed=0)",
            "peak_tflops": peak, "workloads": {}}
@@ -140,6 +140,12 @@ def config_timings(steps: int, dev, stream, flush, peak: float) -> dict:
                    "frac_of_measured_peak": tf / peak, "flops_per_call": fl}
             if causal:
                 rec["tflops_exact_causal_count"] = flops_causal_exact(w.B, w.H, w.N, w.D) / (avg * 1e-3) / 1e12
+            # DRAM bytes per launch from a committed ncu capture of this kernel
+            # on this workload (current kernel source only), beside the
+            # algorithmic bytes (Q, K, V read, O written, fp32 LSE)
+            kname = f"fa_fwd_sm103<{w.D},{w.dtype},{'causal' if causal else 'noncausal'}>"
+            rec["algorithmic_bytes"] = fused_bytes(w.B, w.H, w.N, w.D)
+            rec["traffic"] = _traffic_record(kname, workload_name=name)
             entry["causal" if causal else "noncausal"] = rec
         out["workloads"][name] = entry
         del q, k, v, o, lse
@@ -223,9 +229,10 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(use)}
 
 
-def _traffic_record(kernel_name: str):
+def _traffic_record(kernel_name: str, workload_name: str | None = None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (matched by content hash); otherwise None."""
+    the current kernel source (matched by content hash) and, when
+    ``workload_name`` is given, on that workload; otherwise None."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
@@ -240,6 +247,8 @@ def _traffic_record(kernel_name: str):
             h.update(f.read())
     entry = rec.get(kernel_name)
     if not entry or entry.get("source_sha256") != h.hexdigest():
+        return None
+    if workload_name is not None and entry.get("workload_name") != workload_name:
         return None
     return entry.get("dram_bytes_per_launch")
 

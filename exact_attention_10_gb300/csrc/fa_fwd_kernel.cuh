@@ -728,6 +728,40 @@ __device__ void mma_role(int w, const FwdParams &p, uint32_t sQ, uint32_t sStage
 
 // ------------------------------------------------------------------ softmax
 
+// Hide keys i >= hi (0 <= i < 128, hi per thread) of this thread's row of S
+// in TMEM, by writing -inf there, before the row is read: the 32-column
+// chunks that every row of the warp hides are overwritten whole, and the
+// chunks that the warp's rows split are read, masked row by row and written
+// back.  Warp-collective (tS is the warp's lane quarter of S).  Out of line
+// and rolled, so the softmax loop carries one call instead of a compare and
+// select per score; it runs on masked steps only (the causal diagonal, the
+// ragged last key tile), and the scores read afterwards are the ones the
+// per-score mask would have produced.
+static __device__ __noinline__ void mask_s_tail(uint32_t tS, int hi)
+{
+    hi = hi < 0 ? 0 : (hi > kBN ? kBN : hi);
+    const int lo_w = __reduce_min_sync(0xffffffffu, hi), hi_w = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t ninf = __float_as_uint(-INFINITY);
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBN; c0 += 32) {
+        uint32_t x[32];
+        if (c0 >= hi_w) {   // hidden in every row of the warp
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                x[i] = ninf;
+            ptx::tmem_st32(tS + (uint32_t)c0, x);
+        } else if (c0 + 32 > lo_w) {   // the warp's rows split this chunk
+            ptx::tmem_ld32(tS + (uint32_t)c0, x);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                x[i] = (c0 + i < hi) ? x[i] : ninf;
+            ptx::tmem_st32(tS + (uint32_t)c0, x);
+        }
+    }
+    ptx::tmem_wait_st();
+}
+
 // SEP as in mma_role.  At D = 128 its waits record a timeout inline: they
 // hold S, P or O rescale registers, which a call made the balanced variant
 // spill (1.3 % slower); at D = 64 the inline form measured 1.4 % slower.
@@ -774,22 +808,23 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
         }
         float m = -INFINITY, l = 0.f;                               // running max (log2 units), row sum
 
-        // One step of the recurrence; false if a wait gave up.  MV (a
-        // compile-time constant) says where the mask is applied: 0 never,
-        // 1 always, 2 when `masked` holds.  Whole-tile launches without a
-        // mask (MASK = none) call the copies 0 and 1, so the copy that the
-        // steps without a ragged edge run holds no mask code: the size of
-        // the loop body sets how often its instructions are fetched anew
-        // (measured at D = 64: N = 16384 5.6 % and N = 4096 3 % faster).
-        // Masked and balanced launches keep one copy (MV = 2): there the two
-        // copies cost more in fetches than they saved (causal 5 %, balanced
-        // 1 % slower).
-        auto step = [&](auto mv_c, int jr, int kb0, bool masked) -> bool {
-            constexpr int MV = decltype(mv_c)::value;
+        // One step of the recurrence; false if a wait gave up.  At D = 64 a
+        // masked step without a left band bound has the keys its rows hide
+        // set to -inf in TMEM before S is read (mask_s_tail, out of line), so
+        // the loop body holds no per-score mask code: the size of the loop
+        // body sets how often its instructions are fetched anew (measured:
+        // B2 H16 N4096 3-5 % and N16384 3-8 % faster, results bit for bit
+        // the same).  At D = 128, where a step carries twice the tensor work,
+        // the call measured 1.5 % slower than the per-score code, which it
+        // keeps.
+        auto step = [&](int jr, int kb0, bool masked) -> bool {
             if (!warp_wait<D == 128>(b.s_full(w), s_phase & 1u, c, kSiteSoftSFull))
                 return false;
             ++s_phase;
             ptx::tc_fence_after_sync();
+            constexpr bool TMEM_MASK = (D == 64 && MASK != kMaskBand);
+            if (TMEM_MASK && masked)
+                mask_s_tail(tS, row_hi - kb0);   // keys kb0 + i with i < row_hi - kb0 are visible
 
             uint32_t r[2][64];
             ptx::tmem_ld64(tS, r[0]);   // the whole row of S_w in two instructions
@@ -805,7 +840,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             for (int i = 0; i < 128; ++i)
                 s[i] = __uint_as_float(r[i / 64][i % 64]);
 
-            if (MV == 1 || (MV == 2 && masked)) {
+            if (!TMEM_MASK && masked) {
                 if (MASK == kMaskBand) {
                     // key kb0 + i is visible iff row_lo <= kb0 + i < row_hi (one unsigned compare)
                     const int lo = row_lo - kb0;
@@ -919,15 +954,7 @@ __device__ void softmax_role(const FwdParams &p, uint32_t tmem, Bars<D> b, Ctl c
             // masked where some row's band edge or the key count ends inside the step
             const bool masked = (MASK == kMaskBand) ? (kb0 < edge_lo || kb0 + kBN > edge_hi)   // (edge_hi <= Nkv)
                                                     : ((CAUSAL && kb0 + kBN > edge_hi) || kb0 + kBN > p.Nkv);
-            using MV0 = std::integral_constant<int, 0>;
-            using MV1 = std::integral_constant<int, 1>;
-            using MV2 = std::integral_constant<int, 2>;
-            bool ok;
-            if constexpr (MASK == kMaskNone && !SPLIT)
-                ok = masked ? step(MV1{}, jr, kb0, true) : step(MV0{}, jr, kb0, false);
-            else
-                ok = step(MV2{}, jr, kb0, masked);
-            if (!ok)
+            if (!step(jr, kb0, masked))
                 return;
         }
         if (sep) {   // account for the last P.V of this tile
