@@ -63,7 +63,10 @@ DECODE_SHAPES = ((1, 32, 4, 32768, 128), (8, 32, 1, 8192, 128))
 def decode_timings(steps: int, dev, stream, flush, hbm_gbs: float) -> dict:
     """Mean time of `steps` fa_fwd_qkv calls per decode shape (CUDA events on
     the launching stream, L2 flushed before each call) and the K/V bandwidth
-    it implies, against the measured HBM copy rate."""
+    it implies, against the measured HBM copy rate.  The same calls are also
+    timed back to back without the flush (``us_mean_no_flush``): their K/V
+    (0.5-1 GB) is larger than L2 either way, so the difference is the cost of
+    starting each call with the kernel's code and scheduling data cold."""
     import torch
     from exact_attention_10_gb300 import fa
     out = {"dtype": "bf16", "schedule": "auto", "l2": "flushed between calls", "steps": steps, "shapes": []}
@@ -87,10 +90,21 @@ def decode_timings(steps: int, dev, stream, flush, hbm_gbs: float) -> dict:
         if rc != 0:
             raise fa.FAError(rc, "decode")
         ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
+        for i in range(steps):
+            starts[i].record(stream)
+            fa.forward(q, k, v, scale=D ** -0.5, out=o, lse=lse)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        rc = fa.sync_status(stream.cuda_stream)
+        if rc != 0:
+            raise fa.FAError(rc, "decode")
+        ms_nf = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
         kv = 2 * B * H * Nkv * D * 2
         out["shapes"].append({"B": B, "H": H, "Nq": Nq, "Nkv": Nkv, "D": D, "us_mean": ms * 1e3,
                               "kv_bytes": kv, "kv_gbs": kv / (ms * 1e-3) / 1e9,
-                              "frac_of_measured_hbm": kv / (ms * 1e-3) / 1e9 / hbm_gbs})
+                              "frac_of_measured_hbm": kv / (ms * 1e-3) / 1e9 / hbm_gbs,
+                              "us_mean_no_flush": ms_nf * 1e3,
+                              "frac_of_measured_hbm_no_flush": kv / (ms_nf * 1e-3) / 1e9 / hbm_gbs})
         del q, k, v, o, lse
     return out
 
