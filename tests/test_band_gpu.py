@@ -70,6 +70,11 @@ SQUARE = [  # (B, H, N, D, dtype, (left, right))
     (1, 2, 2049, 128, "bf16", (128, 129)),   # edges one past a tile boundary
     (1, 2, 513, 64, "bf16", (600, 600)),     # wider than the sequence: no mask
     (1, 2, 300, 128, "fp16", (0, 5)),        # looking ahead only: keys i..i+5
+    # unbounded on the left at D = 64: the causal kernels, whose masked steps
+    # hide keys in TMEM before S is read; right edges off the 32-column chunks
+    (1, 3, 1500, 64, "bf16", (-1, 50)),
+    (1, 2, 777, 64, "fp16", (-1, 5)),
+    (2, 2, 1000, 64, "bf16", (-1, 31)),
 ]
 
 
