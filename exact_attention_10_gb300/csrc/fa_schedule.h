@@ -27,6 +27,13 @@
 //    the last part to finish merges them.  A CTA holds at most two partial
 //    parts (the first and the last of its range), in slots 2c and 2c + 1.
 //    The mixed causal order spreads the fixed cost of each part evenly too.
+//  * tail split (a balanced schedule with W > 0, non-causal only): CTA c
+//    first runs whole tiles cW .. cW + W - 1, W = floor(T / G); only the
+//    T - WG tiles of the last, partial wave are laid out as units (from 0)
+//    and split into ranges as above, over the first Gt CTAs.  A CTA's tail
+//    part comes first, so that the merges overlap its whole tiles; and only
+//    the last wave's tiles are cut, about half as many parts and merges as
+//    when every range is cut (each CTA then has one tail part, not two).
 #pragma once
 
 #include <cstdint>
@@ -65,7 +72,8 @@ struct Schedule {
     int rev;        // masked: 1 if the first tile row is longer than the last (a band bounded on the left only)
     int G;          // CTAs in the grid
     int split;      // 1: balanced schedule with partial tiles
-    long long U;    // total units (the balanced schedule requires U <= kSchedMaxUnits)
+    int W;          // balanced: whole tiles per CTA before its units (tail split; 0: every tile is in units)
+    long long U;    // units laid out in ranges (balanced; the tail's alone when W > 0; at most kSchedMaxUnits)
     int range[kSchedMaxGrid + 1];   // balanced: range[c] = floor(U c / G), filled by sched_fill_ranges
 };
 
@@ -282,11 +290,12 @@ FA_HD int sched_steps(const Schedule &s, int t)
     return sched_steps_ct(s, ct);
 }
 
-// Units of all tiles before tile t.
+// Units of all tiles before tile t (tail split: the tail's tiles before t,
+// for t >= WG).
 FA_HD long long sched_prefix(const Schedule &s, int t)
 {
     if (!s.causal)
-        return (long long)t * s.nkv;
+        return (long long)(t - s.W * s.G) * s.nkv;
     if (s.split) {
         const int q = t / (2 * s.BH);
         long long acc = 0;
@@ -312,11 +321,15 @@ FA_HD long long sched_total_units(const Schedule &s)
 }
 
 // Fill the table of CTA range starts (host side; keeps 64-bit divisions out of
-// the kernel).  Requires G <= kSchedMaxGrid and U <= kSchedMaxUnits.
-inline void sched_fill_ranges(Schedule &s)
+// the kernel): the units split evenly over the first gt CTAs (all G when gt
+// is 0); the others' ranges are empty.  Requires G <= kSchedMaxGrid and
+// U <= kSchedMaxUnits.
+inline void sched_fill_ranges(Schedule &s, int gt = 0)
 {
+    if (gt <= 0 || gt > s.G)
+        gt = s.G;
     for (int c = 0; c <= s.G; ++c)
-        s.range[c] = (int)(((unsigned long long)s.U * (unsigned long long)c) / (unsigned long long)s.G);
+        s.range[c] = (int)(((unsigned long long)s.U * (unsigned long long)(c < gt ? c : gt)) / (unsigned long long)gt);
 }
 
 // CTA whose range holds unit u (balanced schedule): the last c with
@@ -337,10 +350,10 @@ FA_HD int sched_cta_of_unit(const Schedule &s, int u)
 // Tile containing unit u (balanced schedule), with its first unit.
 FA_HD int sched_tile_of_unit(const Schedule &s, int u, int &tstart)
 {
-    if (!s.causal) {
+    if (!s.causal) {   // (tail split: the tail's tiles follow the WG whole ones)
         const int t = u / s.nkv;
         tstart = t * s.nkv;
-        return t;
+        return t + s.W * s.G;
     }
     // (balanced schedules only) pairs of tile rows, then the middle row of an odd C
     int acc = 0;
@@ -384,6 +397,7 @@ struct PartIter {
     int u, ue, tstart;   // balanced: next unit, end of the in-order units, first unit of tile t; round-robin: u = round
     int t, tsteps;
     int lt, lke, lts;    // balanced: the range's last part, tile lt (first unit lts) steps [0, lke), still to come (lt >= 0)
+    int wt, we;          // balanced: the whole tiles wt .. we - 1 still to come after the range (tail split)
 
     // The kernel knows its schedule at compile time (SPLIT = s.split) and
     // takes only that path; init / next decide at run time (host code).
@@ -394,7 +408,10 @@ struct PartIter {
         lt = -1;
         lke = 0;
         lts = 0;
+        wt = we = 0;
         if (SPLIT) {
+            wt = c * s.W;
+            we = wt + s.W;
             u = s.range[c];
             ue = s.range[c + 1];
             if (u < ue) {
@@ -431,8 +448,17 @@ struct PartIter {
                 lt = -1;
                 return true;
             }
-            if (u >= ue)
-                return false;
+            if (u >= ue) {
+                if (wt >= we)
+                    return false;
+                p.tile = wt;   // a whole tile of a tail split
+                p.kb = 0;
+                p.ke = sched_steps(s, wt);
+                p.slot = -1;
+                p.ts = 0;
+                ++wt;
+                return true;
+            }
             p.tile = t;
             p.kb = u - tstart;
             p.ke = (ue - tstart < tsteps) ? ue - tstart : tsteps;
@@ -522,20 +548,24 @@ FA_HD int sched_part_slots(const Schedule &s, int t, int nw, int *slots, int max
     return count;
 }
 
-// Work decomposition for one call on `sms` SMs (host side).  The balanced
-// schedule is taken when the round-robin schedule of whole tiles would leave
-// the machine idle in its last wave for more than ~4% of the run and for at
-// least kSchedMinGain steps (a split tile costs its parts a partial write and
-// one of them a merge); its grid is kept small enough that no tile is cut
-// into more than sched_max_parts parts.  Parts have fixed costs (a partial
-// write, a merge, a pipeline start), so with many tiles the balanced schedule
-// is taken only where every CTA's range spans at least two tiles, and not
-// for causal attention, whose short tiles lose to those costs (measured).
+// Work decomposition for one call on `sms` SMs (host side).  Without a mask
+// and with more tiles than SMs, the tail split is taken when the round-robin
+// schedule of whole tiles would leave the machine idle in its last wave for
+// more than ~4% of the run and for at least kSchedMinGain steps (a split tile
+// costs its parts a partial write and one of them a merge), and only where
+// those fixed costs are amortised: every CTA runs at least two whole tiles,
+// or the tiles are at least kSchedTailSteps long.  (Measured: B4 H16 N2048,
+// B2 H16 N4096 and B1 H8 N8192 at D = 64 gain 2, 1.4 and 10 %; B2 H8 N3000,
+// one whole tile of 24 steps per CTA, loses 10-15 %.)  The tail is spread
+// over few enough CTAs that no tile is cut into more than sched_max_parts
+// parts.  Causal attention keeps whole tiles: its short tiles lose to the
+// parts' fixed costs (measured).
 // With few long tiles -- decoding a few queries against many keys -- whole
 // tiles would leave most SMs idle, and the balanced schedule (split-KV) is
 // taken whenever it at least halves the makespan; for heads of at most 64
 // query rows, whose merges are cheap, whenever it saves more than 10 %.
 constexpr int kSchedMinGain = 4;
+constexpr int kSchedTailSteps = 64;
 
 // mode: 0 = as above, 1 = round-robin, 2 = balanced wherever it can be built.
 // N query rows against Nkv keys per head; `causal` here means masked by the
@@ -611,13 +641,30 @@ inline Schedule sched_plan(int N, int Nkv, int BH, bool causal, int sms, int mod
     if (G < 1)
         return s;
     const long long balanced = (s.U + G - 1) / G;
-    const bool many_tiles = !causal && balanced >= 2LL * max_steps && rr * 100 > balanced * 104 &&
-                            rr - balanced >= kSchedMinGain;
+    if (mode == 0 && !causal && s.T > s.G) {   // the tail split, or whole tiles
+        const int W = s.T / s.G, L = s.T - W * s.G;
+        if (L == 0 || (W < 2 && s.nkv < kSchedTailSteps))
+            return s;
+        const long long ut = (long long)L * s.nkv;
+        long long gt = s.G;
+        if (need > 0 && ut / gt < need)
+            gt = ut / need;
+        if (gt < 1)
+            return s;
+        const long long tail = (long long)W * s.nkv + (ut + gt - 1) / gt;
+        if (!(rr * 100 > tail * 104 && rr - tail >= kSchedMinGain))
+            return s;
+        s.split = 1;
+        s.W = W;
+        s.U = ut;
+        sched_fill_ranges(s, (int)gt);
+        return s;
+    }
     const bool few_long_tiles = 2LL * s.T <= sms && max_steps >= 32 && rr >= 2 * balanced;
     // decoding-sized heads (at most 64 query rows) merge cheaply: balance
     // whenever it shortens the makespan by more than 10 %
     const bool short_heads = N <= kSchedShortRows && rr * 100 > balanced * 110;
-    const bool pays = many_tiles || few_long_tiles || short_heads;
+    const bool pays = few_long_tiles || short_heads;
     if (mode == 2 || pays) {
         s.split = 1;
         s.G = (int)G;

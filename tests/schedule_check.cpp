@@ -18,17 +18,27 @@ static int check_schedule(const Schedule &s, bool planned, int wl, int wr);
 
 // A schedule of G CTAs, balanced or not, for the band (wl, wr) as given
 // (kSchedUnbounded: no bound); the planner supplies its mask fields.
-static int check(int N, int Nkv, int BH, int causal, int G, int split, int wl, int wr)
+// split = 2: the tail split (non-causal), every CTA first taking
+// floor(T / G) whole tiles, the rest spread over the first gt CTAs (all G
+// when gt <= 0).
+static int check(int N, int Nkv, int BH, int causal, int G, int split, int wl, int wr, int gt = 0)
 {
     if (G > kSchedMaxGrid)
         return 0;
     Schedule s = sched_plan(N, Nkv, BH, causal != 0, G, 1, wl, wr);
     s.G = G;
-    s.split = split;
+    s.split = split ? 1 : 0;
+    if (split == 2) {
+        if (causal || s.T <= G)
+            return 0;
+        s.W = s.T / G;
+        if (s.T == s.W * G)
+            return 0;
+    }
     s.U = sched_total_units(s);
     if (s.U > kSchedMaxUnits)
         return 0;
-    sched_fill_ranges(s);
+    sched_fill_ranges(s, gt);
     return check_schedule(s, false, wl, wr);
 }
 
@@ -142,6 +152,11 @@ static int check_schedule(const Schedule &s, bool planned, int wl, int wr)
     std::map<std::pair<int, int>, std::set<int>> slots_with_work;   // (tile, w) -> slots
     std::set<int> used_slots;
     long long units = 0;
+    const int tail0 = s.W * G;   // tail split: tiles before tail0 are whole tiles, W per CTA
+    if (s.W > 0 && (!split || s.causal)) {
+        std::printf("whole tiles before the units outside a non-causal balanced schedule\n");
+        return 1;
+    }
     for (int c = 0; c < G; ++c) {
         PartIter it;
         it.init(s, c);
@@ -152,6 +167,16 @@ static int check_schedule(const Schedule &s, bool planned, int wl, int wr)
             if (p.tile < 0 || p.tile >= s.T || p.kb < 0 || p.ke > (int)cover[p.tile].size() || p.kb >= p.ke) {
                 std::printf("bad part c=%d tile=%d kb=%d ke=%d\n", c, p.tile, p.kb, p.ke);
                 return 1;
+            }
+            if (split && p.tile < tail0) {   // a whole tile of the tail split: CTA c's own, kept whole
+                if (p.tile / s.W != c || p.kb != 0 || p.ke != (int)cover[p.tile].size() || p.slot != -1) {
+                    std::printf("c=%d: whole part of tile %d wrong (kb %d ke %d slot %d)\n", c, p.tile, p.kb, p.ke, p.slot);
+                    return 1;
+                }
+                for (int j = p.kb; j < p.ke; ++j)
+                    ++cover[p.tile][j];
+                units += p.ke - p.kb;
+                continue;
             }
             if (split && p.ts != (int)sched_prefix(s, p.tile)) {
                 std::printf("part of tile %d carries first unit %d, expected %lld\n", p.tile, p.ts, sched_prefix(s, p.tile));
@@ -207,12 +232,13 @@ static int check_schedule(const Schedule &s, bool planned, int wl, int wr)
                 std::printf("unit (%d,%zu) covered %d times\n", t, j, cover[t][j]);
                 return 1;
             }
-    if (units != s.U) {
-        std::printf("units %lld != U %lld\n", units, s.U);
+    const long long whole_units = split ? (long long)tail0 * s.nkv : 0;   // (non-causal: nkv units per tile)
+    if (units != s.U + whole_units) {
+        std::printf("units %lld != U %lld + %lld\n", units, s.U, whole_units);
         return 1;
     }
     if (split) {
-        for (int t = 0; t < s.T; ++t) {
+        for (int t = tail0; t < s.T; ++t) {
             int bh, ct;
             sched_decode(s, t, bh, ct);
             for (int w = 0; w < 2; ++w) {
@@ -264,6 +290,21 @@ static int check_limited(int N, int Nkv, int BH, int causal, int sms, int wl, in
 
 int main(int argc, char **argv)
 {
+    // "tail" then "N Nkv BH G gt" cases: tail splits of non-causal heads
+    if (argc > 1 && std::string(argv[1]) == "tail") {
+        int failures = 0, cases = 0;
+        for (int i = 2; i + 5 <= argc; i += 5) {
+            const int N = std::atoi(argv[i]), Nkv = std::atoi(argv[i + 1]), BH = std::atoi(argv[i + 2]);
+            const int G = std::atoi(argv[i + 3]), gt = std::atoi(argv[i + 4]);
+            ++cases;
+            if (check(N, Nkv, BH, 0, G, 2, kSchedUnbounded, kSchedUnbounded, gt)) {
+                std::printf("FAILED tail N=%d Nkv=%d BH=%d G=%d gt=%d\n", N, Nkv, BH, G, gt);
+                ++failures;
+            }
+        }
+        std::printf("%d cases, %d failures\n", cases, failures);
+        return failures ? 1 : 0;
+    }
     // "limit L" then "N Nkv BH causal sms wl wr D" cases: the no-allocation planner
     if (argc > 2 && std::string(argv[1]) == "limit") {
         const unsigned long long limit = std::strtoull(argv[2], nullptr, 10);

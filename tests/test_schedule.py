@@ -111,3 +111,23 @@ def test_no_alloc_planner_falls_back_to_whole_tiles(checker):
         assert f"{len(cases)} cases, 0 failures" in res.stdout, res.stdout
         fallbacks = int(res.stdout.split(",")[-1].split()[0])
         assert (fallbacks > 0) == expect_fallbacks, (limit, res.stdout)
+
+
+TAIL_CASES = []
+for N, Nkv in ((3000, 3000), (1024, 1024), (4096, 4096), (257, 257), (1, 4096), (300, 2000), (513, 129)):
+    for BH in (3, 16, 32, 64, 160):
+        for G in (7, 100, 152):
+            for gt in (0, 3, 50):
+                TAIL_CASES.append((N, Nkv, BH, G, gt))
+
+
+def test_tail_split_schedules(checker):
+    """The tail split (non-causal): every CTA takes its floor(T / G) whole
+    tiles, and the tiles of the last partial wave are spread as units over
+    the first gt CTAs; every unit is covered once, a CTA's partial parts come
+    before its whole tiles, and each split tile's merge expects exactly the
+    parts that hold work."""
+    args = ["tail"] + [str(x) for case in TAIL_CASES for x in case]
+    res = subprocess.run([checker, *args], capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stdout[-2000:]
+    assert f"{len(TAIL_CASES)} cases, 0 failures" in res.stdout, res.stdout[-500:]
