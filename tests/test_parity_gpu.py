@@ -156,6 +156,25 @@ def test_long_context_sampled_rows(name):
     assert float(o.float().abs().max()) <= float(v.float().abs().max()) * 1.01
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_tail_split_long_tiles(D):
+    """B1 H8 N8192 non-causal: 256 CTA tiles of 64 key steps on the GPU's
+    SMs, which the automatic schedule runs as a tail split (each CTA a whole
+    tile, the last wave's 104 tiles cut into parts and merged).  Heads 0 and
+    7 are compared in full, 512 rows of every other head."""
+    q, k, v = make_custom(1, 8, 8192, D, "bf16", seed=8192 + D)
+    scale = D ** -0.5
+    o, lse = _run(q, k, v, False, scale)
+    bh_idx, row_idx = _sample_rows(8, 8192, 512, seed=9, full_heads=(0, 7))
+    o_ref, lse_ref = oracle.rows(q, k, v, False, scale, bh_idx, row_idx)
+    of = o.reshape(8, 8192, D).double().numpy()[bh_idx, row_idx]
+    lf = lse.reshape(8, 8192).double().numpy()[bh_idx, row_idx]
+    emax = float(np.abs(of - o_ref).max())
+    lmax = float(np.abs(lf - lse_ref).max())
+    print(f"tail split D{D}: {len(bh_idx)} rows, max|dO|={emax:.3e} max|dLSE|={lmax:.3e}")
+    assert emax <= TOL_O["bf16"] and lmax <= TOL_LSE
+
+
 EDGE_N = [1, 2, 3, 64, 127, 128, 129, 255, 256, 257, 383, 384, 513]
 
 
