@@ -114,6 +114,24 @@ bool encode_map(CUtensorMap *m, const void *ptr, int BH, int N, int D, bool bf16
     return r == CUDA_SUCCESS;
 }
 
+// Rank-2 map over an fp32 [rows, D] array (the backward's dQ accumulator),
+// 32 columns (128 bytes) x 128 rows per box, 128-byte swizzle: the fused
+// backward pass adds its staged dQ products into it box by box.
+bool encode_map_f32(CUtensorMap *m, float *ptr, long long rows, int D)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Per-(device, stream) workspace for split tiles: partial O and (m, l) for
 // two slots per CTA, and one counter per (tile, Q tile) that must be zero
 // when a launch starts (each launch leaves it zero).  Allocated on the first
@@ -383,8 +401,10 @@ namespace {
 // unbounded; causal = (-1, 0), no mask = (-1, -1)).
 fa_status bwd_impl(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
                    void *dQ, void *dK, void *dV, int B, int H, int N, int Nkv, int D, int left, int right, float scale,
-                   fa_dtype dtype, fa_stream_t stream)
+                   fa_dtype dtype, unsigned int flags, fa_stream_t stream)
 {
+    if (flags & ~FA_BWD_DETERMINISTIC)
+        return FA_ERR_INVALID_VALUE;
     int wl = left, wr = right;   // bounds that cannot bind are dropped: a band of no bounds runs unmasked
     if (N >= 1 && Nkv >= 1)
         fa::sched_band_normalize(N, Nkv, wl, wr);
@@ -446,9 +466,19 @@ fa_status bwd_impl(const void *Q, const void *K, const void *V, const void *O, c
         !encode_map(&a.tv, V, (int)BH, Nkv, D, bf16) || !encode_map(&a.tdo, dO, (int)BH, N, D, bf16))
         return FA_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    float *ws = static_cast<float *>(bwd_workspace(dev, s, (size_t)2 * BH * Npad * sizeof(float)));
+    // D = 64 without FA_BWD_DETERMINISTIC: the fused pass, with an fp32 dQ
+    // accumulator [B*H*Npad, D] after delta and lg (1024-byte aligned: Npad % 128 == 0)
+    const bool fused = D == 64 && !(flags & FA_BWD_DETERMINISTIC);
+    float *ws = static_cast<float *>(
+        bwd_workspace(dev, s, (size_t)(2 + (fused ? D : 0)) * BH * Npad * sizeof(float)));
     if (!ws)
         return FA_ERR_CUDA;
+    a.fused = fused;
+    if (fused) {
+        a.dqa = ws + 2 * BH * Npad;
+        if (!encode_map_f32(&a.tdqa, a.dqa, BH * Npad, D))
+            return FA_ERR_CUDA;
+    }
     a.O = O;
     a.dO = dO;
     a.LSE = LSE;
@@ -479,14 +509,23 @@ extern "C" fa_status fa_bwd(const void *Q, const void *K, const void *V, const v
 {
     if (causal != 0 && causal != 1)
         return FA_ERR_INVALID_VALUE;
-    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, N, D, -1, causal ? 0 : -1, scale, dtype, stream);
+    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, N, D, -1, causal ? 0 : -1, scale, dtype, 0u, stream);
 }
 
 extern "C" fa_status fa_bwd_band(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                                  const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nkv, int D,
                                  int window_left, int window_right, float scale, fa_dtype dtype, fa_stream_t stream)
 {
-    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nkv, D, window_left, window_right, scale, dtype,
+    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nkv, D, window_left, window_right, scale, dtype, 0u,
+                    stream);
+}
+
+extern "C" fa_status fa_bwd_ex(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                               const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nkv, int D,
+                               int window_left, int window_right, float scale, fa_dtype dtype, unsigned int flags,
+                               fa_stream_t stream)
+{
+    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nkv, D, window_left, window_right, scale, dtype, flags,
                     stream);
 }
 

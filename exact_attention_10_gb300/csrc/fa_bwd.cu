@@ -1,5 +1,6 @@
 // fa_bwd.cu -- the backward kernels (fa_bwd_kernel.cuh) and their launch:
-// the per-row pre-pass, then the dQ pass and the dK/dV pass on one stream.
+// the per-row pre-pass, then the dQ pass and the dK/dV pass, or at D = 64 the
+// fused pass and the dQ conversion, on one stream.
 #include "fa_bwd_launch.h"
 
 #include <mutex>
@@ -12,14 +13,14 @@ namespace {
 
 constexpr int kMaxDev = 64;
 
-template <int D, bool BF16, bool CAUSAL, bool KV>
+template <int D, bool BF16, bool CAUSAL, bool KV, bool FQ = false>
 fa_status launch_pass(const CUtensorMap &r0, const CUtensorMap &r1, const CUtensorMap &s0, const CUtensorMap &s1,
-                      const fa::bwd::Params &p, int grid, cudaStream_t stream, int dev)
+                      const CUtensorMap &dq, const fa::bwd::Params &p, int grid, cudaStream_t stream, int dev)
 {
     static std::mutex mu;
     static bool attr_set[kMaxDev] = {};
-    auto kern = fa::bwd::fa_bwd_sm103<D, BF16, CAUSAL, KV>;
-    constexpr int smem = fa::bwd::BCfg<D, KV>::kSmem;
+    auto kern = fa::bwd::fa_bwd_sm103<D, BF16, CAUSAL, KV, FQ>;
+    constexpr int smem = fa::bwd::BCfg<D, KV, FQ>::kSmem;
     if (dev < 0 || dev >= kMaxDev)
         return FA_ERR_UNSUPPORTED_DEVICE;
     {
@@ -32,7 +33,7 @@ fa_status launch_pass(const CUtensorMap &r0, const CUtensorMap &r1, const CUtens
             attr_set[dev] = true;
         }
     }
-    kern<<<grid, fa::bwd::kThreads, smem, stream>>>(r0, r1, s0, s1, p);
+    kern<<<grid, FQ ? fa::bwd::kThreadsFused : fa::bwd::kThreads, smem, stream>>>(r0, r1, s0, s1, dq, p);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
     return FA_OK;
@@ -43,8 +44,10 @@ fa_status launch_all(const BwdLaunch &a, cudaStream_t s, int dev)
 {
     const long long rows = (long long)a.BH * a.Npad;
     const long long threads = rows * (D / 8);
+    const bool fused = (D == 64) && a.fused;
     fa::bwd::fa_bwd_prep<D, BF16><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
-        static_cast<const uint16_t *>(a.O), static_cast<const uint16_t *>(a.dO), a.LSE, a.lg, a.dl, a.N, a.Npad, rows);
+        static_cast<const uint16_t *>(a.O), static_cast<const uint16_t *>(a.dO), a.LSE, a.lg, a.dl,
+        fused ? a.dqa : nullptr, a.N, a.Npad, rows);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
     fa::bwd::Params p{};
@@ -62,18 +65,34 @@ fa_status launch_all(const BwdLaunch &a, cudaStream_t s, int dev)
     p.square_causal = (a.N == a.Nkv && a.wl >= fa::kSchedUnbounded && a.wr == 0) ? 1 : 0;
     p.qk2 = a.scale * 1.4426950408889634f;
     p.scale = a.scale;
+    int grid;
+    if constexpr (D == 64) {
+        if (fused) {   // dK, dV and the dQ accumulator in one pass, then dQ from the accumulator
+            p.T = a.BH * p.nkt;
+            grid = p.T < a.sms ? p.T : a.sms;
+            p.dA = a.dK;
+            p.dB = a.dV;
+            const fa_status st = launch_pass<D, BF16, CAUSAL, true, true>(a.tk, a.tv, a.tq, a.tdo, a.tdqa, p, grid, s, dev);
+            if (st != FA_OK)
+                return st;
+            const long long elems = (long long)a.BH * a.N * D;
+            fa::bwd::fa_bwd_dq_convert<BF16><<<(unsigned)((elems / 8 + 255) / 256), 256, 0, s>>>(
+                a.dqa, static_cast<uint16_t *>(a.dQ), a.N, a.Npad, D, elems, a.scale);
+            return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+        }
+    }
     p.T = a.BH * p.nqt;
-    int grid = p.T < a.sms ? p.T : a.sms;
+    grid = p.T < a.sms ? p.T : a.sms;
     p.dA = a.dQ;
     p.dB = nullptr;
-    fa_status st = launch_pass<D, BF16, CAUSAL, false>(a.tq, a.tdo, a.tk, a.tv, p, grid, s, dev);
+    fa_status st = launch_pass<D, BF16, CAUSAL, false>(a.tq, a.tdo, a.tk, a.tv, a.tq, p, grid, s, dev);
     if (st != FA_OK)
         return st;
     p.T = a.BH * p.nkt;
     grid = p.T < a.sms ? p.T : a.sms;
     p.dA = a.dK;
     p.dB = a.dV;
-    return launch_pass<D, BF16, CAUSAL, true>(a.tk, a.tv, a.tq, a.tdo, p, grid, s, dev);
+    return launch_pass<D, BF16, CAUSAL, true>(a.tk, a.tv, a.tq, a.tdo, a.tq, p, grid, s, dev);
 }
 
 }  // namespace

@@ -68,11 +68,21 @@ constexpr int kTile = 128;   // rows of a resident or streamed tile (keys or que
 // the 384 x 168 = 64512 the block is launched with.
 constexpr uint32_t kRegsCompute = 200;
 constexpr uint32_t kRegsProducer = 96;
+// The fused pass (dK, dV and dQ in one pass, D = 64): 512 threads.  Warp 10
+// issues the dQ products, warps 12-15 read them out of TMEM and add them into
+// an fp32 dQ accumulator in global memory.  2 x 128 x 192 + 2 x 128 x 64 =
+// 65536 registers, the 512 x 128 the block is launched with.
+constexpr int kThreadsFused = 512;
+constexpr int kMmaWarpDq = 10;
+constexpr int kDqWarp0 = 12;
+constexpr uint32_t kRegsComputeFused = 192;
+constexpr uint32_t kRegsOtherFused = 64;
 
 // Wait sites (status word), after the forward's.
 enum : uint32_t {
     kSiteBwdResEmpty = 32, kSiteBwdSlotEmpty, kSiteBwdResFull, kSiteBwdSlotFull, kSiteBwdPFull, kSiteBwdAccFree,
-    kSiteBwdSdFull, kSiteBwdAccFull, kSiteBwdDrain, kSiteBwdTail, kSiteBwdSdFree, kSiteBwdPdFree
+    kSiteBwdSdFull, kSiteBwdAccFull, kSiteBwdDrain, kSiteBwdTail, kSiteBwdSdFree, kSiteBwdPdFree, kSiteBwdDqFull,
+    kSiteBwdDqFree
 };
 
 struct Params {
@@ -94,9 +104,11 @@ struct Params {
     float scale;
 };
 
-template <int D, bool KV>
+// FQ: the fused pass (KV, D = 64 only): dQ products beside dK and dV.
+template <int D, bool KV, bool FQ = false>
 struct BCfg {
     static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+    static_assert(!FQ || (KV && D == 64), "the fused pass is the dK/dV pass at D = 64");
     static constexpr int kBoxes = D / 64;
     static constexpr int kBoxBytes = kTile * 128;     // [128 rows, 64 columns] of 16-bit
     static constexpr int kTileBytes = kTile * D * 2;
@@ -114,11 +126,18 @@ struct BCfg {
     static constexpr int kRing0 = kSplitRing ? 3 : kStages;   // slots of streamed tile 0 (KV: Q; dQ pass: K)
     static constexpr int kRing1 = kSplitRing ? 2 : kStages;   // slots of streamed tile 1 (KV: dO; dQ pass: V)
     static constexpr int kRing1Off = kStageOff + kRing0 * kTileBytes;   // split rings: tile 1's ring
-    static constexpr int kBarOff = kSplitRing ? kRing1Off + kRing1 * kTileBytes : kStageOff + kStages * kStageBytes;
+    // The fused pass: dS^T as an MMA operand, 16-bit [128 keys][128 queries]
+    // in two 64-column boxes (K-major for dK += dS^T Q, MN-major as dS for
+    // dQ = dS K); then the fp32 dQ product of a step, [128 queries][64] in two
+    // 32-column boxes, staged for the reduction into the accumulator.
+    static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kDqOff = kDsOff + (FQ ? kTile * kTile * 2 : 0);
+    static constexpr int kDqBoxBytes = kTile * 128;   // [128 rows, 32 fp32 columns]
+    static constexpr int kBarOff = kSplitRing ? kRing1Off + kRing1 * kTileBytes : kDqOff + (FQ ? kTile * D * 4 : 0);
     // full/empty per slot (unified stages, or ring 0 then ring 1), then res_full, res_empty,
-    // sd_full, p_full, acc_full, acc_free, drain, sd_free, pd_free, p_full_odd
+    // sd_full, p_full, acc_full, acc_free, drain, sd_free, pd_free, p_full_odd; fused: dq_full, dq_free
     static constexpr int kRingBars = kSplitRing ? 2 * (kRing0 + kRing1) : 2 * kStages;
-    static constexpr int kNumBars = kRingBars + 10;
+    static constexpr int kNumBars = kRingBars + 10 + (FQ ? 2 : 0);
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;           // TMEM address, abort flag
     static constexpr int kSmem = kMiscOff + 16 + 1024;                // + slack to align the base to 1024
     static_assert(kSmem <= 232448, "shared memory per CTA");
@@ -129,6 +148,7 @@ struct BCfg {
     // in buffer g % 2); KV pass (D = 64): one P^T and one dS^T buffer after dV, dK.
     static constexpr uint32_t kColDS = KV ? 256 + 2 * D + 64 : 256 + D;
     static constexpr uint32_t kColP = 256 + 2 * D;
+    static constexpr uint32_t kColDQ = 256 + 2 * D + 64;   // fused: the step's dQ product, where dS^T sits otherwise
     static_assert((KV && D == 128) || (KV ? kColDS + 64 : kColDS + 128) <= kTmemCols, "pipelined buffers fit TMEM");
     // Shared-memory address of streamed tile 0 / 1 of global step g.
     __device__ static uint32_t slot0(uint32_t sStage, int g)
@@ -142,10 +162,10 @@ struct BCfg {
     }
 };
 
-template <int D, bool KV>
+template <int D, bool KV, bool FQ = false>
 struct BBars {
     uint32_t base;
-    using C = BCfg<D, KV>;
+    using C = BCfg<D, KV, FQ>;
     __device__ uint32_t full(int s) const { return base + 8u * s; }                    // slot s of ring 0 / stage s
     __device__ uint32_t empty(int s) const { return base + 8u * (C::kRing0 + s); }
     __device__ uint32_t full1(int s) const { return C::kSplitRing ? base + 8u * (2 * C::kRing0 + s) : full(s); }
@@ -168,6 +188,8 @@ struct BBars {
     // waited for step g (nothing else holds them back), and one barrier two
     // phases ahead of its waiter would read as not yet complete.
     __device__ uint32_t p_full_dq(int g) const { return (g & 1) ? at(9) : at(3); }
+    __device__ uint32_t dq_full() const { return at(10); }    // fused: dQ MMA -> read-out warps: the step's dQ product done
+    __device__ uint32_t dq_free() const { return at(11); }    // fused: read-out warps -> dQ MMA: dQ product loaded
 };
 
 // Streamed tiles of resident tile rt under a band mask, [s0, s0 + n): the
@@ -302,12 +324,12 @@ __device__ __forceinline__ uint32_t a_col(int kk)
 
 // ------------------------------------------------------------------ producer
 
-template <int D, bool KV>
+template <int D, bool KV, bool FQ>
 __device__ void bwd_load(const CUtensorMap *tmR0, const CUtensorMap *tmR1, const CUtensorMap *tmS0,
                          const CUtensorMap *tmS1, const Params &p, bool causal, uint32_t sRes, uint32_t sStage,
-                         BBars<D, KV> b, Ctl c)
+                         BBars<D, KV, FQ> b, Ctl c)
 {
-    using C = BCfg<D, KV>;
+    using C = BCfg<D, KV, FQ>;
     int step = 0, tiles = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
@@ -664,11 +686,15 @@ constexpr bool kPipeline = (D == 64) || (!KV && D == 128);
 // sd_full of step g, whose commit follows the MMA that read the buffer at
 // step g - 2, so no extra barrier guards it.  Tensor-pipe order per step:
 // S_{g+1}, dP_{g+1}, dQ_g.
-template <int D, bool BF16, bool KV>
-__device__ void bwd_mma_pipe(const Params &p, bool causal, uint32_t sRes, uint32_t sStage, uint32_t tmem,
-                             BBars<D, KV> b, Ctl c)
+//
+// The fused pass (FQ) takes dS^T from shared memory for dK += dS^T Q (warp
+// 10 reads the same tile as dS for the dQ products, bwd_mma_dq), and its
+// pd_free, res_empty and drain barriers also count warp 10's commits.
+template <int D, bool BF16, bool KV, bool FQ>
+__device__ void bwd_mma_pipe(const Params &p, bool causal, uint32_t sRes, uint32_t sStage, uint32_t sDs, uint32_t tmem,
+                             BBars<D, KV, FQ> b, Ctl c)
 {
-    using C = BCfg<D, KV>;
+    using C = BCfg<D, KV, FQ>;
     constexpr uint32_t kIdescSS = instr_desc_f16(BF16, kTile, kTile, false);
     constexpr uint32_t kIdescTS = instr_desc_f16(BF16, kTile, D, true);
     const uint32_t r0_lo = desc_lo(sRes, 16), r1_lo = desc_lo(sRes + C::kTileBytes, 16);
@@ -749,7 +775,14 @@ __device__ void bwd_mma_pipe(const Params &p, bool causal, uint32_t sRes, uint32
                 for (int kk = 0; kk < kTile / 16; ++kk)
                     ptx::mma_ts(tAcc0, tA0 + 8 * kk, desc_from_lo(m0_lo + kk * (2048 >> 4)), kIdescTS,
                                 (j > 0 || kk > 0) ? 1u : 0u);
-                if (KV) {
+                if (KV && FQ) {   // dS^T K-major in shared memory: 32 bytes per k-step, a box per 64 queries
+                    const uint32_t ds_lo = desc_lo(sDs, 16);
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        ptx::mma_ss(tAcc1, desc_from_lo(ds_lo + (uint32_t)((kk / 4) * (C::kBoxBytes >> 4) + (kk % 4) * 2)),
+                                    desc_from_lo(m1_lo + kk * (2048 >> 4)), kIdescTS, (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(b.pd_free());
+                } else if (KV) {
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
                         ptx::mma_ts(tAcc1, tA1 + 8 * kk, desc_from_lo(m1_lo + kk * (2048 >> 4)), kIdescTS,
@@ -772,10 +805,12 @@ __device__ void bwd_mma_pipe(const Params &p, bool causal, uint32_t sRes, uint32
     wait_landed(b.drain(), 0u, c, kSiteBwdDrain);
 }
 
-template <int D, bool BF16, bool CAUSAL, bool KV>
-__device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage, BBars<D, KV> b, Ctl c)
+// FQ: dS^T goes to the shared-memory tile at sDs instead of TMEM.
+template <int D, bool BF16, bool CAUSAL, bool KV, bool FQ>
+__device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage, uint32_t sDs, BBars<D, KV, FQ> b,
+                                 Ctl c)
 {
-    using C = BCfg<D, KV>;
+    using C = BCfg<D, KV, FQ>;
     const int h = threadIdx.x / 128;                            // column half of S and dP
     const int warp = threadIdx.x / 32;
     const int row = (warp % 4) * 32 + threadIdx.x % 32;         // TMEM lane = row of the resident tile
@@ -870,7 +905,16 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
             for (int i = 0; i < 32; ++i)
                 pk[i] = BF16 ? ptx::pack_bf16x2(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]))
                              : ptx::pack_f16x2(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]));
-            ptx::tmem_st32(tmem + C::kColDS + (KV ? 0u : 64u * (uint32_t)(g & 1)) + lane_off + 32 * h, pk);
+            if (FQ) {   // key row `row`, queries [64h, 64h + 64): one 128-byte swizzled row of box h
+                const uint32_t rb = sDs + (uint32_t)(h * C::kBoxBytes + row * 128);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    ptx::st_shared_v4(rb + (uint32_t)((ch ^ (row & 7)) << 4), pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
+                                      pk[4 * ch + 3]);
+                ptx::fence_proxy_async_smem();   // visible to the tensor core's reads
+            } else {
+                ptx::tmem_st32(tmem + C::kColDS + (KV ? 0u : 64u * (uint32_t)(g & 1)) + lane_off + 32 * h, pk);
+            }
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(KV ? b.p_full() : b.p_full_dq(g));
@@ -910,24 +954,162 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
     }
 }
 
+// ------------------------------------------------------------------ fused pass: dQ
+
+// The fused pass's dQ products (warp 10): per step g, once the compute warps
+// have written dS^T_g (p_full) and the read-out warps have loaded the
+// previous product (dq_free), dQ_g = dS_g K into the dQ columns -- A is the
+// dS^T tile read MN-major (dS: M = 128 queries, contiguous, a box per 64; K =
+// 128 keys, 16 rows = 2 KB per k-step), B the resident K tile read MN-major
+// as in dV += P^T dO.  Its commits: dq_full (the product is final), pd_free
+// (the dS^T tile was read; that barrier also counts warp 9's commit of dV and
+// dK), res_empty after a tile's last step (K was read), and drain.
+template <int D, bool BF16, bool CAUSAL>
+__device__ void bwd_mma_dq(const Params &p, uint32_t sRes, uint32_t sDs, uint32_t tmem, BBars<D, true, true> b, Ctl c)
+{
+    using C = BCfg<D, true, true>;
+    constexpr uint32_t kIdesc = instr_desc_f16(BF16, kTile, D, true, true);   // A and B MN-major
+    const uint32_t a_lo = desc_lo(sDs, C::kBoxBytes), k_lo = desc_lo(sRes, C::kBoxBytes);
+    const uint32_t tDQ = tmem + C::kColDQ;
+    int g = 0, tiles = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int t = bwd_tile(r, blockIdx.x, gridDim.x);
+        if (t >= p.T)
+            break;
+        int bh, rt, s0, n;
+        bwd_decode<true>(p, CAUSAL, t, bh, rt, s0, n);
+        if (!warp_wait(b.res_full(), (uint32_t)tiles & 1u, c, kSiteBwdResFull))
+            break;
+        for (int j = 0; j < n; ++j, ++g) {
+            if (!warp_wait(b.p_full(), (uint32_t)g & 1u, c, kSiteBwdPFull) ||
+                (g > 0 && !warp_wait(b.dq_free(), (uint32_t)(g - 1) & 1u, c, kSiteBwdDqFree))) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    ptx::mma_ss(tDQ, desc_from_lo(a_lo + kk * (2048 >> 4)), desc_from_lo(k_lo + kk * (2048 >> 4)), kIdesc,
+                                kk > 0 ? 1u : 0u);
+                ptx::mma_commit(b.dq_full());
+                ptx::mma_commit(b.pd_free());
+                if (j == n - 1)
+                    ptx::mma_commit(b.res_empty());
+            }
+            __syncwarp();
+        }
+        ++tiles;
+    }
+    if (ptx::elect_one())
+        ptx::mma_commit(b.drain());
+    __syncwarp();
+    wait_landed(b.drain(), 0u, c, kSiteBwdDrain);
+}
+
+// Read-out warps (12-15) sync among themselves (named barrier 3) and agree
+// (named barrier 4, true iff `ok` held in every thread).
+__device__ __forceinline__ void dq_sync()
+{
+    asm volatile("bar.sync 3, 128;" ::: "memory");
+}
+
+__device__ __forceinline__ bool dq_all(bool ok)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 4, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
+}
+
+// The fused pass's read-out (warps 12-15, a thread per query row of the
+// streamed tile): per step, the dQ product's row from TMEM into the fp32
+// staging tile (two 32-column boxes, 128-byte swizzle), released to the next
+// product (dq_free), then one thread adds the tile into the accumulator rows
+// of the step's query tile with two tensor reductions (fp32 add in L2).  The
+// staging is rewritten only after the previous reductions have read it.
+template <int D, bool CAUSAL>
+__device__ void bwd_dq_out(const CUtensorMap *tmDQ, const Params &p, uint32_t tmem, uint32_t sDq,
+                           BBars<D, true, true> b, Ctl c)
+{
+    using C = BCfg<D, true, true>;
+    static_assert(D == 64, "two 32-column boxes");
+    const int warp = threadIdx.x / 32;
+    const int q = (warp % 4) * 32 + threadIdx.x % 32;   // TMEM lane = query row of the streamed tile
+    const uint32_t tq = tmem + C::kColDQ + ((uint32_t)((warp % 4) * 32) << 16);
+    const bool leader = threadIdx.x == kDqWarp0 * 32;
+    bool pending = false;   // leader: reductions issued whose reads of the staging may still run
+    int g = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int t = bwd_tile(r, blockIdx.x, gridDim.x);
+        if (t >= p.T)
+            break;
+        int bh, rt, s0, n;
+        bwd_decode<true>(p, CAUSAL, t, bh, rt, s0, n);
+        for (int j = 0; j < n; ++j, ++g) {
+            if (!dq_all(wait_bounded(b.dq_full(), (uint32_t)g & 1u, c, kSiteBwdDqFull))) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            if (leader && pending)
+                ptx::bulk_wait_group_read0();
+            dq_sync();   // the staging is free
+#pragma unroll
+            for (int cc = 0; cc < D / 16; ++cc) {   // 16 columns at a time: 4 chunks of box cc / 2
+                uint32_t v[16];
+                ptx::tmem_ld16(tq + 16 * cc, v);
+                ptx::tmem_wait_ld();
+                const uint32_t rowb = sDq + (uint32_t)((cc / 2) * C::kDqBoxBytes + q * 128);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int ch = (cc % 2) * 4 + u;
+                    ptx::st_shared_v4(rowb + (uint32_t)((ch ^ (q & 7)) << 4), v[4 * u], v[4 * u + 1], v[4 * u + 2],
+                                      v[4 * u + 3]);
+                }
+            }
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(b.dq_free());
+            ptx::fence_proxy_async_smem();   // the staging, visible to the reductions
+            dq_sync();
+            if (leader) {
+                const int y = bh * p.Npad + (s0 + j) * kTile;
+                ptx::tma_reduce_add_2d(tmDQ, sDq, 0, y);
+                ptx::tma_reduce_add_2d(tmDQ, sDq + C::kDqBoxBytes, 32, y);
+                ptx::bulk_commit_group();
+                pending = true;
+            }
+        }
+    }
+    if (leader && pending)
+        ptx::bulk_wait_group0();   // the reductions are done with the staging (and complete) before exit
+}
+
 // ------------------------------------------------------------------ kernels
 
 // KV = true:  tmR0 = K, tmR1 = V (resident), tmS0 = Q, tmS1 = dO (streamed)
 // KV = false: tmR0 = Q, tmR1 = dO (resident), tmS0 = K, tmS1 = V (streamed)
-template <int D, bool BF16, bool CAUSAL, bool KV>
-__global__ void __launch_bounds__(kThreads, 1)
+// FQ (fused, KV at D = 64): tmDQ = the fp32 dQ accumulator [B*H*Npad, D] (32 x 128 boxes); otherwise unused.
+template <int D, bool BF16, bool CAUSAL, bool KV, bool FQ = false>
+__global__ void __launch_bounds__(FQ ? kThreadsFused : kThreads, 1)
     fa_bwd_sm103(const __grid_constant__ CUtensorMap tmR0, const __grid_constant__ CUtensorMap tmR1,
                  const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
-                 const __grid_constant__ Params p)
+                 const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ Params p)
 {
-    using C = BCfg<D, KV>;
+    using C = BCfg<D, KV, FQ>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;   // 128-byte swizzle atoms need 1024-byte alignment
     uint8_t *base_ptr = smem_raw + (base - raw);
     const uint32_t sRes = base + C::kResOff;
     const uint32_t sStage = base + C::kStageOff;
-    BBars<D, KV> b{base + C::kBarOff};
+    const uint32_t sDs = base + C::kDsOff, sDq = base + C::kDqOff;
+    BBars<D, KV, FQ> b{base + C::kBarOff};
     uint32_t *misc = reinterpret_cast<uint32_t *>(base_ptr + C::kMiscOff);
     Ctl c{reinterpret_cast<volatile int *>(misc + 1)};
     const int warp = threadIdx.x / 32;
@@ -942,16 +1124,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(b.full1(s), 1);
             ptx::mbar_init(b.empty1(s), 1);
         }
+        // the fused pass's two MMA warps both commit res_empty, drain and pd_free
         ptx::mbar_init(b.res_full(), 1);
-        ptx::mbar_init(b.res_empty(), 1);
+        ptx::mbar_init(b.res_empty(), FQ ? 2 : 1);
         ptx::mbar_init(b.sd_full(), 1);
         ptx::mbar_init(b.p_full(), kComputeThreads);
         ptx::mbar_init(b.acc_full(), 1);
         ptx::mbar_init(b.acc_free(), kComputeThreads);
-        ptx::mbar_init(b.drain(), 1);
+        ptx::mbar_init(b.drain(), FQ ? 2 : 1);
         ptx::mbar_init(b.sd_free(), kComputeThreads);
-        ptx::mbar_init(b.pd_free(), 1);
+        ptx::mbar_init(b.pd_free(), FQ ? 2 : 1);
         ptx::mbar_init(b.p_full_dq(1), kComputeThreads);
+        if (FQ) {
+            ptx::mbar_init(b.dq_full(), 1);
+            ptx::mbar_init(b.dq_free(), 128);
+        }
         *c.abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -964,6 +1151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmR1);
         ptx::prefetch_tensormap(&tmS0);
         ptx::prefetch_tensormap(&tmS1);
+        if (FQ)
+            ptx::prefetch_tensormap(&tmDQ);
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -971,21 +1160,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc);
 
     if (threadIdx.x < kComputeThreads) {
-        ptx::regs_increase<kRegsCompute>();
+        ptx::regs_increase<FQ ? kRegsComputeFused : kRegsCompute>();
         if constexpr (kPipeline<D, KV>)
-            bwd_compute_pipe<D, BF16, CAUSAL, KV>(p, tmem, sStage, b, c);
+            bwd_compute_pipe<D, BF16, CAUSAL, KV, FQ>(p, tmem, sStage, sDs, b, c);
         else
             bwd_compute<D, BF16, CAUSAL, KV>(p, tmem, sStage, b, c);
+    } else if (FQ && warp >= kDqWarp0) {
+        ptx::regs_decrease<kRegsOtherFused>();
+        if constexpr (FQ)
+            bwd_dq_out<D, CAUSAL>(&tmDQ, p, tmem, sDq, b, c);
     } else {
-        ptx::regs_decrease<kRegsProducer>();
+        ptx::regs_decrease<FQ ? kRegsOtherFused : kRegsProducer>();
         if (warp == kLoadWarp)
-            bwd_load<D, KV>(&tmR0, &tmR1, &tmS0, &tmS1, p, CAUSAL, sRes, sStage, b, c);
+            bwd_load<D, KV, FQ>(&tmR0, &tmR1, &tmS0, &tmS1, p, CAUSAL, sRes, sStage, b, c);
         else if (warp == kMmaWarp)
         {
             if constexpr (kPipeline<D, KV>)
-                bwd_mma_pipe<D, BF16, KV>(p, CAUSAL, sRes, sStage, tmem, b, c);
+                bwd_mma_pipe<D, BF16, KV, FQ>(p, CAUSAL, sRes, sStage, sDs, tmem, b, c);
             else
                 bwd_mma<D, BF16, KV>(p, CAUSAL, sRes, sStage, tmem, b, c);
+        }
+        else if (FQ && warp == kMmaWarpDq)
+        {
+            if constexpr (FQ)
+                bwd_mma_dq<D, BF16, CAUSAL>(p, sRes, sDs, tmem, b, c);
         }
     }
 
@@ -998,11 +1196,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // delta = rowsum(dO o O) and lg = LSE * log2(e) per query row, padded to
-// whole 128-row tiles: D / 8 threads per row, 16 bytes each.
+// whole 128-row tiles: D / 8 threads per row, 16 bytes each.  dqa (the fused
+// pass's fp32 dQ accumulator, [rows][D], or null): zeroed, 8 values a thread.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
-    fa_bwd_prep(const uint16_t *O, const uint16_t *dO, const float *LSE, float *lg, float *dl, int N, int Npad,
-                long long rows)
+    fa_bwd_prep(const uint16_t *O, const uint16_t *dO, const float *LSE, float *lg, float *dl, float *dqa, int N,
+                int Npad, long long rows)
 {
     constexpr int kTpr = D / 8;   // threads per row: 8 or 16, a divisor of 32
     const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1012,6 +1211,11 @@ __global__ void __launch_bounds__(256)
         return;
     const long long bh = row / Npad;
     const int i = (int)(row - bh * Npad);
+    if (dqa) {
+        float4 *z = reinterpret_cast<float4 *>(dqa + row * D + 8 * part);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float acc = 0.f;
     if (i < N) {
         const size_t e = ((size_t)bh * N + i) * D + 8 * part;
@@ -1050,6 +1254,29 @@ __global__ void __launch_bounds__(256)
         lg[row] = l;
         dl[row] = (i < N) ? acc : 0.f;
     }
+}
+
+// The fused pass's dQ: dQ = scale * the fp32 accumulator, in the input type,
+// for the N real rows of each head (8 values a thread).
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+    fa_bwd_dq_convert(const float *dqa, uint16_t *dQ, int N, int Npad, int D, long long elems, float scale)
+{
+    const long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+    if (e >= elems)
+        return;
+    const long long row = e / D;   // of [B*H*N]; D is a multiple of 8
+    const int col = (int)(e - row * D);
+    const long long bh = row / N;
+    const long long src = (bh * Npad + (row - bh * N)) * D + col;
+    const float4 a = *reinterpret_cast<const float4 *>(dqa + src);
+    const float4 b = *reinterpret_cast<const float4 *>(dqa + src + 4);
+    uint4 o;
+    o.x = BF16 ? ptx::pack_bf16x2(a.x * scale, a.y * scale) : ptx::pack_f16x2(a.x * scale, a.y * scale);
+    o.y = BF16 ? ptx::pack_bf16x2(a.z * scale, a.w * scale) : ptx::pack_f16x2(a.z * scale, a.w * scale);
+    o.z = BF16 ? ptx::pack_bf16x2(b.x * scale, b.y * scale) : ptx::pack_f16x2(b.x * scale, b.y * scale);
+    o.w = BF16 ? ptx::pack_bf16x2(b.z * scale, b.w * scale) : ptx::pack_f16x2(b.z * scale, b.w * scale);
+    *reinterpret_cast<uint4 *>(dQ + e) = o;
 }
 
 }  // namespace bwd

@@ -15,13 +15,17 @@ struct BwdLaunch {
     const float *LSE;              // [B*H, N]
     void *dQ, *dK, *dV;            // dQ [B*H, N, D], dK and dV [B*H, Nkv, D], the input type
     float *lg, *dl;                // workspace: [B*H][Npad] each
+    float *dqa;                    // fused: workspace, the fp32 dQ accumulator [B*H][Npad][D]
+    CUtensorMap tdqa;              // fused: rank-2 map over dqa [B*H*Npad, D], 32 x 128 boxes, 128-byte swizzle
+    bool fused;                    // D = 64: one pass for dK, dV and dQ (dQ through dqa)
     int BH, N, Nkv, Npad, D, sms;   // N query rows, Nkv keys per head
     bool bf16, causal;               // causal: masked by the band below
     int wl, wr;                      // band: query i sees keys [i + Nkv - N - wl, i + Nkv - N + wr] (kSchedUnbounded: none)
     float scale;
 };
 
-// Enqueue the pre-pass, the dQ pass and the dK/dV pass on `s`.
+// Enqueue the pre-pass, then the dQ pass and the dK/dV pass, or (fused) the
+// one pass and the conversion of the dQ accumulator, on `s`.
 fa_status launch_bwd(const BwdLaunch &a, cudaStream_t s, int dev);
 bool take_status_word_bwd(cudaStream_t s, unsigned int *word);
 

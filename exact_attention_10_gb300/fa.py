@@ -12,9 +12,10 @@ import os
 from .build import LIB_PATH
 
 FA_BF16, FA_FP16 = 0, 1
+FA_BWD_DETERMINISTIC = 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_MISALIGNED", 3: "FA_ERR_UNSUPPORTED_DEVICE",
           4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT", 6: "FA_ERR_NO_ALLOC_LIMIT"}
-EXPORTS = ("fa_bwd", "fa_bwd_band", "fa_fwd", "fa_fwd_band", "fa_fwd_ex", "fa_fwd_noalloc", "fa_fwd_qkv", "fa_sync_status",
+EXPORTS = ("fa_bwd", "fa_bwd_band", "fa_bwd_ex", "fa_fwd", "fa_fwd_band", "fa_fwd_ex", "fa_fwd_noalloc", "fa_fwd_qkv", "fa_sync_status",
            "fa_status_string")
 SCHEDULES = {"auto": 0, "whole_tiles": 1, "balanced": 2}
 
@@ -52,6 +53,8 @@ def load(path: str = LIB_PATH):
     lib.fa_bwd.restype = c_int
     lib.fa_bwd_band.argtypes = [vp] * 9 + [c_int] * 7 + [ctypes.c_float, c_int, vp]
     lib.fa_bwd_band.restype = c_int
+    lib.fa_bwd_ex.argtypes = [vp] * 9 + [c_int] * 7 + [ctypes.c_float, c_int, ctypes.c_uint, vp]
+    lib.fa_bwd_ex.restype = c_int
     lib.fa_sync_status.argtypes = [vp]
     lib.fa_sync_status.restype = c_int
     lib.fa_status_string.argtypes = [c_int]
@@ -139,11 +142,13 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
 
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
-             stream=None, window: tuple[int, int] | None = None):
+             stream=None, window: tuple[int, int] | None = None, deterministic: bool = False):
     """Attention backward on CUDA tensors: q, o, do [B, H, Nq, D], k, v
     [B, H, Nkv, D] and lse [B, H, Nq] as ``forward`` returned them (same
     causal / window); returns (dQ, dK, dV).  Square unmasked or causal calls
-    go to fa_bwd; a window, or Nq != Nkv (bottom-right causal), to fa_bwd_band.
+    go to fa_bwd; a window, or Nq != Nkv (bottom-right causal), to fa_bwd_band;
+    ``deterministic`` (dQ by the second pass, the same bits on every call) to
+    fa_bwd_ex with FA_BWD_DETERMINISTIC.
 
     ``dq`` / ``dk`` / ``dv`` may be given to write into existing buffers.
     Raises FAError on any non-OK status.  Asynchronous on ``stream``
@@ -170,7 +175,10 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
     st = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
             dk.data_ptr(), dv.data_ptr())
-    if window is None and Nkv == N:
+    if deterministic:
+        left, right = window if window is not None else (-1, 0 if causal else -1)
+        rc = load().fa_bwd_ex(*ptrs, B, H, N, Nkv, D, int(left), int(right), float(scale), code, FA_BWD_DETERMINISTIC, st)
+    elif window is None and Nkv == N:
         rc = load().fa_bwd(*ptrs, B, H, N, D, int(bool(causal)), float(scale), code, st)
     else:
         left, right = window if window is not None else (-1, 0 if causal else -1)

@@ -235,14 +235,22 @@ FA_API fa_status fa_fwd_noalloc(const void *Q, const void *K, const void *V, voi
  * dQ = scale * dS K,  dK = scale * dS^T Q.  P and dS are rounded to `dtype`
  * for the tensor-core products, which accumulate in fp32.  P is recomputed
  * from LSE ("FlashAttention 2 from PyTorch to Triton", What I am building);
- * dK and dV are accumulated per key tile over the query tiles, dQ in a second
- * pass over the key tiles (its list of limitations), so no atomics are used
- * and the result is deterministic.
+ * dK and dV are accumulated per key tile over the query tiles.  dQ (the
+ * page's list of limitations: "by atomics or a second pass"):
+ *  - D = 64: in the same pass, each key tile's dQ products added into an
+ *    fp32 accumulator in global memory by tensor reductions (fp32 adds in
+ *    L2), then scaled and rounded to `dtype`.  The order of those adds varies
+ *    from call to call, so dQ may differ in its last bits between calls;
+ *    dK and dV do not.
+ *  - D = 128, and any call through fa_bwd_ex with FA_BWD_DETERMINISTIC: in a
+ *    second pass over the key tiles, without atomics; bit for bit the same
+ *    on every call.
  *
  * Scratch: 8 bytes per query row (rounded up to 128 rows per head) for delta
- * and LSE * log2(e), allocated per (device, stream) on first use like the
- * balanced schedule's workspace.  Errors as for fa_fwd; FA_ERR_CUDA if the
- * scratch cannot be allocated.
+ * and LSE * log2(e), plus 4 * D bytes per such row for the dQ accumulator on
+ * the D = 64 single pass, allocated per (device, stream) on first use like
+ * the balanced schedule's workspace.  Errors as for fa_fwd; FA_ERR_CUDA if
+ * the scratch cannot be allocated.
  */
 FA_API fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                         const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int D, int causal,
@@ -263,6 +271,19 @@ FA_API fa_status fa_bwd(const void *Q, const void *K, const void *V, const void 
 FA_API fa_status fa_bwd_band(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                              const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nkv, int D,
                              int window_left, int window_right, float scale, fa_dtype dtype, fa_stream_t stream);
+
+/* fa_bwd_ex flags. */
+#define FA_BWD_DETERMINISTIC 1u /* dQ by the second pass at every D: the same bits on every call */
+
+/*
+ * fa_bwd_ex -- fa_bwd_band with `flags` (0 or FA_BWD_DETERMINISTIC; any other
+ * bit: FA_ERR_INVALID_VALUE).  fa_bwd and fa_bwd_band are fa_bwd_ex with
+ * flags = 0.
+ */
+FA_API fa_status fa_bwd_ex(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                           const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nkv, int D,
+                           int window_left, int window_right, float scale, fa_dtype dtype, unsigned int flags,
+                           fa_stream_t stream);
 
 /*
  * fa_sync_status -- synchronise `stream`, then return and clear the device

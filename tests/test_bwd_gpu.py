@@ -60,11 +60,11 @@ def _inputs(B, H, N, D, dtype, seed):
     return q, k, v, do
 
 
-def _gpu_grads(q, k, v, do, causal, scale):
+def _gpu_grads(q, k, v, do, causal, scale, deterministic=False):
     dev = torch.device("cuda:0")
     qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
     o, lse = fa.forward(qd, kd, vd, causal=causal, scale=scale)
-    dq, dk, dv = fa.backward(qd, kd, vd, o, dod, lse, causal=causal, scale=scale)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, dod, lse, causal=causal, scale=scale, deterministic=deterministic)
     rc = fa.sync_status(torch.cuda.current_stream(dev).cuda_stream)
     assert rc == 0, fa.status_string(rc)
     return dq.cpu(), dk.cpu(), dv.cpu()
@@ -118,11 +118,14 @@ CASES = [  # (B, H, N, D, dtype)
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,H,N,D,dtype", CASES)
 def test_backward_matches_oracle(B, H, N, D, dtype, causal):
+    """At D = 64 both dQ paths: the fused pass (the default) and the second
+    pass (deterministic)."""
     q, k, v, do = _inputs(B, H, N, D, dtype, seed=N + D)
     scale = D ** -0.5
-    grads = _gpu_grads(q, k, v, do, causal, scale)
     refs = oracle.backward(q, k, v, do, causal, scale)
-    _check(grads, refs, dtype, f"B{B} H{H} N{N} D{D} {dtype} causal={int(causal)}")
+    for det in ((False, True) if D == 64 else (False,)):
+        grads = _gpu_grads(q, k, v, do, causal, scale, deterministic=det)
+        _check(grads, refs, dtype, f"B{B} H{H} N{N} D{D} {dtype} causal={int(causal)} deterministic={int(det)}")
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -139,17 +142,37 @@ def test_backward_single_row(D):
 
 
 def test_backward_deterministic_and_invariant():
-    """Two calls give identical bits (no atomics), and the key rows of dK sum
-    to (nearly) zero per head, as every row of dS does."""
+    """Two deterministic calls give identical bits (no atomics), and the key
+    rows of dK sum to (nearly) zero per head, as every row of dS does."""
     B, H, N, D = 2, 4, 1000, 64
     q, k, v, do = _inputs(B, H, N, D, "bf16", seed=3)
-    a = _gpu_grads(q, k, v, do, True, D ** -0.5)
-    b = _gpu_grads(q, k, v, do, True, D ** -0.5)
+    a = _gpu_grads(q, k, v, do, True, D ** -0.5, deterministic=True)
+    b = _gpu_grads(q, k, v, do, True, D ** -0.5, deterministic=True)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
     dk = a[1].double()
     colsum = dk.sum(dim=2).abs().max().item()
     assert colsum <= 1e-2 * dk.abs().sum(dim=2).max().item()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_fused_against_two_pass(causal):
+    """The D = 64 fused pass against the two-pass path on the same inputs:
+    dK and dV come from the same arithmetic in the same order (bit for bit,
+    and on every call); dQ differs only by the order of its fp32 adds, so
+    within a few fp32 roundings of its accumulation, far below the 16-bit
+    output step (checked: at most one unit in the last place of dQ's type,
+    with a floor of 2^-16 of the largest |dQ| for elements that cancel)."""
+    B, H, N, D = 2, 4, 1000, 64
+    q, k, v, do = _inputs(B, H, N, D, "bf16", seed=5)
+    det = _gpu_grads(q, k, v, do, causal, D ** -0.5, deterministic=True)
+    f1 = _gpu_grads(q, k, v, do, causal, D ** -0.5)
+    f2 = _gpu_grads(q, k, v, do, causal, D ** -0.5)
+    for x in (f1, f2):
+        assert torch.equal(x[1], det[1]) and torch.equal(x[2], det[2])
+        a, b = x[0].float(), det[0].float()
+        ulp = torch.maximum(a.abs(), b.abs()) * 2.0 ** -7 + b.abs().max() * 2.0 ** -16
+        assert bool(((a - b).abs() <= ulp).all()), float(((a - b).abs() / ulp).max())
 
 
 @pytest.mark.parametrize("causal", [False, True])
