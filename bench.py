@@ -113,6 +113,9 @@ def decode_timings(steps: int, dev, stream, flush, hbm_gbs: float) -> dict:
 # long-context one is causal at N = 32768 and non-causal at N = 16384.
 CONFIG_WORKLOADS = ("tiny_n256", "b4h16_n1024", "b2h16_n4096", "ragged_n3000_d128_fp16", "long_n32768_d128",
                     "long_n16384_d128")
+# ... of which these also time fa_bwd (the headline workload's backward is in
+# the line's own "backward" object)
+BWD_CONFIG_WORKLOADS = ("b4h16_n1024", "ragged_n3000_d128_fp16", "long_n16384_d128")
 
 
 def config_timings(steps: int, dev, stream, flush, peak: float) -> dict:
@@ -123,7 +126,7 @@ def config_timings(steps: int, dev, stream, flush, peak: float) -> dict:
     import torch
     from exact_attention_10_gb300 import fa
     from exact_attention_10_gb300.accounting import flops, flops_causal_exact, fused_bytes
-    from exact_attention_10_gb300.inputs import WORKLOADS, make_qkv
+    from exact_attention_10_gb300.inputs import WORKLOADS, make_custom, make_qkv
     out = {"schedule": "auto", "l2": "flushed between calls", "steps": steps, "inputs": "make_qkv(seed=0)",
            "peak_tflops": peak, "workloads": {}}
     for name in CONFIG_WORKLOADS:
@@ -160,6 +163,28 @@ def config_timings(steps: int, dev, stream, flush, peak: float) -> dict:
             kname = f"fa_fwd_sm103<{w.D},{w.dtype},{'causal' if causal else 'noncausal'}>"
             rec["algorithmic_bytes"] = fused_bytes(w.B, w.H, w.N, w.D)
             rec["traffic"] = _traffic_record(kname, workload_name=name)
+            if name in BWD_CONFIG_WORKLOADS:   # fa_bwd from this forward's O and LSE, timed the same way
+                do = make_custom(w.B, w.H, w.N, w.D, w.dtype, seed=1)[0].to(dev)
+                grads = tuple(torch.empty_like(x) for x in (q, k, v))
+                for _ in range(3):
+                    fa.backward(q, k, v, o, do, lse, causal=causal, scale=w.scale, dq=grads[0], dk=grads[1],
+                                dv=grads[2])
+                for i in range(steps):
+                    flush.zero_()
+                    starts[i].record(stream)
+                    fa.backward(q, k, v, o, do, lse, causal=causal, scale=w.scale, dq=grads[0], dk=grads[1],
+                                dv=grads[2])
+                    ends[i].record(stream)
+                torch.cuda.synchronize(dev)
+                rc = fa.sync_status(stream.cuda_stream)
+                if rc != 0:
+                    raise fa.FAError(rc, name + " backward")
+                bavg = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
+                btf = 2.5 * fl / (bavg * 1e-3) / 1e12
+                rec["backward"] = {"ms_mean": bavg, "tflops": btf, "frac_of_measured_peak": btf / peak,
+                                   "flops_convention": "2.5 x forward",
+                                   "dq_path": "one pass (fp32 accumulator)" if w.D == 64 else "second pass"}
+                del do, grads
             entry["causal" if causal else "noncausal"] = rec
         out["workloads"][name] = entry
         del q, k, v, o, lse
@@ -516,7 +541,9 @@ def main(argv=None):
         do = make_custom(w.B, w.H, w.N, w.D, w.dtype, seed=1)[0].to(dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         bwd_info = {"flops_convention": "2.5 x forward (five tile products per tile pair)",
-                    "kernels_per_call": 3}
+                    "kernels_per_call": 3,
+                    "dq_path": ("one pass: dQ products added into an fp32 accumulator by TMA reductions"
+                                if w.D == 64 else "second pass over the key tiles")}
         for c in modes:
             call(c)
             for _ in range(3):

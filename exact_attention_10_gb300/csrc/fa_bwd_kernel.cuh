@@ -322,6 +322,45 @@ __device__ __forceinline__ uint32_t a_col(int kk)
     return (uint32_t)(64 * (kk / 4) + 8 * (kk % 4));
 }
 
+// PTX of the fused pass (bulk tensor reductions, 16-byte shared stores).
+namespace fq {
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// 2-D tiled tensor reduction shared -> global: adds the box at `src` to the
+// tensor at (c0, c1) element by element (fp32 add for an fp32 map), as one
+// bulk async-group operation; c0 * 4 bytes must be a multiple of 16.
+__device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, uint32_t src, int c0, int c1)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+// Close this thread's bulk async-group operations issued so far into a group.
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every committed bulk group of this thread has finished reading
+// its shared-memory source (the source may then be overwritten).
+__device__ __forceinline__ void bulk_wait_group_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until every committed bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_group0()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+}  // namespace fq
+
 // ------------------------------------------------------------------ producer
 
 template <int D, bool KV, bool FQ>
@@ -909,7 +948,7 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
                 const uint32_t rb = sDs + (uint32_t)(h * C::kBoxBytes + row * 128);
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch)
-                    ptx::st_shared_v4(rb + (uint32_t)((ch ^ (row & 7)) << 4), pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
+                    fq::st_shared_v4(rb + (uint32_t)((ch ^ (row & 7)) << 4), pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
                                       pk[4 * ch + 3]);
                 ptx::fence_proxy_async_smem();   // visible to the tensor core's reads
             } else {
@@ -956,6 +995,7 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
 
 // ------------------------------------------------------------------ fused pass: dQ
 
+
 // The fused pass's dQ products (warp 10): per step g, once the compute warps
 // have written dS^T_g (p_full) and the read-out warps have loaded the
 // previous product (dq_free), dQ_g = dS_g K into the dQ columns -- A is the
@@ -968,7 +1008,8 @@ template <int D, bool BF16, bool CAUSAL>
 __device__ void bwd_mma_dq(const Params &p, uint32_t sRes, uint32_t sDs, uint32_t tmem, BBars<D, true, true> b, Ctl c)
 {
     using C = BCfg<D, true, true>;
-    constexpr uint32_t kIdesc = instr_desc_f16(BF16, kTile, D, true, true);   // A and B MN-major
+    // instr_desc_f16 with bit 15 (A MN-major) set as well: A and B MN-major
+    constexpr uint32_t kIdesc = instr_desc_f16(BF16, kTile, D, true) | (1u << 15);
     const uint32_t a_lo = desc_lo(sDs, C::kBoxBytes), k_lo = desc_lo(sRes, C::kBoxBytes);
     const uint32_t tDQ = tmem + C::kColDQ;
     int g = 0, tiles = 0;
@@ -1058,7 +1099,7 @@ __device__ void bwd_dq_out(const CUtensorMap *tmDQ, const Params &p, uint32_t tm
             }
             ptx::tc_fence_after_sync();
             if (leader && pending)
-                ptx::bulk_wait_group_read0();
+                fq::bulk_wait_group_read0();
             dq_sync();   // the staging is free
 #pragma unroll
             for (int cc = 0; cc < D / 16; ++cc) {   // 16 columns at a time: 4 chunks of box cc / 2
@@ -1069,7 +1110,7 @@ __device__ void bwd_dq_out(const CUtensorMap *tmDQ, const Params &p, uint32_t tm
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int ch = (cc % 2) * 4 + u;
-                    ptx::st_shared_v4(rowb + (uint32_t)((ch ^ (q & 7)) << 4), v[4 * u], v[4 * u + 1], v[4 * u + 2],
+                    fq::st_shared_v4(rowb + (uint32_t)((ch ^ (q & 7)) << 4), v[4 * u], v[4 * u + 1], v[4 * u + 2],
                                       v[4 * u + 3]);
                 }
             }
@@ -1079,15 +1120,15 @@ __device__ void bwd_dq_out(const CUtensorMap *tmDQ, const Params &p, uint32_t tm
             dq_sync();
             if (leader) {
                 const int y = bh * p.Npad + (s0 + j) * kTile;
-                ptx::tma_reduce_add_2d(tmDQ, sDq, 0, y);
-                ptx::tma_reduce_add_2d(tmDQ, sDq + C::kDqBoxBytes, 32, y);
-                ptx::bulk_commit_group();
+                fq::tma_reduce_add_2d(tmDQ, sDq, 0, y);
+                fq::tma_reduce_add_2d(tmDQ, sDq + C::kDqBoxBytes, 32, y);
+                fq::bulk_commit_group();
                 pending = true;
             }
         }
     }
     if (leader && pending)
-        ptx::bulk_wait_group0();   // the reductions are done with the staging (and complete) before exit
+        fq::bulk_wait_group0();   // the reductions are done with the staging (and complete) before exit
 }
 
 // ------------------------------------------------------------------ kernels

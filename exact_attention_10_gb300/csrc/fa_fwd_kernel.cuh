@@ -273,10 +273,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor for kind::f16 with fp32 accumulation.
-__host__ __device__ constexpr uint32_t instr_desc_f16(bool bf16, int M, int N, bool b_mn_major, bool a_mn_major = false)
+__host__ __device__ constexpr uint32_t instr_desc_f16(bool bf16, int M, int N, bool b_mn_major)
 {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Q-tile step count within a part: Q tile w of the part's tile visits steps

@@ -125,35 +125,6 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
-// 2-D tiled tensor reduction shared -> global: adds the box at `src` to the
-// tensor at (c0, c1) element by element (fp32 add for an fp32 map), as one
-// bulk async-group operation; c0 * 4 bytes must be a multiple of 16.
-__device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, uint32_t src, int c0, int c1)
-{
-    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
-                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(c0), "r"(c1)
-                 : "memory");
-}
-
-// Close this thread's bulk async-group operations issued so far into a group.
-__device__ __forceinline__ void bulk_commit_group()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until every committed bulk group of this thread has finished reading
-// its shared-memory source (the source may then be overwritten).
-__device__ __forceinline__ void bulk_wait_group_read0()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Wait until every committed bulk group of this thread has completed.
-__device__ __forceinline__ void bulk_wait_group0()
-{
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 __device__ __forceinline__ uint64_t l2_policy_evict_last()
 {
     uint64_t p;
@@ -388,11 +359,6 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_u64(uint32_t addr, uint64_t v)
