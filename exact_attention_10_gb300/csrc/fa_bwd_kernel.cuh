@@ -13,8 +13,9 @@
 //
 // Three kernels, in stream order:
 //   fa_bwd_prep   per query row: delta = rowsum(dO o O) and lg = LSE * log2(e),
-//                 laid out [B*H][N rounded up to 128], with lg = +inf on the
-//                 padding rows (and rows that see no key) so their P is 0;
+//                 stored negated (as the passes add them), laid out [B*H][N
+//                 rounded up to 128], with lg = +inf on the padding rows (and
+//                 rows that see no key) so their P is 0;
 //   fa_bwd_sm103<..., KV = true>   dK, dV: a CTA holds one 128-key tile of K
 //                 and V and streams the query tiles (Q, dO, lg, delta) past it;
 //   fa_bwd_sm103<..., KV = false>  dQ: a CTA holds one 128-row tile of Q and
@@ -22,6 +23,15 @@
 //                 pass, which keeps dQ deterministic and out of atomics.
 // Both main passes recompute S and dP; that costs two extra tile products
 // per (query tile, key tile) pair over a single pass with atomic dQ.
+//
+// At D = 64 the default is that single pass instead (FQ, "fused"): the dK/dV
+// pass also computes each step's dQ product dS K (dS^T goes to shared memory
+// so that it can serve as the MMA's A operand for both dK and dQ), and four
+// more warps read the product out of TMEM and add it into an fp32 dQ
+// accumulator [B*H][Npad][D] in global memory with tensor reductions (fp32
+// adds in L2); fa_bwd_prep zeroes the accumulator first and
+// fa_bwd_dq_convert scales and rounds it into dQ last.  The order of the adds
+// varies between calls, so dQ may differ in its last bits from call to call.
 //
 // Per (resident tile, streamed tile) step, with M = 128 lanes of TMEM on the
 // resident tile's rows:
@@ -88,8 +98,8 @@ enum : uint32_t {
 struct Params {
     void *dA;          // KV: dK ([B*H, Nkv, D]); dQ pass: dQ ([B*H, N, D]); the input type
     void *dB;          // KV: dV; dQ pass: unused
-    const float *lg;   // LSE * log2(e) per query row, [B*H][Npad]; +inf on padding rows and rows without keys
-    const float *dl;   // delta = rowsum(dO o O) per query row, [B*H][Npad]
+    const float *lg;   // -LSE * log2(e) per query row, [B*H][Npad]; -inf on padding rows and rows without keys
+    const float *dl;   // -delta = -rowsum(dO o O) per query row, [B*H][Npad]
     int N;             // query rows per head
     int Nkv;           // keys per head
     int Npad;          // N rounded up to a multiple of 128
@@ -577,7 +587,7 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
             break;
         int bh, rt, s0, n;
         bwd_decode<KV>(p, CAUSAL, t, bh, rt, s0, n);
-        // dQ pass: this thread's query row has one lg and delta for the tile.
+        // dQ pass: this thread's query row has one -lg and -delta for the tile.
         float lg_row = 0.f, dl_row = 0.f;
         if (!KV) {
             const size_t off = (size_t)bh * p.Npad + (size_t)rt * kTile + lane_row;
@@ -593,7 +603,7 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
             const uint32_t vec = sStage + st * C::kStageBytes + 2 * C::kTileBytes;   // KV: lg[128], delta[128]
             // Masks: the band's edges (the causal diagonal) and, in the dQ
             // pass, keys past Nkv in the last key tile.  (Padding queries and
-            // queries without keys have lg = +inf, so their P is already 0.)
+            // queries without keys have lg = +inf (stored as -lg = -inf), so their P is already 0.)
             const StepMask sm = bwd_step_mask(p, CAUSAL, KV ? rt : si, KV ? si : rt);
             const int key_limit = KV ? kTile : p.Nkv - si * kTile;  // dQ pass: columns >= key_limit are past Nkv
             const bool masked = !sm.whole || key_limit < kTile;     // warp-uniform
@@ -611,10 +621,10 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
                     uint64_t nl01, nl23;   // -lg for the four columns, as pairs
                     if (KV) {
                         const float4 lg4 = ptx::ld_shared_v4f32(vec + (uint32_t)(c0 + i) * 4);
-                        nl01 = ptx::f2_pack(-lg4.x, -lg4.y);
-                        nl23 = ptx::f2_pack(-lg4.z, -lg4.w);
+                        nl01 = ptx::f2_pack(lg4.x, lg4.y);
+                        nl23 = ptx::f2_pack(lg4.z, lg4.w);
                     } else {
-                        nl01 = nl23 = ptx::f2_pack(-lg_row, -lg_row);
+                        nl01 = nl23 = ptx::f2_pack(lg_row, lg_row);
                     }
                     float x[4];
                     ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), qk2, nl01),
@@ -645,10 +655,10 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
                     uint64_t nd01, nd23;   // -delta, as pairs
                     if (KV) {
                         const float4 d4 = ptx::ld_shared_v4f32(vec + kTile * 4 + (uint32_t)(c0 + i) * 4);
-                        nd01 = ptx::f2_pack(-d4.x, -d4.y);
-                        nd23 = ptx::f2_pack(-d4.z, -d4.w);
+                        nd01 = ptx::f2_pack(d4.x, d4.y);
+                        nd23 = ptx::f2_pack(d4.z, d4.w);
                     } else {
-                        nd01 = nd23 = ptx::f2_pack(-dl_row, -dl_row);
+                        nd01 = nd23 = ptx::f2_pack(dl_row, dl_row);
                     }
                     float ds[4];
                     ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(pr[i], pr[i + 1]),
@@ -866,8 +876,8 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
         uint64_t nlg = 0, ndl = 0;   // dQ pass: this thread's query row's -lg and -delta
         if (!KV) {
             const size_t off = (size_t)bh * p.Npad + (size_t)rt * kTile + row;
-            nlg = ptx::f2_pack(-p.lg[off], -p.lg[off]);
-            ndl = ptx::f2_pack(-p.dl[off], -p.dl[off]);
+            nlg = ptx::f2_pack(p.lg[off], p.lg[off]);
+            ndl = ptx::f2_pack(p.dl[off], p.dl[off]);
         }
         for (int j = 0; j < n; ++j, ++g) {
             const int si = s0 + j;   // streamed tile
@@ -883,7 +893,7 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
             // KV: lane = key, column = query (lg and delta per column, from the
             // stage); dQ pass: lane = query, column = key.  Masks: the band's
             // edges (the causal diagonal), and in the dQ pass keys past Nkv
-            // (padding queries and queries without keys have lg = +inf).
+            // (padding queries and queries without keys have lg = +inf, stored as -inf).
             const uint32_t vec = sStage + (g % C::kStages) * C::kStageBytes + 2 * C::kTileBytes;
             const int limit = KV ? kTile : p.Nkv - si * kTile;   // dQ pass: columns >= limit past Nkv
             const StepMask sm = bwd_step_mask(p, CAUSAL, KV ? rt : si, KV ? si : rt);
@@ -893,17 +903,22 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
             // hidden scores to -inf (exp2 gives 0) in a separate pass, so the
             // main loop carries no mask code.
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-                uint64_t nl = nlg;
+            for (int i = 0; i < 64; i += 4) {
+                uint64_t nl01 = nlg, nl23 = nlg;   // -lg, as pairs (KV: four queries' in one load)
                 if (KV) {
-                    const float2 l2 = ptx::ld_shared_v2f32(vec + (uint32_t)(64 * h + i) * 4);
-                    nl = ptx::f2_pack(-l2.x, -l2.y);
+                    const float4 l4 = ptx::ld_shared_v4f32(vec + (uint32_t)(64 * h + i) * 4);
+                    nl01 = ptx::f2_pack(l4.x, l4.y);
+                    nl23 = ptx::f2_pack(l4.z, l4.w);
                 }
-                float x0, x1;
-                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), qk2, nl),
+                float x0, x1, x2, x3;
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), qk2, nl01),
                                x0, x1);
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), qk2, nl23),
+                               x2, x3);
                 sv[i] = __float_as_uint(x0);
                 sv[i + 1] = __float_as_uint(x1);
+                sv[i + 2] = __float_as_uint(x2);
+                sv[i + 3] = __float_as_uint(x3);
             }
             if (masked) {
                 const uint32_t ninf = __float_as_uint(-INFINITY);
@@ -912,21 +927,26 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
                     sv[i] = ((uint32_t)(lm.a + 64 * h + i) < lm.width) ? sv[i] : ninf;
             }
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-                uint64_t nd = ndl;
+            for (int i = 0; i < 64; i += 4) {
+                uint64_t nd[2] = {ndl, ndl};   // -delta, as pairs (KV: four queries' in one load)
                 if (KV) {
-                    const float2 d2 = ptx::ld_shared_v2f32(vec + kTile * 4 + (uint32_t)(64 * h + i) * 4);
-                    nd = ptx::f2_pack(-d2.x, -d2.y);
+                    const float4 d4 = ptx::ld_shared_v4f32(vec + kTile * 4 + (uint32_t)(64 * h + i) * 4);
+                    nd[0] = ptx::f2_pack(d4.x, d4.y);
+                    nd[1] = ptx::f2_pack(d4.z, d4.w);
                 }
-                const float p0 = ptx::ex2(__uint_as_float(sv[i])), p1 = ptx::ex2(__uint_as_float(sv[i + 1]));
-                float d0, d1;
-                ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1),
-                                           ptx::f2_add(ptx::f2_pack(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), nd)),
-                               d0, d1);
-                sv[i] = __float_as_uint(p0);   // P, kept for KV's P^T
-                sv[i + 1] = __float_as_uint(p1);
-                dv[i] = __float_as_uint(d0);   // dS
-                dv[i + 1] = __float_as_uint(d1);
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const float p0 = ptx::ex2(__uint_as_float(sv[i + e])), p1 = ptx::ex2(__uint_as_float(sv[i + e + 1]));
+                    float d0, d1;
+                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1),
+                                               ptx::f2_add(ptx::f2_pack(__uint_as_float(dv[i + e]), __uint_as_float(dv[i + e + 1])),
+                                                           nd[e / 2])),
+                                   d0, d1);
+                    sv[i + e] = __float_as_uint(p0);   // P, kept for KV's P^T
+                    sv[i + e + 1] = __float_as_uint(p1);
+                    dv[i + e] = __float_as_uint(d0);   // dS
+                    dv[i + e + 1] = __float_as_uint(d1);
+                }
             }
             uint32_t pk[32];
             if (KV) {
@@ -1236,8 +1256,9 @@ __global__ void __launch_bounds__(FQ ? kThreadsFused : kThreads, 1)
     }
 }
 
-// delta = rowsum(dO o O) and lg = LSE * log2(e) per query row, padded to
-// whole 128-row tiles: D / 8 threads per row, 16 bytes each.  dqa (the fused
+// -delta = -rowsum(dO o O) and -lg = -LSE * log2(e) per query row (negated,
+// as the passes add them), padded to whole 128-row tiles: D / 8 threads per
+// row, 16 bytes each.  dqa (the fused
 // pass's fp32 dQ accumulator, [rows][D], or null): zeroed, 8 values a thread.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
@@ -1286,14 +1307,14 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int m = kTpr / 2; m > 0; m /= 2)
         acc += __shfl_xor_sync(group, acc, m);
-    if (part == 0) {
-        float l = INFINITY;
+    if (part == 0) {   // negated, as the passes add them
+        float l = -INFINITY;
         if (i < N) {
             const float lse = LSE[(size_t)bh * N + i];
-            l = (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;   // a row without keys: P = 0
+            l = (lse == -INFINITY) ? -INFINITY : -(lse * 1.4426950408889634f);   // a row without keys: P = 0
         }
         lg[row] = l;
-        dl[row] = (i < N) ? acc : 0.f;
+        dl[row] = (i < N) ? -acc : 0.f;
     }
 }
 
