@@ -948,7 +948,11 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
                     dv[i + e + 1] = __float_as_uint(d1);
                 }
             }
-            uint32_t pk[32];
+            uint32_t pk[32], dk[32];   // P and dS as 16-bit pairs, both packed before the wait below
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                dk[i] = BF16 ? ptx::pack_bf16x2(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]))
+                             : ptx::pack_f16x2(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]));
             if (KV) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
@@ -960,19 +964,15 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
                 ptx::tc_fence_after_sync();
                 ptx::tmem_st32(tmem + C::kColP + lane_off + 32 * h, pk);
             }
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                pk[i] = BF16 ? ptx::pack_bf16x2(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]))
-                             : ptx::pack_f16x2(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]));
             if (FQ) {   // key row `row`, queries [64h, 64h + 64): one 128-byte swizzled row of box h
                 const uint32_t rb = sDs + (uint32_t)(h * C::kBoxBytes + row * 128);
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch)
-                    fq::st_shared_v4(rb + (uint32_t)((ch ^ (row & 7)) << 4), pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
-                                      pk[4 * ch + 3]);
+                    fq::st_shared_v4(rb + (uint32_t)((ch ^ (row & 7)) << 4), dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2],
+                                      dk[4 * ch + 3]);
                 ptx::fence_proxy_async_smem();   // visible to the tensor core's reads
             } else {
-                ptx::tmem_st32(tmem + C::kColDS + (KV ? 0u : 64u * (uint32_t)(g & 1)) + lane_off + 32 * h, pk);
+                ptx::tmem_st32(tmem + C::kColDS + (KV ? 0u : 64u * (uint32_t)(g & 1)) + lane_off + 32 * h, dk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
@@ -1118,24 +1118,29 @@ __device__ void bwd_dq_out(const CUtensorMap *tmDQ, const Params &p, uint32_t tm
                 break;
             }
             ptx::tc_fence_after_sync();
+            // Two round trips to TMEM of 32 columns each (box 0, then box 1);
+            // the product is released as soon as the second has landed.
+            uint32_t v[2][16];
+            ptx::tmem_ld16(tq, v[0]);
+            ptx::tmem_ld16(tq + 16, v[1]);
             if (leader && pending)
                 fq::bulk_wait_group_read0();
             dq_sync();   // the staging is free
+            auto stage_box = [&](int box) {   // this row's 32 columns of box `box`: 8 swizzled 16-byte chunks
+                const uint32_t rowb = sDq + (uint32_t)(box * C::kDqBoxBytes + q * 128);
 #pragma unroll
-            for (int cc = 0; cc < D / 16; ++cc) {   // 16 columns at a time: 4 chunks of box cc / 2
-                uint32_t v[16];
-                ptx::tmem_ld16(tq + 16 * cc, v);
-                ptx::tmem_wait_ld();
-                const uint32_t rowb = sDq + (uint32_t)((cc / 2) * C::kDqBoxBytes + q * 128);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int ch = (cc % 2) * 4 + u;
-                    fq::st_shared_v4(rowb + (uint32_t)((ch ^ (q & 7)) << 4), v[4 * u], v[4 * u + 1], v[4 * u + 2],
-                                      v[4 * u + 3]);
-                }
-            }
+                for (int ch = 0; ch < 8; ++ch)
+                    fq::st_shared_v4(rowb + (uint32_t)((ch ^ (q & 7)) << 4), v[ch / 4][4 * (ch % 4)],
+                                      v[ch / 4][4 * (ch % 4) + 1], v[ch / 4][4 * (ch % 4) + 2], v[ch / 4][4 * (ch % 4) + 3]);
+            };
+            ptx::tmem_wait_ld();
+            stage_box(0);
+            ptx::tmem_ld16(tq + 32, v[0]);
+            ptx::tmem_ld16(tq + 48, v[1]);
+            ptx::tmem_wait_ld();
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(b.dq_free());
+            stage_box(1);
             ptx::fence_proxy_async_smem();   // the staging, visible to the reductions
             dq_sync();
             if (leader) {
