@@ -14,10 +14,10 @@ void fwd(const char *name, bool last)
                 C::kStages, C::kQBufs, C::kMmaWarps, (int)C::kSeparateP, (int)C::kSplitKV, last ? "" : ", ");
 }
 
-template <int D, bool KV>
+template <int D, bool KV, bool FQ = false>
 void bwd(const char *name, bool last)
 {
-    using C = fa::bwd::BCfg<D, KV>;
+    using C = fa::bwd::BCfg<D, KV, FQ>;
     std::printf("\"%s\": {\"pipeline\": %d, \"split\": %d, \"ring0\": %d, \"ring1\": %d}%s", name,
                 (int)fa::bwd::kPipeline<D, KV>, (int)C::kSplitRing, C::kRing0, C::kRing1, last ? "" : ", ");
 }
@@ -29,6 +29,7 @@ int main()
     fwd<128>("fwd128", false);
     bwd<64, false>("d64_dq", false);
     bwd<64, true>("d64_kv", false);
+    bwd<64, true, true>("d64_fused", false);
     bwd<128, false>("d128_dq", false);
     bwd<128, true>("d128_kv", true);
     std::printf("}\n");

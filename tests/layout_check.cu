@@ -81,10 +81,10 @@ void forward(bool split)
     check("forward D=" + std::to_string(D) + (split ? " balanced" : " whole"), r, C::smem_bytes(split));
 }
 
-template <int D, bool KV>
+template <int D, bool KV, bool FQ = false>
 void backward()
 {
-    using C = fa::bwd::BCfg<D, KV>;
+    using C = fa::bwd::BCfg<D, KV, FQ>;
     std::vector<Region> r = {{"resident tiles", C::kResOff, 2L * C::kTileBytes, 1024}};
     if (C::kSplitRing) {
         r.push_back({"ring 0", C::kStageOff, (long)C::kRing0 * C::kTileBytes, 1024});
@@ -92,9 +92,13 @@ void backward()
     } else {
         r.push_back({"stages", C::kStageOff, (long)C::kStages * C::kStageBytes, 1024});
     }
+    if (FQ) {
+        r.push_back({"dS^T tile", C::kDsOff, (long)fa::bwd::kTile * fa::bwd::kTile * 2, 1024});
+        r.push_back({"dQ staging", C::kDqOff, 2L * C::kDqBoxBytes, 1024});
+    }
     r.push_back({"barriers", C::kBarOff, (long)C::kNumBars * 8, 8});
     r.push_back({"misc", C::kMiscOff, 16, 8});
-    check("backward D=" + std::to_string(D) + (KV ? " dK/dV" : " dQ"), r, C::kSmem);
+    check("backward D=" + std::to_string(D) + (FQ ? " fused" : (KV ? " dK/dV" : " dQ")), r, C::kSmem);
 }
 
 }  // namespace
@@ -107,6 +111,7 @@ int main()
     forward<128>(true);
     backward<64, false>();
     backward<64, true>();
+    backward<64, true, true>();
     backward<128, false>();
     backward<128, true>();
     if (failures == 0)

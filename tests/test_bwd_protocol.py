@@ -7,7 +7,11 @@ bwd_compute, bwd_mma_pipe, bwd_compute_pipe):
 * D = 128, dQ pass: pipelined, K and V in separate rings of three and two
   slots, V's slot freed once dP is computed;
 * D = 128, dK/dV pass: not pipelined (P^T and dS^T overwrite S and dP, and the
-  next S follows the products in issue order), two stages.
+  next S follows the products in issue order), two stages;
+* D = 64, fused pass (bwd_mma_dq, bwd_dq_out): the pipelined dK/dV pass plus a
+  second MMA warp that issues each step's dQ product once P / dS are written
+  and the read-out warps have loaded the previous product, and the read-out
+  warps; pd_free (the P^T / dS^T buffers) and res_empty count both MMA warps.
 
 The producer, the MMA warp and the two compute warpgroups (column halves) are
 coroutines following the kernel's waits, arrivals and commits; barriers keep
@@ -19,7 +23,10 @@ CTAs holding one or several resident tiles of varying length must finish.
 The pin: in the pipelined dQ pass nothing holds the compute warps back from
 finishing step g + 1 before the MMA warp waits for step g, so one p_full
 barrier can run two phases ahead of its waiter; the kernel alternates two
-barriers there, and the model must flag the single-barrier form.
+barriers there, and the model must flag the single-barrier form.  In the
+fused pass, a pd_free that counted only the first MMA warp would let the
+compute warps overwrite dS^T before the dQ product has read it; the model
+flags that race.
 """
 from __future__ import annotations
 
@@ -32,15 +39,17 @@ import pytest
 @dataclass(frozen=True)
 class Pass:
     pipeline: bool
-    kv: bool          # dK/dV pass (else dQ)
-    split: bool       # K and V in separate rings (D = 128 dQ pass)
-    ring0: int        # stages, or slots of ring 0
-    ring1: int        # slots of ring 1 (split)
+    kv: bool            # dK/dV pass (else dQ)
+    split: bool         # K and V in separate rings (D = 128 dQ pass)
+    ring0: int          # stages, or slots of ring 0
+    ring1: int          # slots of ring 1 (split)
+    fused: bool = False  # the dK/dV pass with the dQ products (D = 64 default)
 
 
 PASSES = {
     "d64_dq": Pass(pipeline=True, kv=False, split=False, ring0=3, ring1=3),
     "d64_kv": Pass(pipeline=True, kv=True, split=False, ring0=3, ring1=3),
+    "d64_fused": Pass(pipeline=True, kv=True, split=False, ring0=3, ring1=3, fused=True),
     "d128_dq": Pass(pipeline=True, kv=False, split=True, ring0=3, ring1=2),
     "d128_kv": Pass(pipeline=False, kv=True, split=False, ring0=2, ring1=2),
 }
@@ -62,12 +71,16 @@ class Aliased(Exception):
     pass
 
 
+class Race(Exception):
+    pass
+
+
 def wait(bar: Barrier, k: int):
     return ("wait", bar, k)
 
 
 class CTA:
-    def __init__(self, q: Pass, alternate_p_full: bool):
+    def __init__(self, q: Pass, alternate_p_full: bool, dq_counted: bool = True):
         b = Barrier
         self.full = [b(f"full{s}") for s in range(q.ring0)]
         self.empty = [b(f"empty{s}") for s in range(q.ring0)]
@@ -78,6 +91,11 @@ class CTA:
         self.acc_full, self.acc_free = b("acc_full"), b("acc_free", COMPUTE)
         self.sd_free, self.pd_free = b("sd_free", COMPUTE), b("pd_free")
         self.alternate = alternate_p_full
+        if q.fused:   # both MMA warps read the P^T / dS^T buffers and the resident tiles
+            self.pd_free = b("pd_free", 2 if dq_counted else 1)
+            self.res_empty = b("res_empty", 2)
+            self.dq_full, self.dq_free = b("dq_full"), b("dq_free")
+        self.dq_done = 0   # fused: dQ products issued
 
     def p_full_dq(self, g: int):
         """The barrier and phase that carry step g's P / dS in the pipelined dQ pass."""
@@ -147,6 +165,8 @@ def compute_pipe(c: CTA, q: Pass, tiles, pd_wait: bool = True):
             c.sd_free.arrive()
             if q.kv and pd_wait and g > 0:
                 yield wait(c.pd_free, g - 1)
+            if q.fused and c.dq_done < g:   # about to overwrite dS^T, which dQ of step g - 1 reads
+                raise Race(f"dS^T of step {g} written before the dQ product of step {g - 1}")
             if q.kv:
                 c.p_full.arrive()
             else:
@@ -155,6 +175,32 @@ def compute_pipe(c: CTA, q: Pass, tiles, pd_wait: bool = True):
         yield wait(c.acc_full, done)
         c.acc_free.arrive()
         done += 1
+
+
+def dq_mma(c: CTA, q: Pass, tiles):
+    g = t = 0
+    for n in tiles:
+        yield wait(c.res_full, t)
+        for j in range(n):
+            yield wait(c.p_full, g)
+            if g > 0:
+                yield wait(c.dq_free, g - 1)
+            c.dq_done += 1
+            c.dq_full.arrive()
+            c.pd_free.arrive()
+            if j == n - 1:
+                c.res_empty.arrive()
+            g += 1
+        t += 1
+
+
+def dq_out(c: CTA, tiles):
+    g = 0
+    for n in tiles:
+        for _ in range(n):
+            yield wait(c.dq_full, g)
+            c.dq_free.arrive()
+            g += 1
 
 
 def mma_serial(c: CTA, q: Pass, tiles):
@@ -188,12 +234,15 @@ def compute_serial(c: CTA, q: Pass, tiles):
         done += 1
 
 
-def run(name: str, tiles, seed: int, alternate_p_full: bool = True, pd_wait: bool = True) -> str:
+def run(name: str, tiles, seed: int, alternate_p_full: bool = True, pd_wait: bool = True,
+        dq_counted: bool = True) -> str:
     q = PASSES[name]
-    c = CTA(q, alternate_p_full)
+    c = CTA(q, alternate_p_full, dq_counted)
     roles = [loader(c, q, tiles)]
     if q.pipeline:
         roles += [mma_pipe(c, q, tiles)] + [compute_pipe(c, q, tiles, pd_wait) for _ in range(COMPUTE)]
+        if q.fused:
+            roles += [dq_mma(c, q, tiles), dq_out(c, tiles)]
     else:
         roles += [mma_serial(c, q, tiles)] + [compute_serial(c, q, tiles) for _ in range(COMPUTE)]
     blocked = [None] * len(roles)
@@ -222,6 +271,8 @@ def run(name: str, tiles, seed: int, alternate_p_full: bool = True, pd_wait: boo
                 blocked[i] = None
     except Aliased:
         return "aliased"
+    except Race:
+        return "race"
     return "done"
 
 
@@ -248,6 +299,14 @@ def test_pipelined_kv_pass_needs_the_pd_free_wait():
     same lost phase appears."""
     outcomes = {run("d64_kv", [5, 3], seed, pd_wait=False) for seed in range(200)}
     assert "aliased" in outcomes, outcomes
+
+
+def test_fused_pass_needs_pd_free_to_count_the_dq_warp():
+    """The fused pass's pin: with pd_free completed by the first MMA warp
+    alone, the compute warps can overwrite dS^T before the dQ product of the
+    previous step was issued."""
+    outcomes = {run("d64_fused", [5, 3], seed, dq_counted=False) for seed in range(300)}
+    assert "race" in outcomes, outcomes
 
 
 def test_model_matches_the_kernel_constants(kernel_constants):
