@@ -65,8 +65,11 @@ def decode_timings(steps: int, dev, stream, flush, hbm_gbs: float) -> dict:
     the launching stream, L2 flushed before each call) and the K/V bandwidth
     it implies, against the measured HBM copy rate.  The same calls are also
     timed back to back without the flush (``us_mean_no_flush``): their K/V
-    (0.5-1 GB) is larger than L2 either way, so the difference is the cost of
-    starting each call with the kernel's code and scheduling data cold."""
+    (0.5-1 GB, 4-8x the 129 MB L2) is larger than L2 either way, which the
+    timing rules accept in place of a flush.  The difference is the cost of
+    starting each call with the kernel's code and scheduling data cold, and of
+    writing back the dirty lines the flush leaves in L2 (up to its 129 MB)
+    while the call streams its K/V."""
     import torch
     from exact_attention_10_gb300 import fa
     out = {"dtype": "bf16", "schedule": "auto", "l2": "flushed between calls", "steps": steps, "shapes": []}
