@@ -4,6 +4,7 @@
 #include "fa_bwd_launch.h"
 
 #include <mutex>
+#include <utility>
 
 #include "fa_bwd_kernel.cuh"
 
@@ -12,6 +13,26 @@ namespace fa_launch {
 namespace {
 
 constexpr int kMaxDev = 64;
+
+// Launch `kern` on `stream` allowing programmatic dependent launch: it may
+// start while the previous kernel on the stream finishes, and waits for that
+// kernel's completion with griddepcontrol.wait before reading its results.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args &&...args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 template <int D, bool BF16, bool CAUSAL, bool KV, bool FQ = false>
 fa_status launch_pass(const CUtensorMap &r0, const CUtensorMap &r1, const CUtensorMap &s0, const CUtensorMap &s1,
@@ -33,7 +54,15 @@ fa_status launch_pass(const CUtensorMap &r0, const CUtensorMap &r1, const CUtens
             attr_set[dev] = true;
         }
     }
-    kern<<<grid, FQ ? fa::bwd::kThreadsFused : fa::bwd::kThreads, smem, stream>>>(r0, r1, s0, s1, dq, p);
+    if (FQ) {   // right behind the pre-pass (programmatic dependent launch): see fa_bwd_sm103
+        if (launch_dependent(kern, dim3(grid), dim3(fa::bwd::kThreadsFused), smem, stream, r0, r1, s0, s1, dq, p) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_CUDA;
+        }
+        return FA_OK;
+    }
+    kern<<<grid, fa::bwd::kThreads, smem, stream>>>(r0, r1, s0, s1, dq, p);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
     return FA_OK;
@@ -76,9 +105,13 @@ fa_status launch_all(const BwdLaunch &a, cudaStream_t s, int dev)
             if (st != FA_OK)
                 return st;
             const long long elems = (long long)a.BH * a.N * D;
-            fa::bwd::fa_bwd_dq_convert<BF16><<<(unsigned)((elems / 8 + 255) / 256), 256, 0, s>>>(
-                a.dqa, static_cast<uint16_t *>(a.dQ), a.N, a.Npad, D, elems, a.scale);
-            return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+            if (launch_dependent(fa::bwd::fa_bwd_dq_convert<BF16>, dim3((unsigned)((elems / 8 + 255) / 256)), dim3(256),
+                                 0, s, (const float *)a.dqa, static_cast<uint16_t *>(a.dQ), a.N, a.Npad, D, elems,
+                                 a.scale) != cudaSuccess) {
+                cudaGetLastError();
+                return FA_ERR_CUDA;
+            }
+            return FA_OK;
         }
     }
     p.T = a.BH * p.nqt;

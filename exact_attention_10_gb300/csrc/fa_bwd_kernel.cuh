@@ -350,6 +350,21 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, uint32_t src
                  : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start
+// launching (its blocks still wait for this grid with grid_wait before they
+// read what it wrote); and wait until the previous kernel on the stream has
+// completed and its writes are visible (a no-op when this launch did not
+// allow programmatic serialization).
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Close this thread's bulk async-group operations issued so far into a group.
 __device__ __forceinline__ void bulk_commit_group()
 {
@@ -1015,7 +1030,6 @@ __device__ void bwd_compute_pipe(const Params &p, uint32_t tmem, uint32_t sStage
 
 // ------------------------------------------------------------------ fused pass: dQ
 
-
 // The fused pass's dQ products (warp 10): per step g, once the compute warps
 // have written dS^T_g (p_full) and the read-out warps have loaded the
 // previous product (dq_free), dQ_g = dS_g K into the dQ columns -- A is the
@@ -1224,6 +1238,10 @@ __global__ void __launch_bounds__(FQ ? kThreadsFused : kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc);
+    if (FQ) {   // launched right behind the pre-pass: the set-up above overlaps its end
+        fq::grid_launch_dependents();   // the dQ conversion may start launching
+        fq::grid_wait();                // -lg, -delta and the zeroed accumulator are written
+    }
 
     if (threadIdx.x < kComputeThreads) {
         ptx::regs_increase<FQ ? kRegsComputeFused : kRegsCompute>();
@@ -1270,6 +1288,7 @@ __global__ void __launch_bounds__(256)
     fa_bwd_prep(const uint16_t *O, const uint16_t *dO, const float *LSE, float *lg, float *dl, float *dqa, int N,
                 int Npad, long long rows)
 {
+    fq::grid_launch_dependents();   // the fused pass may start launching behind this kernel
     constexpr int kTpr = D / 8;   // threads per row: 8 or 16, a divisor of 32
     const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long row = g / kTpr;
@@ -1329,6 +1348,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(256)
     fa_bwd_dq_convert(const float *dqa, uint16_t *dQ, int N, int Npad, int D, long long elems, float scale)
 {
+    fq::grid_wait();   // launched right behind the fused pass: its accumulator is complete
     const long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (e >= elems)
         return;
