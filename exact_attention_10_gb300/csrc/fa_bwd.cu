@@ -54,17 +54,12 @@ fa_status launch_pass(const CUtensorMap &r0, const CUtensorMap &r1, const CUtens
             attr_set[dev] = true;
         }
     }
-    if (FQ) {   // right behind the pre-pass (programmatic dependent launch): see fa_bwd_sm103
-        if (launch_dependent(kern, dim3(grid), dim3(fa::bwd::kThreadsFused), smem, stream, r0, r1, s0, s1, dq, p) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return FA_ERR_CUDA;
-        }
-        return FA_OK;
-    }
-    kern<<<grid, fa::bwd::kThreads, smem, stream>>>(r0, r1, s0, s1, dq, p);
-    if (cudaGetLastError() != cudaSuccess)
+    // right behind the previous kernel (programmatic dependent launch): see fa_bwd_sm103
+    if (launch_dependent(kern, dim3(grid), dim3(FQ ? fa::bwd::kThreadsFused : fa::bwd::kThreads), smem, stream, r0, r1,
+                         s0, s1, dq, p) != cudaSuccess) {
+        cudaGetLastError();
         return FA_ERR_CUDA;
+    }
     return FA_OK;
 }
 

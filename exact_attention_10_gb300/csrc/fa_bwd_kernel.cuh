@@ -1238,10 +1238,10 @@ __global__ void __launch_bounds__(FQ ? kThreadsFused : kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc);
-    if (FQ) {   // launched right behind the pre-pass: the set-up above overlaps its end
-        fq::grid_launch_dependents();   // the dQ conversion may start launching
-        fq::grid_wait();                // -lg, -delta and the zeroed accumulator are written
-    }
+    // Launched right behind the previous kernel of the backward (programmatic
+    // dependent launch): the set-up above overlaps its end.
+    fq::grid_launch_dependents();   // the next kernel may start launching
+    fq::grid_wait();                // the previous kernel's results (-lg, -delta, the zeroed accumulator) are written
 
     if (threadIdx.x < kComputeThreads) {
         ptx::regs_increase<FQ ? kRegsComputeFused : kRegsCompute>();
