@@ -45,15 +45,19 @@
 // Warp roles (384 threads): warpgroups 0 and 1 compute (warpgroup h takes
 // columns [64h, 64h + 64) of S and dP for all 128 lanes) and write the
 // accumulators out at the end of a tile; warp 8 is the TMA producer; warp 9
-// issues the MMAs and owns TMEM.
+// issues the MMAs and owns TMEM.  The fused pass has 512: warp 10 issues the
+// dQ products and warps 12-15 read them out (warp 11 idles).
 //
 // Tensor memory (512 columns): S or S^T [0,128), dP or dP^T [128,256), then
 // the accumulators: dV [256, 256+D) and dK [256+D, 256+2D) (KV) or dQ
-// [256, 256+D).  P (KV only) and dS are written as 16-bit pairs over the
-// scores they came from: warpgroup h's 64 columns become 32 columns at
-// 64h within the same region, so neither warpgroup overwrites scores the
-// other still has to read.  MMAs from one thread run in issue order, so the
-// next step's S and dP are issued after the MMAs that read P and dS.
+// [256, 256+D).  Serialized passes (D = 128 dK/dV): P and dS are written as
+// 16-bit pairs over the scores they came from: warpgroup h's 64 columns
+// become 32 columns at 64h within the same region, so neither warpgroup
+// overwrites scores the other still has to read; MMAs from one thread run in
+// issue order, so the next step's S and dP are issued after the MMAs that
+// read P and dS.  Pipelined passes keep P^T and dS^T (or dS) in buffers of
+// their own after the accumulators (kColP, kColDS), and the fused pass puts
+// its dQ product where dS^T would be (kColDQ), dS^T going to shared memory.
 //
 // Every mbarrier wait is bounded as in the forward kernel; on expiry the
 // kernel records the site in the status word, leaves its loops, waits (with a
@@ -332,7 +336,8 @@ __device__ __forceinline__ uint32_t a_col(int kk)
     return (uint32_t)(64 * (kk / 4) + 8 * (kk % 4));
 }
 
-// PTX of the fused pass (bulk tensor reductions, 16-byte shared stores).
+// PTX of the fused pass (bulk tensor reductions, 16-byte shared stores) and
+// of the backward's programmatic dependent launch.
 namespace fq {
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
