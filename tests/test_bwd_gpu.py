@@ -175,15 +175,17 @@ def test_backward_fused_against_two_pass(causal):
         assert bool(((a - b).abs() <= ulp).all()), float(((a - b).abs() / ulp).max())
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_backward_long_sequence(causal):
-    """N = 4096, D = 128 over two heads (32 key tiles per head, every
-    combination of diagonal and full tiles), compared in full."""
-    q, k, v, do = _inputs(1, 2, 4096, 128, "bf16", seed=11)
-    scale = 128 ** -0.5
+def test_backward_long_sequence(causal, D):
+    """N = 4096 over two heads (32 key tiles per head, every combination of
+    diagonal and full tiles), compared in full; at D = 64 the fused pass, whose
+    dQ sums 32 key tiles' products in the fp32 accumulator."""
+    q, k, v, do = _inputs(1, 2, 4096, D, "bf16", seed=11)
+    scale = D ** -0.5
     grads = _gpu_grads(q, k, v, do, causal, scale)
     refs = oracle.backward(q, k, v, do, causal, scale)
-    _check(grads, refs, "bf16", f"N4096 D128 causal={int(causal)}")
+    _check(grads, refs, "bf16", f"N4096 D{D} causal={int(causal)}")
 
 
 BAND = [  # (B, H, Nq, Nkv, D, dtype, (left, right))
