@@ -11,22 +11,31 @@ bwd_compute, bwd_mma_pipe, bwd_compute_pipe):
 * D = 64, fused pass (bwd_mma_dq, bwd_dq_out): the pipelined dK/dV pass plus a
   second MMA warp that issues each step's dQ product once P / dS are written
   and the read-out warps have loaded the previous product, and the read-out
-  warps; pd_free (the P^T / dS^T buffers) and res_empty count both MMA warps.
+  warps; pd_free (the P^T / dS^T buffers) and res_empty (the resident K and
+  V) count both MMA warps.
 
 The producer, the MMA warp and the two compute warpgroups (column halves) are
 coroutines following the kernel's waits, arrivals and commits; barriers keep
 exact phase counts, and a waiter that finds its barrier two phases past the
 one it means (a lost phase: its parity would read as not yet complete) is
-reported.  Copies and commits arrive when issued.  Random interleavings over
+reported.  Copies and commits arrive when issued (in the fused pass's model,
+copies land at a random later time, in any order).  Random interleavings over
 CTAs holding one or several resident tiles of varying length must finish.
+
+The fused pass's model also tracks what each buffer holds (the resident K
+and V, the stages, P^T / dS^T, the accumulators; a buffer holds its tile only
+once its copy has landed) and reports a read of the wrong tile or step, or an
+overwrite before the last read, as a race.
 
 The pin: in the pipelined dQ pass nothing holds the compute warps back from
 finishing step g + 1 before the MMA warp waits for step g, so one p_full
 barrier can run two phases ahead of its waiter; the kernel alternates two
 barriers there, and the model must flag the single-barrier form.  In the
 fused pass, a pd_free that counted only the first MMA warp would let the
-compute warps overwrite dS^T before the dQ product has read it; the model
-flags that race.
+compute warps overwrite dS^T before the dQ product has read it, and a
+res_empty that counted only the first MMA warp would let the next tile's K
+overwrite the resident tile that the last dQ product still reads; the model
+flags both races.
 """
 from __future__ import annotations
 
@@ -80,7 +89,7 @@ def wait(bar: Barrier, k: int):
 
 
 class CTA:
-    def __init__(self, q: Pass, alternate_p_full: bool, dq_counted: bool = True):
+    def __init__(self, q: Pass, alternate_p_full: bool, dq_counted: bool = True, res_dq_counted: bool = True):
         b = Barrier
         self.full = [b(f"full{s}") for s in range(q.ring0)]
         self.empty = [b(f"empty{s}") for s in range(q.ring0)]
@@ -93,9 +102,15 @@ class CTA:
         self.alternate = alternate_p_full
         if q.fused:   # both MMA warps read the P^T / dS^T buffers and the resident tiles
             self.pd_free = b("pd_free", 2 if dq_counted else 1)
-            self.res_empty = b("res_empty", 2)
+            self.res_empty = b("res_empty", 2 if res_dq_counted else 1)
             self.dq_full, self.dq_free = b("dq_full"), b("dq_free")
         self.dq_done = 0   # fused: dQ products issued
+        # fused: what the buffers hold -- the resident K and V (tile), stages
+        # (step); products issued (dV / dK), S and dP loaded and accumulators
+        # read out (tiles), per compute warpgroup
+        self.res, self.stage = None, [None] * q.ring0
+        self.prod_done, self.sd_loaded, self.acc_read = 0, [0] * COMPUTE, [0] * COMPUTE
+        self.inflight = []   # fused: copies issued, not landed: (barrier, buffer setter, value)
 
     def p_full_dq(self, g: int):
         """The barrier and phase that carry step g's P / dS in the pipelined dQ pass."""
@@ -165,8 +180,6 @@ def compute_pipe(c: CTA, q: Pass, tiles, pd_wait: bool = True):
             c.sd_free.arrive()
             if q.kv and pd_wait and g > 0:
                 yield wait(c.pd_free, g - 1)
-            if q.fused and c.dq_done < g:   # about to overwrite dS^T, which dQ of step g - 1 reads
-                raise Race(f"dS^T of step {g} written before the dQ product of step {g - 1}")
             if q.kv:
                 c.p_full.arrive()
             else:
@@ -177,24 +190,103 @@ def compute_pipe(c: CTA, q: Pass, tiles, pd_wait: bool = True):
         done += 1
 
 
-def dq_mma(c: CTA, q: Pass, tiles):
-    g = t = 0
-    for n in tiles:
+def check(ok: bool, what: str):
+    if not ok:
+        raise Race(what)
+
+
+def copy(c: CTA, bar: Barrier, setter, value):
+    """Issue a copy: its buffer holds nothing usable until it lands (and arrives on `bar`)."""
+    setter(("loading", value))
+    c.inflight.append((bar, setter, value))
+
+
+def loader_fused(c: CTA, q: Pass, tiles):
+    step = 0
+
+    def set_res(v):
+        c.res = v
+
+    def set_stage(i):
+        return lambda v: c.stage.__setitem__(i, v)
+
+    for t, n in enumerate(tiles):
+        if t > 0:
+            yield wait(c.res_empty, t - 1)
+        copy(c, c.res_full, set_res, t)
+        for _ in range(n):
+            yield wait(c.empty[step % q.ring0], step // q.ring0 - 1)
+            copy(c, c.full[step % q.ring0], set_stage(step % q.ring0), step)
+            step += 1
+
+
+def mma_fused(c: CTA, q: Pass, tiles):
+    g = 0
+
+    def issue_sd(gs, t):
+        if gs > 0:
+            yield wait(c.sd_free, gs - 1)
+        yield wait(c.full[gs % q.ring0], gs // q.ring0)
+        check(c.res == t and c.stage[gs % q.ring0] == gs, f"S and dP of step {gs}: K, V or stage not its own")
+        check(min(c.sd_loaded) >= gs, f"S of step {gs} over S of step {gs - 1} before it was loaded")
+        c.sd_full.arrive()
+
+    for t, n in enumerate(tiles):
+        yield wait(c.res_full, t)
+        yield from issue_sd(g, t)
+        for j in range(n):
+            if j + 1 < n:
+                yield from issue_sd(g + 1, t)
+            if j == 0 and t > 0:
+                yield wait(c.acc_free, t - 1)
+            yield wait(c.p_full, g)
+            check(c.stage[g % q.ring0] == g, f"products of step {g}: stage not its own")
+            check(j > 0 or min(c.acc_read) == t, f"tile {t}'s first products before tile {t - 1}'s accumulators were read")
+            c.prod_done += 1
+            c.pd_free.arrive()
+            c.empty[g % q.ring0].arrive()
+            if j == n - 1:
+                c.acc_full.arrive()
+                c.res_empty.arrive()
+            g += 1
+
+
+def compute_fused(c: CTA, q: Pass, tiles, h: int):
+    g = 0
+    for t, n in enumerate(tiles):
+        for _ in range(n):
+            yield wait(c.sd_full, g)
+            c.sd_loaded[h] = g + 1
+            c.sd_free.arrive()
+            if g > 0:
+                yield wait(c.pd_free, g - 1)
+            check(c.dq_done >= g and c.prod_done >= g, f"P^T / dS^T of step {g} written before step {g - 1}'s products")
+            c.p_full.arrive()
+            g += 1
+        yield wait(c.acc_full, t)
+        check(c.prod_done == g, f"tile {t}'s accumulators read before its last products")
+        c.acc_read[h] = t + 1
+        c.acc_free.arrive()
+
+
+def dq_mma_fused(c: CTA, q: Pass, tiles):
+    g = 0
+    for t, n in enumerate(tiles):
         yield wait(c.res_full, t)
         for j in range(n):
             yield wait(c.p_full, g)
             if g > 0:
                 yield wait(c.dq_free, g - 1)
+            check(c.res == t, f"dQ of step {g}: K not tile {t}'s")
             c.dq_done += 1
             c.dq_full.arrive()
             c.pd_free.arrive()
             if j == n - 1:
                 c.res_empty.arrive()
             g += 1
-        t += 1
 
 
-def dq_out(c: CTA, tiles):
+def dq_out_fused(c: CTA, tiles):
     g = 0
     for n in tiles:
         for _ in range(n):
@@ -235,15 +327,16 @@ def compute_serial(c: CTA, q: Pass, tiles):
 
 
 def run(name: str, tiles, seed: int, alternate_p_full: bool = True, pd_wait: bool = True,
-        dq_counted: bool = True) -> str:
+        dq_counted: bool = True, res_dq_counted: bool = True) -> str:
     q = PASSES[name]
-    c = CTA(q, alternate_p_full, dq_counted)
-    roles = [loader(c, q, tiles)]
-    if q.pipeline:
-        roles += [mma_pipe(c, q, tiles)] + [compute_pipe(c, q, tiles, pd_wait) for _ in range(COMPUTE)]
-        if q.fused:
-            roles += [dq_mma(c, q, tiles), dq_out(c, tiles)]
+    c = CTA(q, alternate_p_full, dq_counted, res_dq_counted)
+    if q.fused:
+        roles = [loader_fused(c, q, tiles), mma_fused(c, q, tiles), dq_mma_fused(c, q, tiles), dq_out_fused(c, tiles)]
+        roles += [compute_fused(c, q, tiles, h) for h in range(COMPUTE)]
+    elif q.pipeline:
+        roles = [loader(c, q, tiles), mma_pipe(c, q, tiles)] + [compute_pipe(c, q, tiles, pd_wait) for _ in range(COMPUTE)]
     else:
+        roles = [loader(c, q, tiles)]
         roles += [mma_serial(c, q, tiles)] + [compute_serial(c, q, tiles) for _ in range(COMPUTE)]
     blocked = [None] * len(roles)
     live = set(range(len(roles)))
@@ -261,9 +354,16 @@ def run(name: str, tiles, seed: int, alternate_p_full: bool = True, pd_wait: boo
     try:
         while live:
             runnable = [i for i in live if ready(i)]
+            if c.inflight:   # the copy engine: land one copy in flight
+                runnable.append(-1)
             if not runnable:
                 return "deadlock"
             i = rng.choice(runnable)
+            if i < 0:
+                bar, setter, value = c.inflight.pop(rng.randrange(len(c.inflight)))
+                setter(value)
+                bar.arrive()
+                continue
             try:
                 blocked[i] = next(roles[i])
             except StopIteration:
@@ -306,6 +406,14 @@ def test_fused_pass_needs_pd_free_to_count_the_dq_warp():
     alone, the compute warps can overwrite dS^T before the dQ product of the
     previous step was issued."""
     outcomes = {run("d64_fused", [5, 3], seed, dq_counted=False) for seed in range(300)}
+    assert "race" in outcomes, outcomes
+
+
+def test_fused_pass_needs_res_empty_to_count_the_dq_warp():
+    """With res_empty completed by the first MMA warp's last products alone,
+    the producer can load the next tile's K over this tile's while the dQ
+    product of its last step still has to read it."""
+    outcomes = {run("d64_fused", [3, 4, 3, 2], seed, res_dq_counted=False) for seed in range(400)}
     assert "race" in outcomes, outcomes
 
 
