@@ -50,12 +50,13 @@
 //
 // Tensor memory (512 columns): S or S^T [0,128), dP or dP^T [128,256), then
 // the accumulators: dV [256, 256+D) and dK [256+D, 256+2D) (KV) or dQ
-// [256, 256+D).  Serialized passes (D = 128 dK/dV): P and dS are written as
-// 16-bit pairs over the scores they came from: warpgroup h's 64 columns
-// become 32 columns at 64h within the same region, so neither warpgroup
-// overwrites scores the other still has to read; MMAs from one thread run in
-// issue order, so the next step's S and dP are issued after the MMAs that
-// read P and dS.  Pipelined passes keep P^T and dS^T (or dS) in buffers of
+// [256, 256+D).  The dK/dV pass at D = 128 has no columns left: P and dS are
+// written as 16-bit pairs over the scores they came from (warpgroup h's 64
+// columns become 32 columns at 64h within the same region, so neither
+// warpgroup overwrites scores the other still has to read), and MMAs from one
+// thread run in issue order, so the next step's S follows the dV product
+// that reads P^T and its dP the dK product that reads dS^T (bwd_mma).
+// Pipelined passes keep P^T and dS^T (or dS) in buffers of
 // their own after the accumulators (kColP, kColDS), and the fused pass puts
 // its dQ product where dS^T would be (kColDQ), dS^T going to shared memory.
 //
@@ -202,6 +203,9 @@ struct BBars {
     // waited for step g (nothing else holds them back), and one barrier two
     // phases ahead of its waiter would read as not yet complete.
     __device__ uint32_t p_full_dq(int g) const { return (g & 1) ? at(9) : at(3); }
+    // The serialized dK/dV pass (D = 128) uses the same slot for dP's
+    // completion (MMA -> compute; S's is sd_full).
+    __device__ uint32_t dp_full() const { return at(9); }
     __device__ uint32_t dq_full() const { return at(10); }    // fused: dQ MMA -> read-out warps: the step's dQ product done
     __device__ uint32_t dq_free() const { return at(11); }    // fused: read-out warps -> dQ MMA: dQ product loaded
 };
@@ -477,19 +481,51 @@ __device__ void bwd_load(const CUtensorMap *tmR0, const CUtensorMap *tmR1, const
 
 // ------------------------------------------------------------------ MMA issuer
 
+// The serialized pass (the dK/dV pass at D = 128, where TMEM holds S, dP, dV
+// and dK and nothing else): P^T and dS^T are written over S and dP (16-bit
+// pairs, see the header), so a step's S and dP can only be computed once the
+// previous step's products have read them.  Per step g the MMA warp issues
+// dV_g (reads P^T_g), S_{g+1} (overwrites it), dK_g (reads dS^T_g) and
+// dP_{g+1} (overwrites it): MMAs from one thread run in issue order, so each
+// overwrite follows the read it displaces.  S and dP complete separate
+// barriers (sd_full, dp_full), so the compute warps start on S_{g+1} while
+// dK_g and dP_{g+1} still run.
 template <int D, bool BF16, bool KV>
 __device__ void bwd_mma(const Params &p, bool causal, uint32_t sRes, uint32_t sStage, uint32_t tmem,
                         BBars<D, KV> b, Ctl c)
 {
+    static_assert(KV, "the serialized pass is the dK/dV pass");
     using C = BCfg<D, KV>;
     constexpr uint32_t kIdescSS = instr_desc_f16(BF16, kTile, kTile, false);   // both operands K-major
     constexpr uint32_t kIdescTS = instr_desc_f16(BF16, kTile, D, true);        // B MN-major
     const uint32_t r0_lo = desc_lo(sRes, 16), r1_lo = desc_lo(sRes + C::kTileBytes, 16);
     const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
     const uint32_t tAcc0 = tmem + C::kColAcc0, tAcc1 = tmem + C::kColAcc1;
-    int step = 0, tiles = 0;
-    uint32_t n_p = 0;
+    int g = 0, tiles = 0;
     bool ok = true;
+
+    auto stage_ready = [&](int gs) -> bool {
+        if (!warp_wait(b.full(gs % C::kStages), (uint32_t)(gs / C::kStages) & 1u, c, kSiteBwdSlotFull))
+            return false;
+        ptx::tc_fence_after_sync();
+        return true;
+    };
+    // S^T = K Q^T (or dP^T = V dO^T) of step gs into `col`, then `bar`: K-major
+    // operands advance 32 bytes per k-step inside a 128-byte swizzle row and
+    // one box (16 KB) per 64 columns.
+    auto issue_sd = [&](int gs, uint32_t r_lo, uint32_t s_off, uint32_t col, uint32_t bar) {
+        const uint32_t s_lo = desc_lo(sStage + (uint32_t)((gs % C::kStages) * C::kStageBytes) + s_off, 16);
+        if (ptx::elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)((kk / 4) * (C::kBoxBytes >> 4) + (kk % 4) * 2);
+                ptx::mma_ss(col, desc_from_lo(r_lo + off), desc_from_lo(s_lo + off), kIdescSS, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(bar);
+        }
+        __syncwarp();
+    };
+
     for (int r = 0; ok; ++r) {
         const int t = bwd_tile(r, blockIdx.x, gridDim.x);
         if (t >= p.T)
@@ -499,62 +535,48 @@ __device__ void bwd_mma(const Params &p, bool causal, uint32_t sRes, uint32_t sS
         if (!warp_wait(b.res_full(), (uint32_t)tiles & 1u, c, kSiteBwdResFull))
             break;
         ptx::tc_fence_after_sync();
-        for (int j = 0; j < n; ++j, ++step) {
-            const int st = step % C::kStages;
-            if (!warp_wait(b.full(st), (uint32_t)(step / C::kStages) & 1u, c, kSiteBwdSlotFull)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after_sync();
-            const uint32_t sa = sStage + st * C::kStageBytes;
-            const uint32_t s0_lo = desc_lo(sa, 16), s1_lo = desc_lo(sa + C::kTileBytes, 16);
-            if (ptx::elect_one()) {
-                // S (S^T) = R0 S0^T and dP (dP^T) = R1 S1^T over D / 16 k-steps:
-                // K-major operands advance 32 bytes per step inside a 128-byte
-                // swizzle row and one box (16 KB) per 64 columns.
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk / 4) * (C::kBoxBytes >> 4) + (kk % 4) * 2);
-                    ptx::mma_ss(tS, desc_from_lo(r0_lo + off), desc_from_lo(s0_lo + off), kIdescSS, kk > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk / 4) * (C::kBoxBytes >> 4) + (kk % 4) * 2);
-                    ptx::mma_ss(tDP, desc_from_lo(r1_lo + off), desc_from_lo(s1_lo + off), kIdescSS,
-                                kk > 0 ? 1u : 0u);
-                }
-                ptx::mma_commit(b.sd_full());
-            }
-            __syncwarp();
+        if (!stage_ready(g))
+            break;
+        issue_sd(g, r0_lo, 0u, tS, b.sd_full());
+        issue_sd(g, r1_lo, (uint32_t)C::kTileBytes, tDP, b.dp_full());
+        for (int j = 0; j < n; ++j, ++g) {
             if (j == 0 && tiles > 0 &&   // the accumulators are overwritten: the previous tile's were read
                 !warp_wait(b.acc_free(), (uint32_t)(tiles - 1) & 1u, c, kSiteBwdAccFree)) {
                 ok = false;
                 break;
             }
-            if (!warp_wait(b.p_full(), n_p & 1u, c, kSiteBwdPFull)) {
+            if (!warp_wait(b.p_full(), (uint32_t)g & 1u, c, kSiteBwdPFull)) {
                 ok = false;
                 break;
             }
-            ++n_p;
             ptx::tc_fence_after_sync();
-            // KV:  dV += P^T dO (P^T in the S columns), dK += dS^T Q (dS^T in the dP columns)
-            // dQ:  dQ += dS K (dS in the S columns)
-            // The 16-bit A operand comes from TMEM, 8 columns per 16 rows of the
-            // streamed tile; the B operand is the streamed tile read MN-major
-            // (16 rows = 2 KB per k-step, leading byte offset = the box stride).
-            const uint32_t m0_lo = desc_lo(sa + (KV ? C::kTileBytes : 0), C::kBoxBytes);   // KV: dO; dQ: K
-            const uint32_t m1_lo = desc_lo(sa, C::kBoxBytes);                               // KV: Q
+            // dV += P^T dO, dK += dS^T Q: the 16-bit A operand from TMEM, 8 columns
+            // per 16 rows of the streamed tile; the B operand the streamed tile
+            // read MN-major (16 rows = 2 KB per k-step, leading byte offset = the
+            // box stride).
+            const int st = g % C::kStages;
+            const uint32_t sa = sStage + (uint32_t)(st * C::kStageBytes);
+            const uint32_t m0_lo = desc_lo(sa + C::kTileBytes, C::kBoxBytes);   // dO
+            const uint32_t m1_lo = desc_lo(sa, C::kBoxBytes);                   // Q
             if (ptx::elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
                     ptx::mma_ts(tAcc0, tS + a_col(kk), desc_from_lo(m0_lo + kk * (2048 >> 4)), kIdescTS,
                                 (j > 0 || kk > 0) ? 1u : 0u);
-                if (KV) {
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        ptx::mma_ts(tAcc1, tDP + a_col(kk), desc_from_lo(m1_lo + kk * (2048 >> 4)), kIdescTS,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            __syncwarp();
+            if (j + 1 < n) {   // S_{g+1} over P^T_g, behind dV_g
+                if (!stage_ready(g + 1)) {
+                    ok = false;
+                    break;
                 }
+                issue_sd(g + 1, r0_lo, 0u, tS, b.sd_full());
+            }
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    ptx::mma_ts(tAcc1, tDP + a_col(kk), desc_from_lo(m1_lo + kk * (2048 >> 4)), kIdescTS,
+                                (j > 0 || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(b.empty(st));
                 if (j == n - 1) {
                     ptx::mma_commit(b.acc_full());
@@ -562,6 +584,8 @@ __device__ void bwd_mma(const Params &p, bool causal, uint32_t sRes, uint32_t sS
                 }
             }
             __syncwarp();
+            if (j + 1 < n)   // dP_{g+1} over dS^T_g, behind dK_g
+                issue_sd(g + 1, r1_lo, (uint32_t)C::kTileBytes, tDP, b.dp_full());
         }
         ++tiles;
     }
@@ -591,15 +615,22 @@ __device__ __forceinline__ void store_row32(void *dst, const uint32_t (&v)[32], 
         ptx::st_global_v4(d4 + q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 
+// The serialized pass's compute warps: per step, S (sd_full): P^T = exp2(S^T
+// s log2 e - lg) over this warpgroup's 64 columns of S; then dP (dp_full):
+// dS^T = P^T (dP^T - delta) over its 64 columns of dP.  Each is written as
+// 32 columns of 16-bit pairs at the start of the columns it came from, once
+// this thread has loaded them.
 template <int D, bool BF16, bool CAUSAL, bool KV>
 __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBars<D, KV> b, Ctl c)
 {
+    static_assert(KV, "the serialized pass is the dK/dV pass");
     using C = BCfg<D, KV>;
     const int h = threadIdx.x / 128;                // column half of S and dP
     const int warp = threadIdx.x / 32;
     const int lane_row = (warp % 4) * 32 + threadIdx.x % 32;   // TMEM lane = row of the resident tile
     const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
-    const uint32_t tS = tmem + C::kColS + lane_off, tDP = tmem + C::kColDP + lane_off;
+    const uint32_t tS = tmem + C::kColS + lane_off + 64 * h, tDP = tmem + C::kColDP + lane_off + 64 * h;
+    const uint64_t qk2 = ptx::f2_pack(p.qk2, p.qk2);
     int step = 0, tiles = 0;
     for (int r = 0;; ++r) {
         const int t = bwd_tile(r, blockIdx.x, gridDim.x);
@@ -607,91 +638,79 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
             break;
         int bh, rt, s0, n;
         bwd_decode<KV>(p, CAUSAL, t, bh, rt, s0, n);
-        // dQ pass: this thread's query row has one -lg and -delta for the tile.
-        float lg_row = 0.f, dl_row = 0.f;
-        if (!KV) {
-            const size_t off = (size_t)bh * p.Npad + (size_t)rt * kTile + lane_row;
-            lg_row = p.lg[off];
-            dl_row = p.dl[off];
-        }
         for (int j = 0; j < n; ++j, ++step) {
             const int st = step % C::kStages;
-            const int si = s0 + j;   // streamed tile index
+            const int si = s0 + j;   // streamed (query) tile index
             if (!warp_wait(b.sd_full(), (uint32_t)step & 1u, c, kSiteBwdSdFull))
                 return;
             ptx::tc_fence_after_sync();
-            const uint32_t vec = sStage + st * C::kStageBytes + 2 * C::kTileBytes;   // KV: lg[128], delta[128]
-            // Masks: the band's edges (the causal diagonal) and, in the dQ
-            // pass, keys past Nkv in the last key tile.  (Padding queries and
-            // queries without keys have lg = +inf (stored as -lg = -inf), so their P is already 0.)
-            const StepMask sm = bwd_step_mask(p, CAUSAL, KV ? rt : si, KV ? si : rt);
-            const int key_limit = KV ? kTile : p.Nkv - si * kTile;  // dQ pass: columns >= key_limit are past Nkv
-            const bool masked = !sm.whole || key_limit < kTile;     // warp-uniform
-            const uint64_t qk2 = ptx::f2_pack(p.qk2, p.qk2);
+            const uint32_t vec = sStage + st * C::kStageBytes + 2 * C::kTileBytes;   // lg[128], delta[128]
+            // Masks: the band's edges (the causal diagonal); padding queries
+            // and queries without keys have lg = +inf (stored as -lg = -inf),
+            // so their P is already 0.
+            const StepMask sm = bwd_step_mask(p, CAUSAL, rt, si);
+            const bool masked = !sm.whole;   // warp-uniform
+            uint32_t pv[64];   // S, then P (fp32)
+            ptx::tmem_ld64(tS, pv);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 64; i += 4) {
+                const float4 lg4 = ptx::ld_shared_v4f32(vec + (uint32_t)(64 * h + i) * 4);   // -lg of four queries
+                float x[4];
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), qk2,
+                                           ptx::f2_pack(lg4.x, lg4.y)),
+                               x[0], x[1]);
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(pv[i + 2]), __uint_as_float(pv[i + 3])), qk2,
+                                           ptx::f2_pack(lg4.z, lg4.w)),
+                               x[2], x[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    pv[i + e] = __float_as_uint(ptx::ex2(x[e]));
+            }
+            if (masked) {   // lane = key, column = query
+                const LaneMask lm = bwd_lane_mask<KV>(sm, lane_row, kTile);
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    pv[i] = ((uint32_t)(lm.a + 64 * h + i) < lm.width) ? pv[i] : 0u;
+            }
+            {   // P^T over the first 32 of this warpgroup's S columns
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    pk[i] = BF16 ? ptx::pack_bf16x2(__uint_as_float(pv[2 * i]), __uint_as_float(pv[2 * i + 1]))
+                                 : ptx::pack_f16x2(__uint_as_float(pv[2 * i]), __uint_as_float(pv[2 * i + 1]));
+                ptx::tmem_st32(tS, pk);
+            }
+            if (!warp_wait(b.dp_full(), (uint32_t)step & 1u, c, kSiteBwdSdFull))
+                return;
+            ptx::tc_fence_after_sync();
+            // dS^T over the first 32 of this warpgroup's dP columns, in two
+            // halves of 32 dP columns each (all of this thread's dP columns are
+            // loaded before any is overwritten).
+            uint32_t dv[2][32];
+            ptx::tmem_ld32(tDP, dv[0]);
+            ptx::tmem_ld32(tDP + 32, dv[1]);
+            ptx::tmem_wait_ld();
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
-                const int c0 = 64 * h + 32 * ch;   // first column of this chunk
-                uint32_t sv[32], dv[32];
-                ptx::tmem_ld32(tS + c0, sv);        // S and dP of the chunk, one wait
-                ptx::tmem_ld32(tDP + c0, dv);
-                ptx::tmem_wait_ld();
-                float pr[32];
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    uint64_t nl01, nl23;   // -lg for the four columns, as pairs
-                    if (KV) {
-                        const float4 lg4 = ptx::ld_shared_v4f32(vec + (uint32_t)(c0 + i) * 4);
-                        nl01 = ptx::f2_pack(lg4.x, lg4.y);
-                        nl23 = ptx::f2_pack(lg4.z, lg4.w);
-                    } else {
-                        nl01 = nl23 = ptx::f2_pack(lg_row, lg_row);
-                    }
-                    float x[4];
-                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), qk2, nl01),
-                                   x[0], x[1]);
-                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), qk2,
-                                               nl23),
-                                   x[2], x[3]);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        pr[i + e] = ptx::ex2(x[e]);
-                }
-                if (masked) {   // KV: lane = key, column = query; dQ pass: lane = query, column = key
-                    const LaneMask lm = bwd_lane_mask<KV>(sm, lane_row, key_limit);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        pr[i] = ((uint32_t)(lm.a + c0 + i) < lm.width) ? pr[i] : 0.f;
-                }
-                if (KV) {   // P^T, 16-bit pairs, over this chunk's first 16 columns
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[i] = BF16 ? ptx::pack_bf16x2(pr[2 * i], pr[2 * i + 1]) : ptx::pack_f16x2(pr[2 * i], pr[2 * i + 1]);
-                    tmem_st16(tS + 64 * h + 16 * ch, pk);
-                }
                 uint32_t dk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
-                    uint64_t nd01, nd23;   // -delta, as pairs
-                    if (KV) {
-                        const float4 d4 = ptx::ld_shared_v4f32(vec + kTile * 4 + (uint32_t)(c0 + i) * 4);
-                        nd01 = ptx::f2_pack(d4.x, d4.y);
-                        nd23 = ptx::f2_pack(d4.z, d4.w);
-                    } else {
-                        nd01 = nd23 = ptx::f2_pack(dl_row, dl_row);
-                    }
+                    const int q = 32 * ch + i;   // this warpgroup's column
+                    const float4 d4 = ptx::ld_shared_v4f32(vec + kTile * 4 + (uint32_t)(64 * h + q) * 4);   // -delta
                     float ds[4];
-                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(pr[i], pr[i + 1]),
-                                               ptx::f2_add(ptx::f2_pack(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), nd01)),
+                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(pv[q]), __uint_as_float(pv[q + 1])),
+                                               ptx::f2_add(ptx::f2_pack(__uint_as_float(dv[ch][i]), __uint_as_float(dv[ch][i + 1])),
+                                                           ptx::f2_pack(d4.x, d4.y))),
                                    ds[0], ds[1]);
-                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(pr[i + 2], pr[i + 3]),
-                                               ptx::f2_add(ptx::f2_pack(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), nd23)),
+                    ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(pv[q + 2]), __uint_as_float(pv[q + 3])),
+                                               ptx::f2_add(ptx::f2_pack(__uint_as_float(dv[ch][i + 2]), __uint_as_float(dv[ch][i + 3])),
+                                                           ptx::f2_pack(d4.z, d4.w))),
                                    ds[2], ds[3]);
                     dk[i / 2] = BF16 ? ptx::pack_bf16x2(ds[0], ds[1]) : ptx::pack_f16x2(ds[0], ds[1]);
                     dk[i / 2 + 1] = BF16 ? ptx::pack_bf16x2(ds[2], ds[3]) : ptx::pack_f16x2(ds[2], ds[3]);
                 }
-                // dS (dS^T): KV over the dP columns, dQ pass over the S columns
-                tmem_st16((KV ? tDP : tS) + 64 * h + 16 * ch, dk);
+                tmem_st16(tDP + 16 * ch, dk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
@@ -737,13 +756,14 @@ __device__ void bwd_compute(const Params &p, uint32_t tmem, uint32_t sStage, BBa
 
 // ------------------------------------------------------------------ dQ pass, pipelined
 
-// Pipelined at D = 64 only.  The pipelined order wants S_{g+2} right after
-// the products of step g, and stage g + 2 can only be loaded once they have
-// released stage g; with the two stages that fit beside the resident tiles at
-// D = 128 that load is exposed on every step (measured on the dQ pass: 892 ->
-// 840 TFLOP/s at N = 16384), and the KV pass has no TMEM left for separate
-// P^T / dS^T buffers at D = 128; so D = 128 keeps the serialized step
-// (S and dP, compute, accumulating products).
+// Pipelined: D = 64, and the dQ pass at D = 128 (K and V in rings of their
+// own).  The pipelined order wants S_{g+2} right after the products of step
+// g, and stage g + 2 can only be loaded once they have released stage g; with
+// the two stages of both tiles that fit beside the resident tiles at D = 128
+// that load was exposed on every step (measured on the dQ pass: 892 -> 840
+// TFLOP/s at N = 16384).  The dK/dV pass at D = 128 has no TMEM left for
+// separate P^T / dS^T buffers and keeps them over S and dP (bwd_mma,
+// bwd_compute).
 template <int D, bool KV>
 constexpr bool kPipeline = (D == 64) || (!KV && D == 128);
 
@@ -1219,7 +1239,7 @@ __global__ void __launch_bounds__(FQ ? kThreadsFused : kThreads, 1)
         ptx::mbar_init(b.drain(), FQ ? 2 : 1);
         ptx::mbar_init(b.sd_free(), kComputeThreads);
         ptx::mbar_init(b.pd_free(), FQ ? 2 : 1);
-        ptx::mbar_init(b.p_full_dq(1), kComputeThreads);
+        ptx::mbar_init(b.p_full_dq(1), KV ? 1 : kComputeThreads);   // KV: dp_full, committed by the MMA warp
         if (FQ) {
             ptx::mbar_init(b.dq_full(), 1);
             ptx::mbar_init(b.dq_free(), 128);

@@ -6,8 +6,11 @@ bwd_compute, bwd_mma_pipe, bwd_compute_pipe):
   compute warps have loaded S_g and dP_g), three stages of both streamed tiles;
 * D = 128, dQ pass: pipelined, K and V in separate rings of three and two
   slots, V's slot freed once dP is computed;
-* D = 128, dK/dV pass: not pipelined (P^T and dS^T overwrite S and dP, and the
-  next S follows the products in issue order), two stages;
+* D = 128, dK/dV pass: P^T and dS^T overwrite S and dP, two stages; per step
+  the MMA warp issues dV_g, S_{g+1}, dK_g, dP_{g+1} (each overwrite after the
+  read it displaces, in issue order), S and dP completing separate barriers
+  (sd_full, dp_full) so that the compute warps start on S_{g+1} while dK_g and
+  dP_{g+1} still run;
 * D = 64, fused pass (bwd_mma_dq, bwd_dq_out): the pipelined dK/dV pass plus a
   second MMA warp that issues each step's dQ product once P / dS are written
   and the read-out warps have loaded the previous product, and the read-out
@@ -22,9 +25,10 @@ reported.  Copies and commits arrive when issued (in the fused pass's model,
 copies land at a random later time, in any order).  Random interleavings over
 CTAs holding one or several resident tiles of varying length must finish.
 
-The fused pass's model also tracks what each buffer holds (the resident K
-and V, the stages, P^T / dS^T, the accumulators; a buffer holds its tile only
-once its copy has landed) and reports a read of the wrong tile or step, or an
+The models of the fused pass and of the D = 128 dK/dV pass also track what
+each buffer holds (the resident K and V, the stages, S / P^T and dP / dS^T
+per column half, the accumulators; a buffer holds its tile only once its
+copy has landed) and report a read of the wrong tile or step, or an
 overwrite before the last read, as a race.
 
 The pin: in the pipelined dQ pass nothing holds the compute warps back from
@@ -35,7 +39,8 @@ fused pass, a pd_free that counted only the first MMA warp would let the
 compute warps overwrite dS^T before the dQ product has read it, and a
 res_empty that counted only the first MMA warp would let the next tile's K
 overwrite the resident tile that the last dQ product still reads; the model
-flags both races.
+flags both races; and in the D = 128 dK/dV pass, dP_{g+1} issued ahead of
+dK_g would overwrite dS^T_g before dK_g reads it.
 """
 from __future__ import annotations
 
@@ -109,6 +114,8 @@ class CTA:
         # (step); products issued (dV / dK), S and dP loaded and accumulators
         # read out (tiles), per compute warpgroup
         self.res, self.stage = None, [None] * q.ring0
+        self.dp_full = Barrier("dp_full")   # D = 128 dK/dV pass: dP of a step ready (S's: sd_full)
+        self.s_reg, self.dp_reg = [None] * COMPUTE, [None] * COMPUTE   # (what, step) per column half
         self.prod_done, self.sd_loaded, self.acc_read = 0, [0] * COMPUTE, [0] * COMPUTE
         self.inflight = []   # fused: copies issued, not landed: (barrier, buffer setter, value)
 
@@ -295,39 +302,76 @@ def dq_out_fused(c: CTA, tiles):
             g += 1
 
 
-def mma_serial(c: CTA, q: Pass, tiles):
-    step = done = n_p = 0
-    for n in tiles:
-        yield wait(c.res_full, done)
+def mma_serial(c: CTA, q: Pass, tiles, dp_before_dk: bool = False):
+    g = 0
+
+    def issue_s(gs, t):
+        check(c.res == t and c.stage[gs % q.ring0] == gs, f"S of step {gs}: K or stage not its own")
+        for h in range(COMPUTE):   # the previous S was loaded (and P^T written over it and read by dV)
+            check(c.s_reg[h] in (None, ("pt", gs - 1)), f"S of step {gs} over {c.s_reg[h]}")
+            c.s_reg[h] = ("s", gs)
+        c.sd_full.arrive()
+
+    def issue_dp(gs, t):
+        check(c.res == t and c.stage[gs % q.ring0] == gs, f"dP of step {gs}: V or stage not its own")
+        for h in range(COMPUTE):   # dS^T of the previous step was read by dK
+            check(c.dp_reg[h] in (None, ("read", gs - 1)), f"dP of step {gs} over {c.dp_reg[h]}")
+            c.dp_reg[h] = ("dp", gs)
+        c.dp_full.arrive()
+
+    for t, n in enumerate(tiles):
+        yield wait(c.res_full, t)
+        yield wait(c.full[g % q.ring0], g // q.ring0)
+        issue_s(g, t)
+        yield None   # (the tensor pipe takes time: others may run between two issues)
+        issue_dp(g, t)
         for j in range(n):
-            yield wait(c.full[step % q.ring0], step // q.ring0)
-            c.sd_full.arrive()
-            if j == 0 and done > 0:
-                yield wait(c.acc_free, done - 1)
-            yield wait(c.p_full, n_p)
-            n_p += 1
-            c.empty[step % q.ring0].arrive()
+            if j == 0 and t > 0:
+                yield wait(c.acc_free, t - 1)
+            yield wait(c.p_full, g)
+            check(c.stage[g % q.ring0] == g, f"products of step {g}: stage not its own")
+            check(j > 0 or min(c.acc_read) == t, f"tile {t}'s first products before tile {t - 1}'s accumulators were read")
+            for h in range(COMPUTE):   # dV_g reads P^T_g
+                check(c.s_reg[h] == ("pt", g), f"dV of step {g} reads {c.s_reg[h]}")
+            if j + 1 < n:
+                yield wait(c.full[(g + 1) % q.ring0], (g + 1) // q.ring0)
+                issue_s(g + 1, t)
+                yield None
+                if dp_before_dk:
+                    issue_dp(g + 1, t)
+            for h in range(COMPUTE):   # dK_g reads dS^T_g
+                check(c.dp_reg[h] == ("dst", g), f"dK of step {g} reads {c.dp_reg[h]}")
+                c.dp_reg[h] = ("read", g)
+            c.prod_done += 1
+            c.empty[g % q.ring0].arrive()
             if j == n - 1:
                 c.acc_full.arrive()
                 c.res_empty.arrive()
-            step += 1
-        done += 1
+            if j + 1 < n and not dp_before_dk:
+                issue_dp(g + 1, t)
+            g += 1
 
 
-def compute_serial(c: CTA, q: Pass, tiles):
-    step = done = 0
-    for n in tiles:
+def compute_serial(c: CTA, q: Pass, tiles, h: int):
+    g = 0
+    for t, n in enumerate(tiles):
         for _ in range(n):
-            yield wait(c.sd_full, step)
+            yield wait(c.sd_full, g)
+            check(c.s_reg[h] == ("s", g), f"step {g} loads {c.s_reg[h]} for S")
+            c.s_reg[h] = ("pt", g)     # S loaded, P^T written over it
+            yield wait(c.dp_full, g)
+            check(c.dp_reg[h] == ("dp", g), f"step {g} loads {c.dp_reg[h]} for dP")
+            c.dp_reg[h] = ("dst", g)   # dP loaded, dS^T written over it
             c.p_full.arrive()
-            step += 1
-        yield wait(c.acc_full, done)
+            g += 1
+        yield wait(c.acc_full, t)
+        check(c.prod_done == g, f"tile {t}'s accumulators read before its last products")
+        c.acc_read[h] = t + 1
         c.acc_free.arrive()
-        done += 1
 
 
 def run(name: str, tiles, seed: int, alternate_p_full: bool = True, pd_wait: bool = True,
-        dq_counted: bool = True, res_dq_counted: bool = True) -> str:
+        dq_counted: bool = True, res_dq_counted: bool = True, dp_before_dk: bool = False) -> str:
     q = PASSES[name]
     c = CTA(q, alternate_p_full, dq_counted, res_dq_counted)
     if q.fused:
@@ -336,8 +380,8 @@ def run(name: str, tiles, seed: int, alternate_p_full: bool = True, pd_wait: boo
     elif q.pipeline:
         roles = [loader(c, q, tiles), mma_pipe(c, q, tiles)] + [compute_pipe(c, q, tiles, pd_wait) for _ in range(COMPUTE)]
     else:
-        roles = [loader(c, q, tiles)]
-        roles += [mma_serial(c, q, tiles)] + [compute_serial(c, q, tiles) for _ in range(COMPUTE)]
+        roles = [loader_fused(c, q, tiles), mma_serial(c, q, tiles, dp_before_dk)]
+        roles += [compute_serial(c, q, tiles, h) for h in range(COMPUTE)]
     blocked = [None] * len(roles)
     live = set(range(len(roles)))
     rng = random.Random(seed)
@@ -414,6 +458,12 @@ def test_fused_pass_needs_res_empty_to_count_the_dq_warp():
     the producer can load the next tile's K over this tile's while the dQ
     product of its last step still has to read it."""
     outcomes = {run("d64_fused", [3, 4, 3, 2], seed, res_dq_counted=False) for seed in range(400)}
+    assert "race" in outcomes, outcomes
+
+
+def test_d128_kv_pass_needs_dk_before_the_next_dp():
+    """dS^T_g sits in dP's columns: the next step's dP may only follow dK_g."""
+    outcomes = {run("d128_kv", [4, 3], seed, dp_before_dk=True) for seed in range(100)}
     assert "race" in outcomes, outcomes
 
 
