@@ -6,8 +6,8 @@ attention of the same Q, K, V.  Errors are measured normwise per gradient,
 ||g - g_ref|| / ||g_ref||, and row by row: each row's largest element error
 against that row's own largest reference element plus the gradient's RMS
 (see BOUNDS).  Cases cover D = 64 and 128, bf16 and fp16,
-causal and not, one and several 128-row tiles, ragged lengths, N = 1, and a
-4096-row sequence compared in full.
+causal and not, one and several 128-row tiles, ragged lengths, N = 1, a
+4096-row sequence compared in full, and CTAs that run several key tiles.
 """
 from __future__ import annotations
 
@@ -186,6 +186,24 @@ def test_backward_long_sequence(causal, D):
     grads = _gpu_grads(q, k, v, do, causal, scale)
     refs = oracle.backward(q, k, v, do, causal, scale)
     _check(grads, refs, "bf16", f"N4096 D{D} causal={int(causal)}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_several_tiles_per_cta(causal, D):
+    """B4 H16 N1024: 512 key tiles over the SMs, so every CTA runs several
+    (of uneven length when causal) and the passes' hand-over from one key tile
+    to the next -- the resident tiles reloaded, the accumulators read out and
+    restarted, the next tile's first S and dP -- is exercised on every CTA.
+    Four heads spread over the batch are compared in full."""
+    B, H, N = 4, 16, 1024
+    q, k, v, do = _inputs(B, H, N, D, "bf16", seed=23)
+    scale = D ** -0.5
+    grads = _gpu_grads(q, k, v, do, causal, scale)
+    for b, h in ((0, 0), (1, 5), (2, 10), (3, 15)):
+        sl = lambda x: x[b:b + 1, h:h + 1]
+        refs = oracle.backward(sl(q), sl(k), sl(v), sl(do), causal, scale)
+        _check(tuple(sl(g) for g in grads), refs, "bf16", f"B4 H16 N1024 D{D} causal={int(causal)} b{b} h{h}")
 
 
 BAND = [  # (B, H, Nq, Nkv, D, dtype, (left, right))
