@@ -150,7 +150,8 @@ struct BCfg {
     static constexpr int kDqBoxBytes = kTile * 128;   // [128 rows, 32 fp32 columns]
     static constexpr int kBarOff = kSplitRing ? kRing1Off + kRing1 * kTileBytes : kDqOff + (FQ ? kTile * D * 4 : 0);
     // full/empty per slot (unified stages, or ring 0 then ring 1), then res_full, res_empty,
-    // sd_full, p_full, acc_full, acc_free, drain, sd_free, pd_free, p_full_odd; fused: dq_full, dq_free
+    // sd_full, p_full, acc_full, acc_free, drain, sd_free, pd_free, p_full_odd (dQ pass) or dp_full
+    // (the dK/dV pass at D = 128); fused: dq_full, dq_free
     static constexpr int kRingBars = kSplitRing ? 2 * (kRing0 + kRing1) : 2 * kStages;
     static constexpr int kNumBars = kRingBars + 10 + (FQ ? 2 : 0);
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;           // TMEM address, abort flag
