@@ -811,7 +811,7 @@ __device__ void bwd_mma_pipe(const Params &p, bool causal, uint32_t sRes, uint32
     // S_g = R0 S0_g^T and dP_g = R1 S1_g^T into their columns (the previous
     // step's S and dP must have been loaded by the compute warps).
     auto issue_sd = [&](int gs) -> bool {
-        if (C::kSplitRing) {   // (the dQ pass at D = 128: measured 3-4 % faster; mixed at D = 64)
+        if (C::kSplitRing) {   // the dQ pass at D = 128 (measured 1.4-4 % faster; neutral in the fused pass)
             if (!warp_wait_all(b.sd_free(), (uint32_t)(gs - 1) & 1u, gs > 0, b.full(gs % C::kRing0),
                                (uint32_t)(gs / C::kRing0) & 1u, true, b.full1(gs % C::kRing1),
                                (uint32_t)(gs / C::kRing1) & 1u, true, c, kSiteBwdSlotFull))
